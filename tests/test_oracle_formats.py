@@ -1,0 +1,152 @@
+"""Pins for the oracle's half conversion, block sizes and block decoders.
+
+Each check compares the oracle against something other than itself: the IEEE
+binary16 definition (via numpy's independent float16 conversion and hand
+values), sizes printed on the pages, and blocks built and decoded by hand
+from the printed code (tests/golden/*.json, each citing its source).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+from conftest import GOLDEN
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---- binary16 -------------------------------------------------------------
+def test_f16_all_halves_decode_like_numpy():
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.f16_bits_to_f32(h)
+    ref = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_f16_roundtrip_every_finite_half():
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = h.view(np.float16).astype(np.float32)
+    keep = ~np.isnan(f)
+    back = oracle.f32_to_f16_bits(f[keep])
+    assert np.array_equal(back, h[keep])
+
+
+def test_f16_encode_matches_numpy_rne_random_and_edges():
+    rng = np.random.Generator(np.random.PCG64(7))
+    bits = rng.integers(0, 2**32, size=400_000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[~np.isnan(f)]
+    # midpoints between neighbouring halves: the tie cases
+    h = np.arange(0, 0x7bff, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mid = ((lo + hi) / 2).astype(np.float32)
+    allf = np.concatenate([f, mid, -mid, np.float32([65504, 65519.99, 65520, 65536, 1e30, -1e30, 1e-30])])
+    ours = oracle.f32_to_f16_bits(allf)
+    with np.errstate(over="ignore"):
+        ref = allf.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_f16_hand_values():
+    g = _golden("f16.json")
+    for val, hexbits in g["cases"]:
+        assert int(oracle.f32_to_f16_bits([np.float32(float(val))])[0]) == int(hexbits, 16), val
+
+
+# ---- sizes ----------------------------------------------------------------
+def test_block_sizes_from_pages():
+    # 18 / 144 / 210 / 36 bytes and 4.5 bits per weight for Q4_0 and Q4_K
+    assert oracle.block_bytes(oracle.Q4_0) == 18 and oracle.block_elems(oracle.Q4_0) == 32
+    assert oracle.block_bytes(oracle.Q4_K) == 144 and oracle.block_elems(oracle.Q4_K) == 256
+    assert oracle.block_bytes(oracle.Q6_K) == 210 and oracle.block_elems(oracle.Q6_K) == 256
+    assert oracle.block_bytes(oracle.Q8_1) == 36 and oracle.block_elems(oracle.Q8_1) == 32
+    assert 18 * 8 / 32 == 4.5 and 144 * 8 / 256 == 4.5
+
+
+def test_row_and_padding_sizes():
+    # one 4096-wide Q4_K row: 16 super-blocks, 2304 bytes (the 4096x4096 launch example)
+    assert oracle.row_bytes(oracle.Q4_K, 4096) == 2304
+    assert oracle.row_bytes(oracle.Q4_0, 4096) == 2304
+    assert oracle.row_bytes(oracle.Q6_K, 4096) == 3360
+    assert oracle.row_bytes(oracle.Q6_K, 14336) == 11760
+    assert oracle.row_bytes(oracle.Q4_K, 11008) == 6192
+    # activations padded to a multiple of 512 (MATRIX_ROW_PADDING)
+    assert oracle.q8_1_padded_k(4096) == 4096
+    assert oracle.q8_1_padded_k(11008) == 11264 and 11264 // 32 == 352
+    assert oracle.q8_1_padded_k(1) == 512
+    with pytest.raises(ValueError):
+        oracle.row_bytes(oracle.Q4_K, 4096 + 32)
+
+
+# ---- decoders against hand-built blocks ------------------------------------
+def _expect_from(g, n_sub, sub_len):
+    exp = np.repeat(np.asarray(g["default_by_subblock"], dtype=np.float64), sub_len)
+    assert exp.size == n_sub * sub_len
+    for idx, v in g["exceptions"]:
+        exp[idx] = v
+    return exp
+
+
+def test_q4_K_decode_hand_block():
+    g = _golden("q4_K_block.json")
+    blk = np.frombuffer(bytes.fromhex(g["block_hex"]), dtype=np.uint8)
+    got = oracle.dequantize_rows(oracle.Q4_K, blk, 256)[0]
+    assert np.array_equal(got, _expect_from(g, 8, 32))
+    # the printed fp32 row function agrees exactly on this block (all values exact in fp32)
+    assert np.array_equal(oracle.dequantize_row_q4_K_f32(blk, 256).astype(np.float64), got)
+
+
+def test_q4_0_decode_hand_block():
+    g = _golden("q4_0_block.json")
+    blk = np.frombuffer(bytes.fromhex(g["block_hex"]), dtype=np.uint8)
+    got = oracle.dequantize_rows(oracle.Q4_0, blk, 32)[0]
+    exp = np.full(32, g["default"])
+    for idx, v in g["exceptions"]:
+        exp[idx] = v
+    assert np.array_equal(got, exp)
+
+
+def test_q6_K_decode_hand_block():
+    g = _golden("q6_K_block.json")
+    blk = np.frombuffer(bytes.fromhex(g["block_hex"]), dtype=np.uint8)
+    got = oracle.dequantize_rows(oracle.Q6_K, blk, 256)[0]
+    assert np.array_equal(got, _expect_from(g, 16, 16))
+
+
+def test_q4_K_f32_row_function_matches_exact_decode_on_random_blocks():
+    W = oracle.random_blocks(oracle.Q4_K, 8, 1024, seed=11)
+    exact = oracle.dequantize_rows(oracle.Q4_K, W, 1024)
+    for r in range(8):
+        f32 = oracle.dequantize_row_q4_K_f32(W[r], 1024).astype(np.float64)
+        # d*sc, dmin*m and d1*q - m1 are three fp32 roundings of exact values
+        tol = 4 * np.finfo(np.float32).eps * (np.abs(exact[r]) + 64 * 2.0**-4 * 63)
+        assert np.all(np.abs(f32 - exact[r]) <= tol)
+
+
+def test_q4_K_every_scale_min_pair_roundtrips_through_pack_and_decode():
+    # pack (sc, m) into the 12 scale bytes via the quantizer of a crafted
+    # super-block is indirect; instead check that decoding uses each 6-bit
+    # field independently: a block whose qs are all 1 decodes to d*sc - dmin*m.
+    rng = np.random.Generator(np.random.PCG64(3))
+    for trial in range(64):
+        sc = rng.integers(0, 64, 8)
+        m = rng.integers(0, 64, 8)
+        s = np.zeros(12, dtype=np.uint8)
+        for j in range(4):   # packing written from the unpack rule on the mul_mat_vec_q page
+            s[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+            s[j + 4] = (m[j] & 63) | ((m[j + 4] >> 4) << 6)
+            s[j + 8] = (sc[j + 4] & 15) | ((m[j + 4] & 15) << 4)
+        blk = np.concatenate([np.frombuffer(bytes.fromhex("003c0038"), dtype=np.uint8), s,
+                              np.full(128, 0x11, dtype=np.uint8)])
+        got = oracle.dequantize_rows(oracle.Q4_K, blk, 256)[0].reshape(8, 32)
+        exp = (1.0 * sc - 0.5 * m)[:, None]
+        assert np.array_equal(got, np.broadcast_to(exp, (8, 32)))
