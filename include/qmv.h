@@ -1,0 +1,186 @@
+/*
+ * libqmv -- quantized decode GEMV for NVIDIA GB300 (sm_103a).
+ *
+ * Computes y = W . x for decode-time LLM inference, where W is stored in the
+ * GGUF block formats Q4_0, Q4_K or Q6_K and x is first quantized to q8_1
+ * blocks.  Each block product is an int8 dot product (dp4a) scaled by the
+ * block scales.  The operation and the formats follow the page
+ * "llama.cpp 源码完全拆解(十四)：mul_mat_vec_q——解码时一条量化权重如何被 dp4a
+ * 逐块点积" (sections "权重的排法", "激活的量化", "dp4a", "一次 vec_dot 的解剖",
+ * "融合", "MoE") and "GGUF 量化内幕 第16章" (16.1.2 block structs,
+ * 16.2.1 dequantize_row_q4_K).
+ *
+ * Conventions shared by every call:
+ *   - Ownership: the caller allocates and owns every buffer; device pointers
+ *     point to device memory.  The library allocates no memory and keeps no
+ *     per-call state.
+ *   - Execution: calls are asynchronous on `stream` (a cudaStream_t passed as
+ *     void*, NULL for the legacy default stream).  Arguments are validated on
+ *     the host before anything is launched; a failed validation launches
+ *     nothing and returns the status below.  A failed launch returns
+ *     QMV_ERR_CUDA.
+ *   - Layouts: W is row-major, row r at W + r*qmv_row_bytes(type, K), blocks
+ *     back to back within a row (GGUF order).  Activations are q8_1 rows of
+ *     qmv_q8_1_padded_k(K)/32 blocks of 36 bytes, column c at
+ *     xq + c*qmv_q8_1_bytes(K, 1), as written by qmv_quantize_q8_1.  Outputs
+ *     are fp32, column-major over rows: y[c*M + r].
+ *   - Limits: 1 <= ncols <= 8 (MMVQ_MAX_BATCH_SIZE on the page); K a
+ *     positive multiple of the block size (32 for Q4_0, 256 for Q4_K/Q6_K);
+ *     M >= 1.  W must be 2-byte aligned, xq 4-byte aligned, y 4-byte
+ *     aligned.  Rows whose byte size is a multiple of 16 with a 16-byte
+ *     aligned W take the streaming path; other shapes take a slower generic
+ *     path with identical results.
+ *   - Threads: calls are thread-safe; the tuning overrides below are
+ *     process-wide.
+ *   - Waits: kernels never wait without a time limit.  A limit that runs out
+ *     (which only a broken device or driver can cause) sets a sticky device
+ *     fault word, read by qmv_device_fault().
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Type ids, numbered as ggml numbers them ("GGUF 量化内幕 第16章", 16.1.1). */
+typedef enum {
+    QMV_TYPE_Q4_0 = 2,  /* 32 weights per 18-byte block: half d, 16 bytes of nibbles; w = d*(q-8) */
+    QMV_TYPE_Q8_1 = 9,  /* 32 int8 activations per 36-byte block: half d, half s = d*sum(q) */
+    QMV_TYPE_Q4_K = 12, /* 256 weights per 144-byte block: half d, half dmin, 12 bytes of 6-bit
+                           scales/mins, 128 bytes of nibbles; w = d*sc*q - dmin*m */
+    QMV_TYPE_Q6_K = 14  /* 256 weights per 210-byte block: ql[128], qh[64], int8 scales[16],
+                           half d; w = d*sc*(v-32), v = 6-bit code */
+} qmv_type;
+
+typedef enum {
+    QMV_OK = 0,
+    QMV_ERR_NULL = 1,         /* a required pointer is NULL */
+    QMV_ERR_TYPE = 2,         /* unsupported type id */
+    QMV_ERR_SHAPE = 3,        /* M, K, ldx, n_expert, n_tokens or top_k out of range */
+    QMV_ERR_NCOLS = 4,        /* ncols (or n_tokens for MoE) not in 1..8 */
+    QMV_ERR_ALIGN = 5,        /* a pointer violates the alignment stated above */
+    QMV_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
+    QMV_ERR_IDS = 7,          /* reserved: invalid expert ids are reported through dev_status */
+    QMV_ERR_DEVICE_FAULT = 8  /* a kernel's bounded wait ran out (see qmv_device_fault) */
+} qmv_status;
+
+/* Human-readable name of a status code (static storage). */
+const char *qmv_status_str(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int qmv_version(void);
+
+/* ---- sizes ---------------------------------------------------------------- */
+
+/* Bytes of one weight row: (K / block elems) * block bytes; 0 if the type is
+ * not a weight type or K is not a positive multiple of its block size. */
+size_t qmv_row_bytes(int type, int64_t K);
+
+/* K rounded up to a multiple of 512: activations are quantized and strided
+ * with this padded width (MATRIX_ROW_PADDING on the mul_mat_vec_q page,
+ * section "激活的量化"); the padding quantizes to zero blocks. */
+int64_t qmv_q8_1_padded_k(int64_t K);
+
+/* Bytes of ncols q8_1 activation rows: ncols * padded_k/32 * 36. */
+size_t qmv_q8_1_bytes(int64_t K, int ncols);
+
+/* ---- activation quantization -------------------------------------------------
+ * q8_1 quantization of ncols fp32 columns (mul_mat_vec_q page, quantize_q8_1
+ * kernel): per 32 values amax = max|x|, d = amax/127 in fp32, q = round(x/d)
+ * (halfway cases away from zero), stored d and s = d*sum(q) as half.  Column c
+ * is read from x + c*ldx (K floats, device); values past K quantize as zeros
+ * up to the padded width.  xq receives qmv_q8_1_bytes(K, ncols) bytes.
+ * Readings where the page is silent: s holds d*sum(q) (the struct comment)
+ * rather than the float sum of x; a block whose amax/127 underflows to zero
+ * quantizes to zero; codes are clamped to [-127, 127].
+ * Inputs must be finite.  ncols may exceed 8 here (any ncols >= 1). */
+int qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *xq, void *stream);
+
+/* ---- weight quantization ------------------------------------------------------
+ * Quantizes an fp32 matrix w (M rows of K floats, row r at w + r*ldw,
+ * device) into blocks of `type` written to W (M * qmv_row_bytes bytes).
+ * Q4_0 follows the rule on "解构LLM：以llama.cpp分析模型推理过程", section
+ * "量化格式" (scale = max|x|/7, q = round(x/scale) + 8).  The Q4_K and Q6_K
+ * quantizers are not printed on the pages; they are plain min/max (Q4_K) and
+ * absmax (Q6_K) rules taken from the stored half scales.  Bit-identical to
+ * the repository's CPU oracle.  Not performance-critical (a preparation step).
+ * Inputs must be finite with |x| < 1e4. */
+int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t ldw, void *W,
+                         void *stream);
+
+/* ---- GEMV ---------------------------------------------------------------------
+ * y[c*M + r] = sum over blocks of the block formula for row r and activation
+ * column c, for c < ncols (mul_mat_vec_q page, vec_dot_q4_0_q8_1_impl,
+ * vec_dot_q4_K_q8_1_impl_vmmq and the Q6_K vec_dot):
+ *   Q4_0: sum_b d4 * (d8*sumi - 8*s)              sumi = sum of code*qy
+ *   Q4_K: sum_sb d*sc*d8*dot1 - dmin*m*d8*dot2     dot1 = sum code*qy, dot2 = sum qy
+ *   Q6_K: sum_sb d*sc*d8*sum((v-32)*qy)            per 16-value sub-block
+ * accumulated in fp32.  W is read exactly once per call whatever ncols is;
+ * each weight block is decoded once and reused for every column. */
+int qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols,
+                    float *y, void *stream);
+
+/* Fused gate/up GEMV with SwiGLU epilogue (mul_mat_vec_q page, section
+ * "融合"): both products are accumulated in one pass over the shared q8_1
+ * activations and y[c*M + r] = up * silu(gate), silu(g) = g/(1+exp(-g)).
+ * W_gate and W_up have identical shape and type.  The page fuses only at a
+ * single column; this call accepts 1 <= ncols <= 8. */
+int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_up, int64_t M,
+                                   int64_t K, const void *xq, int ncols, float *y, void *stream);
+
+/* Expert-indexed GEMV for mixture-of-experts (mul_mat_vec_q page, section
+ * "MoE"): W holds n_expert matrices back to back (expert e at
+ * W + e*M*row_bytes); xq holds one q8_1 row per token; ids (device, int32,
+ * [n_tokens][top_k]) names the expert of each token slot.  Output
+ * y[(t*top_k + k)*M + r] = (W[ids[t][k]] . x[t])[r].  Tokens routed to the
+ * same expert share one pass over its weights; experts no token selects are
+ * not read.  An id outside [0, n_expert) zero-fills that slot's output; if
+ * dev_status is not NULL the kernel stores there the number of such slots
+ * (0 when all ids are valid).  1 <= n_tokens <= 8, 1 <= top_k <= 32,
+ * 1 <= n_expert <= 65535. */
+int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int64_t K,
+                       const void *xq, const int32_t *ids, int n_tokens, int top_k, float *y,
+                       int32_t *dev_status, void *stream);
+
+/* ---- verification --------------------------------------------------------------
+ * The exact int32 intermediates of the block formulas, computed by the same
+ * device code as qmv_mul_mat_vec (for bit-exact parity tests).  out is
+ * [ncols][M][n] int32 with
+ *   Q4_0: n = K/32, per block sum of code*qy (code = raw nibble 0..15);
+ *   Q4_K: n = K/16, per 32-value sub-block the pair (dot1, dot2);
+ *   Q6_K: n = K/16, per 16-value sub-block sum (v-32)*qy.
+ * out is cleared and written asynchronously on stream. */
+int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const void *xq,
+                            int ncols, int32_t *out, void *stream);
+
+/* Reads and clears the sticky device fault word of the current device: 0 if
+ * no kernel's bounded wait has run out since the last call, else a nonzero
+ * code.  Synchronous (waits for the device). */
+int qmv_device_fault(unsigned int *code);
+
+/* ---- tuning (process-wide) -----------------------------------------------------
+ * Overrides the launch geometry the library picks for the streaming GEMV of
+ * `type` (0 = keep the built-in choice for that field): threads per CTA
+ * (multiple of 32, <= 256), weight units per pipeline slice, pipeline
+ * stages, and resident CTAs per SM.  Meant for tuning sweeps. */
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm);
+
+/* Enables (1, default) or disables (0) programmatic dependent launch for the
+ * library's q8_1 and GEMV kernels.  When enabled, a GEMV may start streaming
+ * its weights while the kernel before it on the stream is still finishing,
+ * and reads activations, ids and writes outputs only after that kernel has
+ * completed.  The weights must therefore not be written by a kernel that
+ * signals early completion (griddepcontrol.launch_dependents); ordinary
+ * kernels and copies are waited for as usual, and the library's own kernels
+ * never write weights except qmv_quantize_weights, which launches
+ * ordinarily. */
+int qmv_set_pdl(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMV_H */

@@ -1,0 +1,444 @@
+// C ABI of libqmv: argument validation, launch-geometry choice and launches.
+// The public contract is documented in include/qmv.h.
+#include <algorithm>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/qmv.h"
+#include "gemv_stream.cuh"
+#include "kernels.h"
+
+namespace qmv {
+
+const void *gemv_stream_fn_q4_0(int mode, int nc);
+const void *gemv_stream_fn_q4_K(int mode, int nc);
+const void *gemv_stream_fn_q6_K(int mode, int nc);
+const void *gemv_generic_fn_q4_0(int mode);
+const void *gemv_generic_fn_q4_K(int mode);
+const void *gemv_generic_fn_q6_K(int mode);
+
+const void *gemv_stream_fn(int type, int mode, int nc)
+{
+    switch (type) {
+    case FMT_Q4_0: return gemv_stream_fn_q4_0(mode, nc);
+    case FMT_Q4_K: return gemv_stream_fn_q4_K(mode, nc);
+    case FMT_Q6_K: return gemv_stream_fn_q6_K(mode, nc);
+    default: return nullptr;
+    }
+}
+
+const void *gemv_generic_fn(int type, int mode)
+{
+    switch (type) {
+    case FMT_Q4_0: return gemv_generic_fn_q4_0(mode);
+    case FMT_Q4_K: return gemv_generic_fn_q4_K(mode);
+    case FMT_Q6_K: return gemv_generic_fn_q6_K(mode);
+    default: return nullptr;
+    }
+}
+
+int gemv_unit_bytes(int type)
+{
+    switch (type) {
+    case FMT_Q4_0: return FmtTraits<FMT_Q4_0>::UNIT_BYTES;
+    case FMT_Q4_K: return FmtTraits<FMT_Q4_K>::UNIT_BYTES;
+    case FMT_Q6_K: return FmtTraits<FMT_Q6_K>::UNIT_BYTES;
+    default: return 0;
+    }
+}
+
+static int unit_elems(int type) { return type == FMT_Q6_K ? 2048 : 256; }
+static int block_elems(int type) { return type == FMT_Q4_0 ? QK4_0 : QK_K; }
+static int block_bytes(int type)
+{
+    return type == FMT_Q4_0 ? Q4_0_BYTES : type == FMT_Q4_K ? Q4_K_BYTES : Q6_K_BYTES;
+}
+static bool weight_type(int t) { return t == FMT_Q4_0 || t == FMT_Q4_K || t == FMT_Q6_K; }
+
+// Sticky fault word written by kernels whose bounded wait ran out.
+__device__ unsigned int g_fault_word;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr size_t SMEM_RESERVE = 1024;  // static shared memory and alignment slack per CTA
+
+std::atomic<int> g_pdl{1};
+
+struct Tuning {
+    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0};
+};
+Tuning g_tuning[3];
+
+int tidx(int type) { return type == FMT_Q4_0 ? 0 : type == FMT_Q4_K ? 1 : 2; }
+
+std::mutex g_mu;
+std::map<std::tuple<int, const void *, int, size_t>, int> g_occupancy;  // (dev, fn, threads, smem) -> CTAs/SM
+std::map<std::pair<int, const void *>, bool> g_smem_attr;
+int g_num_sms[MAX_DEVICES];
+int g_smem_optin[MAX_DEVICES];
+unsigned int *g_fault_ptr[MAX_DEVICES];
+
+qmv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ERR_CUDA; }
+
+struct DevInfo {
+    int dev;
+    int num_sms;
+    size_t smem_limit;  // dynamic shared memory a CTA may use
+    unsigned int *fault;
+};
+
+qmv_status device_info(DevInfo &d)
+{
+    if (cudaGetDevice(&d.dev) != cudaSuccess) return QMV_ERR_CUDA;
+    if (d.dev < 0 || d.dev >= MAX_DEVICES) return QMV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_num_sms[d.dev]) {
+        int n = 0, optin = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d.dev) != cudaSuccess) return QMV_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.dev) != cudaSuccess)
+            return QMV_ERR_CUDA;
+        g_smem_optin[d.dev] = optin;
+        void *f = nullptr;
+        if (cudaGetSymbolAddress(&f, g_fault_word) != cudaSuccess) return QMV_ERR_CUDA;
+        g_fault_ptr[d.dev] = static_cast<unsigned int *>(f);
+        g_num_sms[d.dev] = n;
+    }
+    d.num_sms = g_num_sms[d.dev];
+    d.smem_limit = static_cast<size_t>(g_smem_optin[d.dev]) - SMEM_RESERVE;
+    d.fault = g_fault_ptr[d.dev];
+    return QMV_OK;
+}
+
+qmv_status ensure_smem_attr(const DevInfo &d, const void *fn)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(d.dev, fn);
+    if (g_smem_attr.count(key)) return QMV_OK;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(d.smem_limit)) !=
+        cudaSuccess)
+        return QMV_ERR_CUDA;
+    g_smem_attr[key] = true;
+    return QMV_OK;
+}
+
+int occupancy(int dev, const void *fn, int threads, size_t smem)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(dev, fn, threads, smem);
+    auto it = g_occupancy.find(key);
+    if (it != g_occupancy.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess) n = 0;
+    g_occupancy[key] = n;
+    return n;
+}
+
+int round_nc(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Launch {
+    const void *fn = nullptr;
+    bool stream = false;
+    GemvParams p{};
+    dim3 grid, block;
+    size_t smem = 0;
+};
+
+// Chooses the kernel and its geometry.  The streaming kernel needs 16-byte
+// aligned rows and pointers and an activation area that fits in shared memory;
+// everything else goes to the generic kernel.
+qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_active, int n_potential_experts,
+                Launch &L)
+{
+    const int nc_t = (mode == MODE_PLAIN) ? nc_active : round_nc(nc_active);
+    const int ub = gemv_unit_bytes(type);
+    bool streamable = (p.row_bytes % 16 == 0) && (p.K % unit_elems(type) == 0) &&
+                      (reinterpret_cast<uintptr_t>(p.W) % 16 == 0) &&
+                      (mode != MODE_GATE || reinterpret_cast<uintptr_t>(p.W2) % 16 == 0);
+    const size_t act = align_up(static_cast<size_t>(nc_t) * p.K * 3 / 2, 128);
+    if (act + 4096 > dev.smem_limit) streamable = false;
+
+    if (streamable) {
+        const Tuning &tu = g_tuning[tidx(type)];
+        int threads = tu.threads.load() ? tu.threads.load() : 128;
+        int slice_units = tu.slice_units.load() ? tu.slice_units.load() : (type == FMT_Q6_K ? 1 : 4);
+        int stages = tu.stages.load() ? tu.stages.load() : (type == FMT_Q6_K ? 2 : 4);
+        const int units_per_row = p.K / unit_elems(type);
+        threads = std::max(32, std::min(MAX_THREADS, threads / 32 * 32));
+        slice_units = std::max(1, std::min(slice_units, units_per_row));
+        stages = std::max(1, std::min(stages, 16));
+        size_t smem = 0;
+        for (;;) {
+            const size_t slot = static_cast<size_t>(NR) * slice_units * ub;
+            // activations | rings | 16 B over-read pad | mbarriers | alignment slack
+            smem = act + static_cast<size_t>(threads / 32) * stages * slot + 16 +
+                   static_cast<size_t>(threads / 32) * stages * 8 + 128;
+            if (smem <= dev.smem_limit) break;
+            if (stages > 2) --stages;
+            else if (slice_units > 1) slice_units = (slice_units + 1) / 2;
+            else if (threads > 32) threads /= 2;
+            else { streamable = false; break; }
+        }
+        if (streamable) {
+            L.fn = gemv_stream_fn(type, mode, nc_t);
+            if (!L.fn) return QMV_ERR_NCOLS;
+            if (ensure_smem_attr(dev, L.fn) != QMV_OK) return QMV_ERR_CUDA;
+            const int R = (mode == MODE_GATE) ? NR / 2 : NR;
+            p.units_per_row = units_per_row;
+            p.slice_units = slice_units;
+            p.n_slices = (units_per_row + slice_units - 1) / slice_units;
+            p.stages = stages;
+            p.n_groups = (p.M + R - 1) / R;
+            p.act_bytes = static_cast<uint32_t>(act);
+            p.slice_stride = static_cast<uint32_t>(slice_units * ub);
+            p.slot_bytes = static_cast<uint32_t>(NR) * p.slice_stride;
+            const int warps = threads / 32;
+            int occ = occupancy(dev.dev, L.fn, threads, smem);
+            if (occ <= 0) return QMV_ERR_CUDA;
+            if (tu.ctas_per_sm.load() > 0) occ = std::min(occ, tu.ctas_per_sm.load());
+            const int64_t cap = static_cast<int64_t>(occ) * dev.num_sms;
+            const int64_t need = (p.n_groups + warps - 1) / warps;
+            int64_t gx = std::min(need, cap);
+            if (mode == MODE_MOE) gx = std::min(need, std::max<int64_t>(1, (cap + n_potential_experts - 1) / n_potential_experts));
+            L.stream = true;
+            L.p = p;
+            L.block = dim3(threads);
+            L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)), mode == MODE_MOE ? p.n_expert + 1 : 1);
+            L.smem = smem;
+            return QMV_OK;
+        }
+    }
+    L.fn = gemv_generic_fn(type, mode);
+    if (!L.fn) return QMV_ERR_TYPE;
+    L.stream = false;
+    L.p = p;
+    const int threads = 128;
+    const int64_t need = (p.M + 3) / 4;
+    int64_t gx = std::min<int64_t>(need, static_cast<int64_t>(dev.num_sms) * 16);
+    if (mode == MODE_MOE) gx = std::min<int64_t>(need, std::max<int64_t>(1, dev.num_sms * 16 / n_potential_experts));
+    L.block = dim3(threads);
+    L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)), mode == MODE_MOE ? p.n_expert + 1 : 1);
+    L.smem = 0;
+    return QMV_OK;
+}
+
+qmv_status launch(const Launch &L, const DevInfo &dev, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = L.grid;
+    cfg.blockDim = L.block;
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_pdl.load() ? 1 : 0;
+    GemvParams p = L.p;
+    unsigned int *fault = dev.fault;
+    void *args_stream[2] = {&p, &fault};
+    void *args_generic[1] = {&p};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, L.stream ? args_stream : args_generic);
+    return cuda_status(e);
+}
+
+qmv_status check_common(int type, const void *W, int64_t M, int64_t K, const void *xq, const void *out)
+{
+    if (!weight_type(type)) return QMV_ERR_TYPE;
+    if (!W || !xq || !out) return QMV_ERR_NULL;
+    if (M <= 0 || K <= 0 || K % block_elems(type) != 0) return QMV_ERR_SHAPE;
+    if (K > (int64_t(1) << 28) || M > (int64_t(1) << 40)) return QMV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(W) % 2 || reinterpret_cast<uintptr_t>(xq) % 4 ||
+        reinterpret_cast<uintptr_t>(out) % 4)
+        return QMV_ERR_ALIGN;
+    return QMV_OK;
+}
+
+GemvParams base_params(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols)
+{
+    GemvParams p{};
+    p.W = static_cast<const uint8_t *>(W);
+    p.xq = static_cast<const uint8_t *>(xq);
+    p.M = M;
+    p.ldy = M;
+    p.K = static_cast<int>(K);
+    p.ncols = ncols;
+    p.row_bytes = K / block_elems(type) * block_bytes(type);
+    p.xq_col_bytes = (K + ROW_PAD - 1) / ROW_PAD * ROW_PAD / QK8_1 * Q8_1_BYTES;
+    return p;
+}
+
+}  // namespace
+}  // namespace qmv
+
+using namespace qmv;
+
+extern "C" {
+
+const char *qmv_status_str(int s)
+{
+    switch (s) {
+    case QMV_OK: return "ok";
+    case QMV_ERR_NULL: return "null pointer";
+    case QMV_ERR_TYPE: return "unsupported type";
+    case QMV_ERR_SHAPE: return "bad shape";
+    case QMV_ERR_NCOLS: return "ncols out of range";
+    case QMV_ERR_ALIGN: return "misaligned pointer";
+    case QMV_ERR_CUDA: return "CUDA error";
+    case QMV_ERR_IDS: return "invalid expert id";
+    case QMV_ERR_DEVICE_FAULT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int qmv_version(void) { return 10000; }
+
+size_t qmv_row_bytes(int type, int64_t K)
+{
+    if (!weight_type(type) || K <= 0 || K % block_elems(type)) return 0;
+    return static_cast<size_t>(K / block_elems(type) * block_bytes(type));
+}
+
+int64_t qmv_q8_1_padded_k(int64_t K) { return K <= 0 ? 0 : (K + ROW_PAD - 1) / ROW_PAD * ROW_PAD; }
+
+size_t qmv_q8_1_bytes(int64_t K, int ncols)
+{
+    if (K <= 0 || ncols <= 0) return 0;
+    return static_cast<size_t>(ncols) * static_cast<size_t>(qmv_q8_1_padded_k(K) / QK8_1 * Q8_1_BYTES);
+}
+
+int qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *xq, void *stream)
+{
+    if (!x || !xq) return QMV_ERR_NULL;
+    if (K <= 0 || ncols <= 0 || ldx < K || K > (int64_t(1) << 28)) return QMV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(xq) % 4) return QMV_ERR_ALIGN;
+    return cuda_status(launch_quantize_q8_1(x, K, ncols, ldx, static_cast<uint8_t *>(xq),
+                                            static_cast<cudaStream_t>(stream), g_pdl.load() != 0));
+}
+
+int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t ldw, void *W, void *stream)
+{
+    if (!weight_type(type)) return QMV_ERR_TYPE;
+    if (!w || !W) return QMV_ERR_NULL;
+    if (M <= 0 || K <= 0 || K % block_elems(type) || ldw < K) return QMV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(w) % 4) return QMV_ERR_ALIGN;
+    return cuda_status(launch_quantize_weights(type, w, M, K, ldw, static_cast<uint8_t *>(W),
+                                               static_cast<int64_t>(qmv_row_bytes(type, K)),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+int qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols, float *y,
+                    void *stream)
+{
+    qmv_status s = check_common(type, W, M, K, xq, y);
+    if (s != QMV_OK) return s;
+    if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W, M, K, xq, ncols);
+    p.y = y;
+    Launch L;
+    if ((s = plan(type, MODE_PLAIN, dev, p, ncols, 1, L)) != QMV_OK) return s;
+    return launch(L, dev, static_cast<cudaStream_t>(stream));
+}
+
+int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_up, int64_t M, int64_t K,
+                                   const void *xq, int ncols, float *y, void *stream)
+{
+    qmv_status s = check_common(type, W_up, M, K, xq, y);
+    if (s != QMV_OK) return s;
+    if (!W_gate) return QMV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(W_gate) % 2) return QMV_ERR_ALIGN;
+    if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W_up, M, K, xq, ncols);
+    p.W2 = static_cast<const uint8_t *>(W_gate);
+    p.y = y;
+    Launch L;
+    if ((s = plan(type, MODE_GATE, dev, p, ncols, 1, L)) != QMV_OK) return s;
+    return launch(L, dev, static_cast<cudaStream_t>(stream));
+}
+
+int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const void *xq,
+                       const int32_t *ids, int n_tokens, int top_k, float *y, int32_t *dev_status, void *stream)
+{
+    qmv_status s = check_common(type, W, M, K, xq, y);
+    if (s != QMV_OK) return s;
+    if (!ids) return QMV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(ids) % 4 || reinterpret_cast<uintptr_t>(dev_status) % 4) return QMV_ERR_ALIGN;
+    if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
+    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W, M, K, xq, n_tokens);
+    p.y = y;
+    p.ids = ids;
+    p.status = dev_status;
+    p.n_tokens = n_tokens;
+    p.top_k = top_k;
+    p.n_expert = static_cast<int>(n_expert);
+    p.expert_bytes = M * p.row_bytes;
+    const int potential = static_cast<int>(std::min<int64_t>(n_expert, static_cast<int64_t>(n_tokens) * top_k));
+    Launch L;
+    if ((s = plan(type, MODE_MOE, dev, p, n_tokens, potential, L)) != QMV_OK) return s;
+    return launch(L, dev, static_cast<cudaStream_t>(stream));
+}
+
+int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols, int32_t *out,
+                            void *stream)
+{
+    qmv_status s = check_common(type, W, M, K, xq, out);
+    if (s != QMV_OK) return s;
+    if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    const int64_t per_row = (type == FMT_Q4_0) ? K / 32 : K / 16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(out, 0, static_cast<size_t>(ncols) * M * per_row * sizeof(int32_t), st) != cudaSuccess)
+        return QMV_ERR_CUDA;
+    GemvParams p = base_params(type, W, M, K, xq, ncols);
+    p.dbg = out;
+    Launch L;
+    if ((s = plan(type, MODE_DEBUG, dev, p, ncols, 1, L)) != QMV_OK) return s;
+    return launch(L, dev, st);
+}
+
+int qmv_device_fault(unsigned int *code)
+{
+    if (!code) return QMV_ERR_NULL;
+    DevInfo dev;
+    qmv_status s = device_info(dev);
+    if (s != QMV_OK) return s;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpy(&v, dev.fault, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return QMV_ERR_CUDA;
+    if (cudaMemcpy(dev.fault, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return QMV_ERR_CUDA;
+    *code = v;
+    return QMV_OK;
+}
+
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm)
+{
+    if (!weight_type(type)) return QMV_ERR_TYPE;
+    if (threads < 0 || threads > MAX_THREADS || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
+        ctas_per_sm < 0)
+        return QMV_ERR_SHAPE;
+    Tuning &t = g_tuning[tidx(type)];
+    t.threads = threads;
+    t.slice_units = slice_units;
+    t.stages = stages;
+    t.ctas_per_sm = ctas_per_sm;
+    return QMV_OK;
+}
+
+int qmv_set_pdl(int enable)
+{
+    g_pdl = enable ? 1 : 0;
+    return QMV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,238 @@
+// q8_1 activation quantization and the weight quantizers.
+//
+// Every integer code is decided in fp32 with explicitly rounded operations
+// (__fdiv_rn, __fmul_rn, __fadd_rn: never fused or reassociated), C roundf
+// (halfway cases away from zero) and round-to-nearest-even half conversion,
+// so the bytes are a deterministic function of the input floats.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qmv {
+
+__device__ __forceinline__ int clamp_round(float z, float lo, float hi)
+{
+    float r = roundf(z);
+    if (r < lo) r = lo;
+    if (r > hi) r = hi;
+    return static_cast<int>(r);
+}
+
+__device__ __forceinline__ uint32_t f2h_bits(float f)
+{
+    return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(f)));
+}
+
+__device__ __forceinline__ float h2f(uint32_t bits)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
+// ---- q8_1 ------------------------------------------------------------------
+// "llama.cpp 源码完全拆解(十四)：mul_mat_vec_q", quantize_q8_1 kernel: one warp
+// per 32-value block, amax and the code sum reduced by warp shuffles.  Values
+// past K read as zero (the 512-padding).  s = half(d * sum(q)).
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restrict__ x, int64_t K, int64_t ldx,
+                                                            int64_t nb_pad, int64_t n_blocks,
+                                                            uint8_t *__restrict__ xq)
+{
+    pdl_launch_dependents();
+    pdl_wait();  // x may be the output of the previous kernel
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= n_blocks) return;  // uniform per warp
+    const int lane = threadIdx.x & 31;
+    const int64_t c = gw / nb_pad;
+    const int64_t k = (gw - c * nb_pad) * QK8_1 + lane;
+    const float v = k < K ? x[c * ldx + k] : 0.0f;
+    const float amax = warp_max(fabsf(v));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const int q = (d == 0.0f) ? 0 : clamp_round(__fdiv_rn(v, d), -127.0f, 127.0f);
+    const int sum = warp_sum_int(q);
+    // pack four codes per 32-bit store
+    const uint32_t b0 = static_cast<uint32_t>(q) & 0xffu;
+    const uint32_t b1 = static_cast<uint32_t>(__shfl_down_sync(0xffffffffu, q, 1)) & 0xffu;
+    const uint32_t b2 = static_cast<uint32_t>(__shfl_down_sync(0xffffffffu, q, 2)) & 0xffu;
+    const uint32_t b3 = static_cast<uint32_t>(__shfl_down_sync(0xffffffffu, q, 3)) & 0xffu;
+    uint32_t *blk = reinterpret_cast<uint32_t *>(xq + gw * Q8_1_BYTES);
+    if ((lane & 3) == 0) blk[1 + (lane >> 2)] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    if (lane == 0) blk[0] = f2h_bits(d) | (f2h_bits(__fmul_rn(d, static_cast<float>(sum))) << 16);
+}
+
+// ---- Q4_0 --------------------------------------------------------------------
+// "解构LLM：以llama.cpp分析模型推理过程", section "量化格式": scale = max|x|/7,
+// q = round(x/scale) + 8 (clamped to 0..15), scale stored as half.
+__global__ void quantize_q4_0_kernel(const float *__restrict__ w, int64_t M, int64_t nb, int64_t ldw,
+                                     int64_t row_bytes, uint8_t *__restrict__ W)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M * nb) return;
+    const int64_t r = i / nb, b = i - r * nb;
+    const float *v = w + r * ldw + b * QK4_0;
+    uint8_t *blk = W + r * row_bytes + b * Q4_0_BYTES;
+    float amax = 0.0f;
+    for (int e = 0; e < QK4_0; ++e) {
+        const float a = fabsf(v[e]);
+        if (a > amax) amax = a;
+    }
+    const float d = __fdiv_rn(amax, 7.0f);
+    const uint32_t dh = f2h_bits(d);
+    blk[0] = dh & 0xff;
+    blk[1] = dh >> 8;
+    for (int e = 0; e < 16; ++e) {
+        const int q0 = (d == 0.0f) ? 8 : clamp_round(__fdiv_rn(v[e], d), -8.0f, 7.0f) + 8;
+        const int q1 = (d == 0.0f) ? 8 : clamp_round(__fdiv_rn(v[e + 16], d), -8.0f, 7.0f) + 8;
+        blk[2 + e] = static_cast<uint8_t>(q0 | (q1 << 4));
+    }
+}
+
+// ---- Q4_K --------------------------------------------------------------------
+// Plain min/max reading (the pages give no quantizer): per 32-value sub-block
+// lo = min(0, min x), step = (max x - lo)/15; d = max step/63 and
+// dmin = max(-lo)/63 stored as half; 6-bit sc, m rounded against the stored
+// halves; q = round((x + dmin*m)/(d*sc)) clamped to 0..15.
+__global__ void quantize_q4_K_kernel(const float *__restrict__ w, int64_t M, int64_t nb, int64_t ldw,
+                                     int64_t row_bytes, uint8_t *__restrict__ W)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M * nb) return;
+    const int64_t r = i / nb, b = i - r * nb;
+    const float *v = w + r * ldw + b * QK_K;
+    uint8_t *blk = W + r * row_bytes + b * Q4_K_BYTES;
+    float step[8], neg[8];
+    for (int sb = 0; sb < 8; ++sb) {
+        const float *p = v + 32 * sb;
+        float mn = p[0], mx = p[0];
+        for (int e = 1; e < 32; ++e) {
+            if (p[e] < mn) mn = p[e];
+            if (p[e] > mx) mx = p[e];
+        }
+        const float lo = (mn < 0.0f) ? mn : 0.0f;
+        step[sb] = __fdiv_rn(__fsub_rn(mx, lo), 15.0f);
+        neg[sb] = (mn < 0.0f) ? -mn : 0.0f;
+    }
+    float smax = 0.0f, nmax = 0.0f;
+    for (int sb = 0; sb < 8; ++sb) {
+        if (step[sb] > smax) smax = step[sb];
+        if (neg[sb] > nmax) nmax = neg[sb];
+    }
+    const uint32_t dh = f2h_bits(__fdiv_rn(smax, 63.0f));
+    const uint32_t mh = f2h_bits(__fdiv_rn(nmax, 63.0f));
+    const float df = h2f(dh), mf = h2f(mh);
+    int sc[8], m[8];
+    for (int sb = 0; sb < 8; ++sb) {
+        sc[sb] = (df > 0.0f) ? clamp_round(__fdiv_rn(step[sb], df), 0.0f, 63.0f) : 0;
+        m[sb] = (mf > 0.0f) ? clamp_round(__fdiv_rn(neg[sb], mf), 0.0f, 63.0f) : 0;
+    }
+    blk[0] = dh & 0xff;
+    blk[1] = dh >> 8;
+    blk[2] = mh & 0xff;
+    blk[3] = mh >> 8;
+    // 6-bit packing: sub-blocks 0-3 in the low 6 bits of bytes 0-3 (scales)
+    // and 4-7 (mins); sub-blocks 4-7 split into a nibble in bytes 8-11 and
+    // two bits in the top of bytes 0-3 (scales) / 4-7 (mins).
+    for (int j = 0; j < 4; ++j) {
+        blk[4 + j] = static_cast<uint8_t>((sc[j] & 63) | ((sc[j + 4] >> 4) << 6));
+        blk[8 + j] = static_cast<uint8_t>((m[j] & 63) | ((m[j + 4] >> 4) << 6));
+        blk[12 + j] = static_cast<uint8_t>((sc[j + 4] & 15) | ((m[j + 4] & 15) << 4));
+    }
+    for (int c = 0; c < 4; ++c)
+        for (int l = 0; l < 32; ++l) {
+            int q2[2];
+            for (int h = 0; h < 2; ++h) {
+                const int sb = 2 * c + h;
+                const float t = __fmul_rn(df, static_cast<float>(sc[sb]));
+                const float z = __fadd_rn(v[64 * c + 32 * h + l], __fmul_rn(mf, static_cast<float>(m[sb])));
+                q2[h] = (t > 0.0f) ? clamp_round(__fdiv_rn(z, t), 0.0f, 15.0f) : 0;
+            }
+            blk[16 + 32 * c + l] = static_cast<uint8_t>(q2[0] | (q2[1] << 4));
+        }
+}
+
+// ---- Q6_K --------------------------------------------------------------------
+// Plain absmax reading: per 16-value sub-block s = max|x|/31; d = max s/127
+// stored as half; int8 sc = round(s/d); v = round(x/(d*sc)) clamped to
+// -32..31, stored +32.  Byte order: ql[128], qh[64], scales[16], d.
+__global__ void quantize_q6_K_kernel(const float *__restrict__ w, int64_t M, int64_t nb, int64_t ldw,
+                                     int64_t row_bytes, uint8_t *__restrict__ W)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M * nb) return;
+    const int64_t r = i / nb, b = i - r * nb;
+    const float *v = w + r * ldw + b * QK_K;
+    uint8_t *blk = W + r * row_bytes + b * Q6_K_BYTES;
+    float s[16];
+    float smax = 0.0f;
+    for (int sb = 0; sb < 16; ++sb) {
+        float amax = 0.0f;
+        for (int e = 0; e < 16; ++e) {
+            const float a = fabsf(v[16 * sb + e]);
+            if (a > amax) amax = a;
+        }
+        s[sb] = __fdiv_rn(amax, 31.0f);
+    }
+    for (int sb = 0; sb < 16; ++sb)
+        if (s[sb] > smax) smax = s[sb];
+    const uint32_t dh = f2h_bits(__fdiv_rn(smax, 127.0f));
+    const float df = h2f(dh);
+    int sc[16];
+    for (int sb = 0; sb < 16; ++sb) sc[sb] = (df > 0.0f) ? clamp_round(__fdiv_rn(s[sb], df), -128.0f, 127.0f) : 0;
+    auto code = [&](int e) {
+        const float t = __fmul_rn(df, static_cast<float>(sc[e >> 4]));
+        return (t != 0.0f) ? clamp_round(__fdiv_rn(v[e], t), -32.0f, 31.0f) + 32 : 32;
+    };
+    // ql byte j: element 128h + jj (low nibble) and 128h + 64 + jj (high), h = j/64, jj = j%64
+    for (int j = 0; j < 128; ++j) {
+        const int h = j >> 6, jj = j & 63;
+        blk[j] = static_cast<uint8_t>((code(128 * h + jj) & 15) | ((code(128 * h + 64 + jj) & 15) << 4));
+    }
+    // qh byte j: bits 2g..2g+1 hold the top two bits of element 128h + 32g + l, h = j/32, l = j%32
+    for (int j = 0; j < 64; ++j) {
+        const int h = j >> 5, l = j & 31;
+        uint32_t hb = 0;
+        for (int g = 0; g < 4; ++g) hb |= static_cast<uint32_t>((code(128 * h + 32 * g + l) >> 4) & 3) << (2 * g);
+        blk[128 + j] = static_cast<uint8_t>(hb);
+    }
+    for (int sb = 0; sb < 16; ++sb) blk[192 + sb] = static_cast<uint8_t>(static_cast<int8_t>(sc[sb]));
+    blk[208] = dh & 0xff;
+    blk[209] = dh >> 8;
+}
+
+// ---- launchers -----------------------------------------------------------------
+
+cudaError_t launch_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, uint8_t *xq, cudaStream_t st,
+                                 bool pdl)
+{
+    const int64_t nb_pad = (K + ROW_PAD - 1) / ROW_PAD * ROW_PAD / QK8_1;
+    const int64_t n_blocks = nb_pad * ncols;
+    const int threads = 256;
+    const int64_t grid = (n_blocks * 32 + threads - 1) / threads;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel, x, K, ldx, nb_pad, n_blocks, xq);
+}
+
+cudaError_t launch_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t ldw, uint8_t *W,
+                                    int64_t row_bytes, cudaStream_t st)
+{
+    const int64_t nb = K / (type == FMT_Q4_0 ? QK4_0 : QK_K);
+    const int64_t n = M * nb;
+    const int threads = 128;
+    const int64_t grid = (n + threads - 1) / threads;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    if (type == FMT_Q4_0)
+        quantize_q4_0_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(w, M, nb, ldw, row_bytes, W);
+    else if (type == FMT_Q4_K)
+        quantize_q4_K_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(w, M, nb, ldw, row_bytes, W);
+    else
+        quantize_q6_K_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(w, M, nb, ldw, row_bytes, W);
+    return cudaGetLastError();
+}
+
+}  // namespace qmv

@@ -1,0 +1,92 @@
+"""The C-ABI library builds, loads, exports every symbol include/qmv.h
+declares, agrees with the oracle on sizes, and rejects bad arguments on the
+host before launching anything (no GPU needed: no compute call is made)."""
+import ctypes
+import os
+import re
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qlib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import quantized_decode_gemv_qmv_gb300 as q
+
+    return q
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "qmv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports(qlib):
+    assert _declared_symbols() == sorted(qlib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(qlib):
+    L = ctypes.CDLL(qlib.library_path())
+    for name in _declared_symbols():
+        assert hasattr(L, name), name
+
+
+@pytest.mark.parametrize("t", oracle.WEIGHT_TYPES)
+@pytest.mark.parametrize("K", [32, 256, 4096, 11008, 14336, 2048 + 256])
+def test_sizes_agree_with_oracle(qlib, t, K):
+    qk = oracle.block_elems(t)
+    exp = oracle.row_bytes(t, K) if K % qk == 0 else 0
+    assert qlib.row_bytes(t, K) == exp
+    assert qlib.q8_1_padded_k(K) == oracle.q8_1_padded_k(K)
+    assert qlib.q8_1_bytes(K, 3) == 3 * oracle.q8_1_row_bytes(K)
+
+
+def test_status_strings_and_version(qlib):
+    L = qlib.lib()
+    assert L.qmv_status_str(0) == b"ok"
+    assert L.qmv_status_str(3) == b"bad shape"
+    assert L.qmv_version() >= 10000
+
+
+def test_host_validation_rejects_bad_arguments(qlib):
+    L = qlib.lib()
+    p = ctypes.c_void_p(0x1000)      # never dereferenced: validation fails first
+    nul = ctypes.c_void_p(0)
+    # bad type, null pointers, bad shapes and column counts
+    assert L.qmv_mul_mat_vec(5, p, 16, 256, p, 1, p, nul) == 2
+    assert L.qmv_mul_mat_vec(12, nul, 16, 256, p, 1, p, nul) == 1
+    assert L.qmv_mul_mat_vec(12, p, 16, 250, p, 1, p, nul) == 3
+    assert L.qmv_mul_mat_vec(12, p, 0, 256, p, 1, p, nul) == 3
+    assert L.qmv_mul_mat_vec(12, p, 16, 256, p, 0, p, nul) == 4
+    assert L.qmv_mul_mat_vec(12, p, 16, 256, p, 9, p, nul) == 4
+    assert L.qmv_mul_mat_vec(2, p, 16, 48, p, 1, p, nul) == 3
+    # misaligned pointers
+    assert L.qmv_mul_mat_vec(12, ctypes.c_void_p(0x1001), 16, 256, p, 1, p, nul) == 5
+    assert L.qmv_mul_mat_vec(12, p, 16, 256, ctypes.c_void_p(0x1002), 1, p, nul) == 5
+    # gate/up and MoE specifics
+    assert L.qmv_mul_mat_vec_gate_up_swiglu(12, nul, p, 16, 256, p, 1, p, nul) == 1
+    assert L.qmv_mul_mat_vec_id(12, p, 8, 16, 256, p, nul, 4, 2, p, nul, nul) == 1
+    assert L.qmv_mul_mat_vec_id(12, p, 8, 16, 256, p, p, 9, 2, p, nul, nul) == 4
+    assert L.qmv_mul_mat_vec_id(12, p, 0, 16, 256, p, p, 4, 2, p, nul, nul) == 3
+    assert L.qmv_mul_mat_vec_id(12, p, 8, 16, 256, p, p, 4, 33, p, nul, nul) == 3
+    # quantizers
+    assert L.qmv_quantize_q8_1(nul, 256, 1, 256, p, nul) == 1
+    assert L.qmv_quantize_q8_1(p, 256, 1, 100, p, nul) == 3
+    assert L.qmv_quantize_weights(12, p, 4, 100, 100, p, nul) == 3
+    assert L.qmv_quantize_weights(9, p, 4, 256, 256, p, nul) == 2
+    assert L.qmv_debug_subblock_sums(14, p, 4, 256, p, 0, p, nul) == 4
+    # tuning knobs validate too
+    assert L.qmv_set_tuning(12, 100, 0, 0, 0) == 3
+    assert L.qmv_set_tuning(3, 0, 0, 0, 0) == 2
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0) == 0

@@ -1,0 +1,137 @@
+"""Full-size parity at the benchmark shapes, in the launch configuration the
+benchmark times (default geometry, programmatic dependent launch on).
+
+Weights are the seeded N(0, 0.02) matrices quantized by the oracle; the GPU
+weight quantizer must reproduce those bytes exactly at full size; outputs are
+checked on sampled rows the oracle computes one by one (first, last and 120
+random rows), within 1e-4 of each row's L1 norm of scaled terms.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def q():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import quantized_decode_gemv_qmv_gb300 as qq
+
+    torch.cuda.set_device(0)
+    qq.set_pdl(True)
+    for t in qq.WEIGHT_TYPES:
+        qq.set_tuning(t)
+    return qq
+
+
+def dev(a):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    import torch
+
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def sample_rows(M, seed):
+    r = synthetic.host_rng(seed).choice(M, size=min(M, 120), replace=False)
+    return np.unique(np.concatenate([np.arange(min(4, M)), np.arange(max(0, M - 4), M), r]))
+
+
+def quantized(q, t, M, K, seed):
+    """(oracle bytes, device bytes): the device copy comes from the GPU
+    quantizer, which must match the oracle bit for bit."""
+    w = synthetic.weights_f32(seed, M, K)
+    W = oracle.quantize_rows(t, w)
+    Wd = q.quantize_weights(t, dev(w))
+    assert np.array_equal(host(Wd), W), "GPU weight quantizer differs from the oracle"
+    return W, Wd
+
+
+CONFIGS = [
+    ("q4_0 4096x4096", oracle.Q4_0, 4096, 4096, 0.0),
+    ("q4_K 4096x4096", oracle.Q4_K, 4096, 4096, 0.01),
+    ("q4_K 11008x4096", oracle.Q4_K, 11008, 4096, 0.01),
+    ("q4_K 4096x11008", oracle.Q4_K, 4096, 11008, 0.01),
+    ("q6_K 32000x4096", oracle.Q6_K, 32000, 4096, 0.0),
+    ("q6_K 4096x14336", oracle.Q6_K, 4096, 14336, 0.0),
+]
+
+
+@pytest.mark.parametrize("name,t,M,K,outl", CONFIGS, ids=[c[0] for c in CONFIGS])
+def test_fullsize_gemv_ncols1(q, name, t, M, K, outl):
+    W, Wd = quantized(q, t, M, K, seed=zlib.crc32(name.encode()) % 100000)
+    x = synthetic.activations_f32(17, 1, K, outlier_frac=outl)
+    xq_ref = oracle.quantize_q8_1(x)
+    xq = q.quantize_q8_1(dev(x))
+    assert np.array_equal(host(xq), xq_ref)
+    y = host(q.mul_mat_vec(t, Wd, M, K, xq, 1))
+    rows = sample_rows(M, 18)
+    y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq_ref, 1, rows=rows)
+    err = np.abs(y[:, rows] - y_ref)
+    assert np.all(err <= TOL * l1), (err / l1).max()
+    assert np.all(np.isfinite(y))
+
+
+def test_fullsize_q4_K_small_batch_sweep(q):
+    t, M, K = oracle.Q4_K, 14336, 4096
+    W, Wd = quantized(q, t, M, K, seed=4141)
+    rows = sample_rows(M, 19)
+    for ncols in range(1, 9):
+        x = synthetic.activations_f32(20 + ncols, ncols, K)
+        xq_ref = oracle.quantize_q8_1(x)
+        y = host(q.mul_mat_vec(t, Wd, M, K, dev(xq_ref), ncols))
+        y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq_ref, ncols, rows=rows)
+        assert np.all(np.abs(y[:, rows] - y_ref) <= TOL * l1), ncols
+
+
+def test_fullsize_fused_gate_up(q):
+    t, M, K = oracle.Q4_K, 14336, 4096
+    Wg, Wgd = quantized(q, t, M, K, seed=5151)
+    Wu, Wud = quantized(q, t, M, K, seed=5152)
+    xq_ref = oracle.quantize_q8_1(synthetic.activations_f32(53, 1, K))
+    y = host(q.mul_mat_vec_gate_up_swiglu(t, Wgd, Wud, M, K, dev(xq_ref), 1))
+    rows = sample_rows(M, 54)
+    g, l1g = oracle.gemv_formula(t, Wg, M, K, xq_ref, 1, rows=rows)
+    u, l1u = oracle.gemv_formula(t, Wu, M, K, xq_ref, 1, rows=rows)
+    sig = 1.0 / (1.0 + np.exp(-g))
+    tol = np.abs(u) * np.abs(sig * (1 + g * (1 - sig))) * TOL * l1g + np.abs(g * sig) * TOL * l1u + 1e-6 * np.abs(u * g * sig)
+    assert np.all(np.abs(y[:, rows] - oracle.swiglu(g, u)) <= tol)
+
+
+def test_fullsize_moe(q):
+    import torch
+
+    t, E, M, K, T, k = oracle.Q4_K, 8, 14336, 4096, 4, 2
+    rb = oracle.row_bytes(t, K)
+    W = np.empty((E, M * rb), dtype=np.uint8)
+    Wd = torch.empty((E, M * rb), dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        We, Wed = quantized(q, t, M, K, seed=6000 + e)
+        W[e] = We.reshape(-1)
+        Wd[e] = Wed.reshape(-1)
+    ids = synthetic.moe_ids(61, T, k, E)
+    xq_ref = oracle.quantize_q8_1(synthetic.activations_f32(62, T, K))
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    y = host(q.mul_mat_vec_id(t, Wd, E, M, K, dev(xq_ref), dev(ids), status=status))
+    assert int(host(status)[0]) == 0
+    rows = sample_rows(M, 63)
+    y_ref, l1, bad = oracle.moe_gemv(t, W, E, M, K, xq_ref, ids, rows=rows)
+    assert bad == 0
+    assert np.all(np.abs(y[:, :, rows] - y_ref) <= TOL * l1)
