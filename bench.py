@@ -444,6 +444,33 @@ def run_gpu(args):
     return 0
 
 
+def run_kernel_only(args):
+    """A few GEMV launches of one shape (for profiler captures): two distinct
+    weight copies alternate so consecutive launches do not hit in L2."""
+    import torch
+
+    import synthetic
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import quantized_decode_gemv_qmv_gb300 as q
+
+    if args.kernel_only not in SHAPES:
+        raise SystemExit(f"unknown shape {args.kernel_only}; choose from {list(SHAPES)}")
+    M, K = SHAPES[args.kernel_only]
+    torch.cuda.set_device(0)
+    Ws = [q.quantize_weights(Q4_K, synthetic.device_normal_f32(7 + i, (M, K), 0.02, "cuda")) for i in range(4)]
+    x = torch.from_numpy(synthetic.activations_f32(9, 1, K, outlier_frac=0.01)).cuda()
+    xq = q.quantize_q8_1(x)
+    y = torch.empty((1, M), dtype=torch.float32, device="cuda")
+    for i in range(args.launches):
+        q.mul_mat_vec(Q4_K, Ws[i % len(Ws)], M, K, xq, 1, out=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel_only": args.kernel_only, "launches": args.launches,
+                      "weight_bytes_per_launch": int(Ws[0].numel())}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,10 +479,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=6.0, help="CPU-baseline timing budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-only", default=None, help="profiling aid: only GEMV launches of one shape")
+    ap.add_argument("--launches", type=int, default=8)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel_only:
+        return run_kernel_only(args)
     return run_gpu(args)
 
 

@@ -32,9 +32,11 @@
  *     path with identical results.
  *   - Threads: calls are thread-safe; the tuning overrides below are
  *     process-wide.
- *   - Waits: kernels never wait without a time limit.  A limit that runs out
- *     (which only a broken device or driver can cause) sets a sticky device
- *     fault word, read by qmv_device_fault().
+ *   - Waits: the Q4_0/Q4_K streaming kernel waits on shared-memory
+ *     barriers for its tensor copies; every such wait is bounded (about one
+ *     second).  A wait that runs out sets a sticky device fault word, the
+ *     kernel drains its copies in flight and returns without writing the
+ *     affected rows; qmv_device_fault() reads and clears that word.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -165,9 +167,11 @@ int qmv_device_fault(unsigned int *code);
 /* ---- tuning (process-wide) -----------------------------------------------------
  * Overrides the launch geometry the library picks for the streaming GEMV of
  * `type` (0 = keep the built-in choice for that field): threads per CTA
- * (multiple of 32, <= 256), weight units per pipeline slice, pipeline
- * stages, and resident CTAs per SM.  Meant for tuning sweeps. */
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm);
+ * (multiple of 32, <= 256), weight units per slice (Q4_0/Q4_K: lanes per row,
+ * rounded to a power of two <= 32; Q6_K: 2048-value units per slice), pipeline
+ * stages, resident CTAs per SM, and rows per lane (Q4_0/Q4_K: 1 or 2).  Meant
+ * for tuning sweeps. */
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int rows_per_lane);
 
 /* Enables (1, default) or disables (0) programmatic dependent launch for the
  * library's q8_1 and GEMV kernels.  When enabled, a GEMV may start streaming

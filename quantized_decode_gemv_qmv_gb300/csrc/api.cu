@@ -6,8 +6,10 @@
 #include <mutex>
 #include <tuple>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/qmv.h"
-#include "gemv_stream.cuh"
+#include "gemv_units.cuh"
 #include "kernels.h"
 
 namespace qmv {
@@ -68,7 +70,7 @@ constexpr size_t SMEM_RESERVE = 1024;  // static shared memory and alignment sla
 std::atomic<int> g_pdl{1};
 
 struct Tuning {
-    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0};
+    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, rows_per_lane{0};
 };
 Tuning g_tuning[3];
 
@@ -143,6 +145,9 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Launch {
     const void *fn = nullptr;
     bool stream = false;
+    bool units = false;       // units kernel: takes two tensor maps and the fault word
+    CUtensorMap tm[2];
+    unsigned int *fault = nullptr;
     GemvParams p{};
     dim3 grid, block;
     size_t smem = 0;
@@ -151,12 +156,128 @@ struct Launch {
 // Chooses the kernel and its geometry.  The streaming kernel needs 16-byte
 // aligned rows and pointers and an activation area that fits in shared memory;
 // everything else goes to the generic kernel.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Tensor map viewing `rows` rows of row_bytes bytes at base as a 3D array
+// [rows][row_bytes/144 units][18 eight-byte elements], with a box of
+// 18 x box_units x box_rows.
+bool encode_rows_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t row_bytes, int box_units, int box_rows)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return false;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(UNIT_B / 8), static_cast<cuuint64_t>(row_bytes / UNIT_B),
+                                static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(UNIT_B), static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(UNIT_B / 8), static_cast<cuuint32_t>(box_units),
+                               static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pow2_at_least(int v)
+{
+    int p2 = 1;
+    while (p2 < v) p2 <<= 1;
+    return p2;
+}
+
+// Geometry of the units kernel (Q4_0 / Q4_K): KW lanes per row (power of
+// two <= 32), RT = rows-per-lane * 32/KW rows per group, a per-warp ring of `stages` slots of NM boxes
+// of RT rows x KW units, a light grid of a few CTAs per SM.  Returns false if
+// the activations do not fit in shared memory.
+bool plan_units(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t, int n_potential_experts,
+                Launch &L)
+{
+    const Tuning &tu = g_tuning[tidx(type)];
+    const int U = static_cast<int>(p.K / 256);
+    const int NM = (mode == MODE_GATE) ? 2 : 1;
+    int KW = tu.slice_units.load() ? pow2_at_least(tu.slice_units.load()) : std::min(8, pow2_at_least(U));
+    KW = std::max(1, std::min(32, KW));
+    int threads = tu.threads.load() ? tu.threads.load() : 128;
+    threads = std::max(32, std::min(MAX_THREADS, threads / 32 * 32));
+    int stages = tu.stages.load() ? tu.stages.load() : 2;
+    stages = std::max(1, std::min(stages, 8));
+    int rpl = tu.rows_per_lane.load() ? tu.rows_per_lane.load() : UNITS_RPL;
+    rpl = std::max(1, std::min(UNITS_RPL, rpl));
+    const int RT = rpl * 32 / KW;
+    const int64_t rows_total = (mode == MODE_MOE) ? p.M * p.n_expert : p.M;
+    if (rows_total >= (int64_t(1) << 31)) return false;
+    const size_t box = static_cast<size_t>(RT) * KW * UNIT_B;
+    const size_t slot = static_cast<size_t>(NM) * box;
+    const size_t act = align_up(static_cast<size_t>(nc_t) * U * (ACT_QS_STRIDE + ACT_SC_STRIDE), 128);
+    size_t smem = 0;
+    for (;;) {
+        const size_t warps = static_cast<size_t>(threads / 32);
+        smem = act + warps * stages * slot + warps * stages * 8 + 128;
+        if (smem <= dev.smem_limit) break;
+        if (stages > 2) --stages;
+        else if (threads > 32) threads /= 2;
+        else return false;
+    }
+    L.fn = gemv_stream_fn(type, mode, nc_t);
+    if (!L.fn) return false;
+    if (ensure_smem_attr(dev, L.fn) != QMV_OK) return false;
+    if (!encode_rows_map(&L.tm[0], p.W, rows_total, p.row_bytes, KW, RT)) return false;
+    if (mode == MODE_GATE) {
+        if (!encode_rows_map(&L.tm[1], p.W2, rows_total, p.row_bytes, KW, RT)) return false;
+    } else {
+        L.tm[1] = L.tm[0];
+    }
+    p.units_per_row = U;
+    p.slice_units = KW;
+    p.n_slices = (U + KW - 1) / KW;
+    p.stages = stages;
+    p.rpl = rpl;
+    p.n_groups = (p.M + RT - 1) / RT;
+    p.act_bytes = static_cast<uint32_t>(act);
+    p.slice_stride = static_cast<uint32_t>(KW * UNIT_B);
+    p.slot_bytes = static_cast<uint32_t>(slot);
+    int occ = occupancy(dev.dev, L.fn, threads, smem);
+    if (occ <= 0) return false;
+    const int want = tu.ctas_per_sm.load() > 0 ? tu.ctas_per_sm.load() : 2;
+    occ = std::min(occ, want);
+    // Balanced work: with W warps at most, every warp gets k = ceil(G/W) or
+    // k-1 groups; the grid is sized so the warps' shares are as equal as the
+    // granularity allows.
+    const int warps = threads / 32;
+    int64_t max_ctas = static_cast<int64_t>(occ) * dev.num_sms;
+    if (mode == MODE_MOE) max_ctas = std::max<int64_t>(1, (max_ctas + n_potential_experts - 1) / n_potential_experts);
+    const int64_t max_warps = max_ctas * warps;
+    const int64_t k = (p.n_groups + max_warps - 1) / max_warps;
+    const int64_t want_warps = (p.n_groups + k - 1) / k;
+    const int64_t gx = std::min(max_ctas, (want_warps + warps - 1) / warps);
+    L.stream = true;
+    L.units = true;
+    L.fault = dev.fault;
+    L.p = p;
+    L.block = dim3(threads);
+    L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)), mode == MODE_MOE ? p.n_expert + 1 : 1);
+    L.smem = smem;
+    return true;
+}
+
 qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_active, int n_potential_experts,
                 Launch &L)
 {
     const int nc_t = (mode == MODE_PLAIN) ? nc_active : round_nc(nc_active);
+    if (type != FMT_Q6_K && p.row_bytes % 16 == 0 && p.K % 256 == 0 && reinterpret_cast<uintptr_t>(p.W) % 16 == 0 &&
+        (mode != MODE_GATE || reinterpret_cast<uintptr_t>(p.W2) % 16 == 0)) {
+        if (plan_units(type, mode, dev, p, nc_t, n_potential_experts, L)) return QMV_OK;
+    }
     const int ub = gemv_unit_bytes(type);
-    bool streamable = (p.row_bytes % 16 == 0) && (p.K % unit_elems(type) == 0) &&
+    bool streamable = type == FMT_Q6_K && (p.row_bytes % 16 == 0) && (p.K % unit_elems(type) == 0) &&
                       (reinterpret_cast<uintptr_t>(p.W) % 16 == 0) &&
                       (mode != MODE_GATE || reinterpret_cast<uintptr_t>(p.W2) % 16 == 0);
     const size_t act = align_up(static_cast<size_t>(nc_t) * p.K * 3 / 2, 128);
@@ -169,14 +290,15 @@ qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_act
         int stages = tu.stages.load() ? tu.stages.load() : (type == FMT_Q6_K ? 2 : 4);
         const int units_per_row = p.K / unit_elems(type);
         threads = std::max(32, std::min(MAX_THREADS, threads / 32 * 32));
+        threads = std::min(threads, 32 * units_per_row);  // every warp of the K-split gets >= 1 unit
         slice_units = std::max(1, std::min(slice_units, units_per_row));
-        stages = std::max(1, std::min(stages, 16));
+        stages = std::max(1, std::min(stages, 8));
         size_t smem = 0;
         for (;;) {
+            const size_t warps = static_cast<size_t>(threads / 32);
             const size_t slot = static_cast<size_t>(NR) * slice_units * ub;
-            // activations | rings | 16 B over-read pad | mbarriers | alignment slack
-            smem = act + static_cast<size_t>(threads / 32) * stages * slot + 16 +
-                   static_cast<size_t>(threads / 32) * stages * 8 + 128;
+            // activations | rings | 16 B over-read pad | partial sums | alignment slack
+            smem = act + warps * stages * slot + 16 + 2 * warps * NR * nc_t * 4 + 128;
             if (smem <= dev.smem_limit) break;
             if (stages > 2) --stages;
             else if (slice_units > 1) slice_units = (slice_units + 1) / 2;
@@ -196,14 +318,16 @@ qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_act
             p.act_bytes = static_cast<uint32_t>(act);
             p.slice_stride = static_cast<uint32_t>(slice_units * ub);
             p.slot_bytes = static_cast<uint32_t>(NR) * p.slice_stride;
-            const int warps = threads / 32;
             int occ = occupancy(dev.dev, L.fn, threads, smem);
             if (occ <= 0) return QMV_ERR_CUDA;
-            if (tu.ctas_per_sm.load() > 0) occ = std::min(occ, tu.ctas_per_sm.load());
+            // A light grid: a few CTAs per SM leave room for the next kernel's
+            // CTAs, which start streaming their weights while this one drains.
+            const int want = tu.ctas_per_sm.load() > 0 ? tu.ctas_per_sm.load() : 2;
+            occ = std::min(occ, want);
             const int64_t cap = static_cast<int64_t>(occ) * dev.num_sms;
-            const int64_t need = (p.n_groups + warps - 1) / warps;
-            int64_t gx = std::min(need, cap);
-            if (mode == MODE_MOE) gx = std::min(need, std::max<int64_t>(1, (cap + n_potential_experts - 1) / n_potential_experts));
+            int64_t gx = std::min(p.n_groups, cap);
+            if (mode == MODE_MOE)
+                gx = std::min(p.n_groups, std::max<int64_t>(1, (cap + n_potential_experts - 1) / n_potential_experts));
             L.stream = true;
             L.p = p;
             L.block = dim3(threads);
@@ -226,7 +350,7 @@ qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_act
     return QMV_OK;
 }
 
-qmv_status launch(const Launch &L, const DevInfo &dev, cudaStream_t st)
+qmv_status launch(const Launch &L, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = L.grid;
@@ -239,10 +363,11 @@ qmv_status launch(const Launch &L, const DevInfo &dev, cudaStream_t st)
     cfg.attrs = attr;
     cfg.numAttrs = g_pdl.load() ? 1 : 0;
     GemvParams p = L.p;
-    unsigned int *fault = dev.fault;
-    void *args_stream[2] = {&p, &fault};
-    void *args_generic[1] = {&p};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, L.stream ? args_stream : args_generic);
+    CUtensorMap tm0 = L.tm[0], tm1 = L.tm[1];
+    unsigned int *fault = L.fault;
+    void *args_units[4] = {&tm0, &tm1, &p, &fault};
+    void *args[1] = {&p};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, L.units ? args_units : args);
     return cuda_status(e);
 }
 
@@ -325,7 +450,7 @@ int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (!w || !W) return QMV_ERR_NULL;
     if (M <= 0 || K <= 0 || K % block_elems(type) || ldw < K) return QMV_ERR_SHAPE;
-    if (reinterpret_cast<uintptr_t>(w) % 4) return QMV_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(w) % 4 || reinterpret_cast<uintptr_t>(W) % 2) return QMV_ERR_ALIGN;
     return cuda_status(launch_quantize_weights(type, w, M, K, ldw, static_cast<uint8_t *>(W),
                                                static_cast<int64_t>(qmv_row_bytes(type, K)),
                                                static_cast<cudaStream_t>(stream)));
@@ -343,7 +468,7 @@ int qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *x
     p.y = y;
     Launch L;
     if ((s = plan(type, MODE_PLAIN, dev, p, ncols, 1, L)) != QMV_OK) return s;
-    return launch(L, dev, static_cast<cudaStream_t>(stream));
+    return launch(L, static_cast<cudaStream_t>(stream));
 }
 
 int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_up, int64_t M, int64_t K,
@@ -361,7 +486,7 @@ int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_u
     p.y = y;
     Launch L;
     if ((s = plan(type, MODE_GATE, dev, p, ncols, 1, L)) != QMV_OK) return s;
-    return launch(L, dev, static_cast<cudaStream_t>(stream));
+    return launch(L, static_cast<cudaStream_t>(stream));
 }
 
 int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const void *xq,
@@ -386,7 +511,7 @@ int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int
     const int potential = static_cast<int>(std::min<int64_t>(n_expert, static_cast<int64_t>(n_tokens) * top_k));
     Launch L;
     if ((s = plan(type, MODE_MOE, dev, p, n_tokens, potential, L)) != QMV_OK) return s;
-    return launch(L, dev, static_cast<cudaStream_t>(stream));
+    return launch(L, static_cast<cudaStream_t>(stream));
 }
 
 int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols, int32_t *out,
@@ -405,7 +530,7 @@ int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const
     p.dbg = out;
     Launch L;
     if ((s = plan(type, MODE_DEBUG, dev, p, ncols, 1, L)) != QMV_OK) return s;
-    return launch(L, dev, st);
+    return launch(L, st);
 }
 
 int qmv_device_fault(unsigned int *code)
@@ -421,17 +546,18 @@ int qmv_device_fault(unsigned int *code)
     return QMV_OK;
 }
 
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm)
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int rows_per_lane)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (threads < 0 || threads > MAX_THREADS || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
-        ctas_per_sm < 0)
+        ctas_per_sm < 0 || rows_per_lane < 0 || rows_per_lane > 2)
         return QMV_ERR_SHAPE;
     Tuning &t = g_tuning[tidx(type)];
     t.threads = threads;
     t.slice_units = slice_units;
     t.stages = stages;
     t.ctas_per_sm = ctas_per_sm;
+    t.rows_per_lane = rows_per_lane;
     return QMV_OK;
 }
 

@@ -207,6 +207,36 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// ---- per-thread asynchronous copies (cp.async, 16 bytes) --------------------
+
+// 16-byte global -> shared copy that bypasses registers and L1 (.cg); both
+// addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most n of this thread's committed copy groups are pending
+// (hardware completion of in-flight loads; n is clamped to 0..7).
+__device__ __forceinline__ void cp_async_wait(int n)
+{
+    switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
+}
+
 // ---- programmatic dependent launch ------------------------------------------
 
 // Blocks until the grids this grid depends on have completed and their memory

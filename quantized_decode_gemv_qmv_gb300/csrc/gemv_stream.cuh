@@ -7,22 +7,24 @@
 // subtracts dmin*m*d8*sum(qy), Q6_K subtracts 32*sum(qy) per sub-block).
 //
 // How it computes it is a GB300 design, not the page's:
-//   * Weights are streamed by the TMA engine (cp.async.bulk) into a per-warp
-//     ring of shared-memory slots completing on mbarriers, several slots in
-//     flight per warp, so each SM keeps tens of KB of weight reads
-//     outstanding without spending registers on them.
-//   * A warp owns R rows at a time; each ring slot holds one K-slice of those
-//     rows.  Lanes split the slice into 32-weight items (format-specific), so
-//     the shared-memory reads of a warp hit 32 distinct banks.
+//   * A light persistent grid (a few CTAs per SM) in which each CTA owns a
+//     contiguous, balanced range of row groups.  The kernel signals
+//     programmatic completion at entry and issues its first weight copies
+//     before waiting on the previous grid (griddepcontrol), so consecutive
+//     GEMVs co-reside and keep HBM busy across kernel boundaries.
+//   * Weights stream into a per-warp ring of shared-memory slots with
+//     per-lane 16-byte cp.async copies (no register cost, no per-copy engine
+//     overhead), several slots in flight per warp.
+//   * The CTA's warps split K: warp w owns a contiguous run of weight units of
+//     every row of the group; each slot holds one K-slice of R rows.  Lanes
+//     split the slice into 32-weight items (format-specific) so a warp's
+//     shared-memory reads hit 32 distinct banks.
 //   * Activations are repacked once per CTA into shared memory in the order
 //     the items read them; each item loads its activations once and reuses
 //     them for all R rows, and decodes each weight item once and reuses it for
 //     all ncols columns (the page re-decodes per column).
-//   * Lane partial sums are reduced with warp shuffles only (no cross-warp
-//     shared-memory reduction: K is not split across warps).
-//   * The kernel signals programmatic completion at entry and starts its
-//     weight stream before waiting on the previous grid (griddepcontrol), so
-//     consecutive GEMVs overlap their ramp and tail.
+//   * Lane partials are reduced with warp shuffles, the warps' partials once
+//     per row group through shared memory.
 #pragma once
 
 #include "common.cuh"
@@ -78,6 +80,7 @@ struct GemvParams {
     int slice_units;
     int n_slices;
     int stages;
+    int rpl;                // units kernel: rows per lane (1 or 2)
     uint32_t act_bytes;     // shared bytes of the activation area
     uint32_t slot_bytes;    // shared bytes of one ring slot
     uint32_t slice_stride;  // shared bytes of one row-slice inside a slot
@@ -309,15 +312,23 @@ __device__ __forceinline__ float silu_f32(float g)
 }
 
 // ---- the kernel ------------------------------------------------------------
+//
+// CTA b owns row groups [b*G/grid, (b+1)*G/grid) (G = ceil(M/R)).  Warp w
+// streams weight units [w*U/S, (w+1)*U/S) of each of those groups' rows
+// through its own ring of `stages` slots; every lane commits exactly one
+// cp.async group per slot, so "slot n has landed" is wait_group(issued-n-1)
+// followed by __syncwarp.  Ring cursors are 32-bit counters advanced
+// incrementally.  Once per group the warps' partial sums meet in shared memory
+// (double-buffered by group parity, one __syncthreads per group) and warp 0
+// writes the outputs.
 
 template <int F, int NC, int MODE>
-__global__ void __launch_bounds__(MAX_THREADS) gemv_stream_kernel(const GemvParams p, unsigned int *fault)
+__global__ void __launch_bounds__(MAX_THREADS) gemv_stream_kernel(const GemvParams p)
 {
     using T = FmtTraits<F>;
     constexpr int R = (MODE == MODE_GATE) ? NR / 2 : NR;  // output rows per group
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    // 128-byte aligned base (the host reserves 128 extra bytes): bulk-copy
-    // destinations must be 16-byte aligned.
+    // 128-byte aligned base (the host reserves 128 extra bytes)
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     __shared__ int s_tok[8];
     __shared__ uint32_t s_slots[8];
@@ -325,7 +336,7 @@ __global__ void __launch_bounds__(MAX_THREADS) gemv_stream_kernel(const GemvPara
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
+    const int S = blockDim.x >> 5;
     const int K = p.K;
     const int items_row = K >> 5;
 
@@ -368,48 +379,52 @@ __global__ void __launch_bounds__(MAX_THREADS) gemv_stream_kernel(const GemvPara
         W = p.W + (size_t)blockIdx.y * p.expert_bytes;
     }
 
-    // ring of this warp
+    // shared layout: [activations][rings S x stages x slot][16 B over-read pad][partials 2 x S x NR x NC]
     uint8_t *ring = smem + p.act_bytes + (size_t)warp * p.stages * p.slot_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.act_bytes + (size_t)nwarps * p.stages * p.slot_bytes + 16) +
-                     (size_t)warp * p.stages;
+    float *partials = reinterpret_cast<float *>(smem + p.act_bytes + (size_t)S * p.stages * p.slot_bytes + 16);
 
-    const int64_t gwarp = (int64_t)blockIdx.x * nwarps + warp;
-    const int64_t gstride = (int64_t)gridDim.x * nwarps;
-    const int64_t my_groups = gwarp < p.n_groups ? (p.n_groups - 1 - gwarp) / gstride + 1 : 0;
-    const int64_t total = my_groups * p.n_slices;
+    const int U = p.units_per_row;
+    const int ub = (warp * U) / S;            // this warp's units [ub, ue)
+    const int ue = ((warp + 1) * U) / S;
+    const int KS = p.slice_units;
+    const int n_sl = (ue - ub + KS - 1) / KS;  // slices per group (0 if the warp has no units)
+    const int64_t g_begin = (static_cast<int64_t>(blockIdx.x) * p.n_groups) / gridDim.x;
+    const int64_t g_end = (static_cast<int64_t>(blockIdx.x + 1) * p.n_groups) / gridDim.x;
+    const int64_t my_groups = g_end - g_begin;
+    const int64_t total = my_groups * n_sl;   // slices this warp streams in the whole call
     const int stages = p.stages;
-    const uint64_t policy = policy_evict_first();
 
-    auto issue = [&](int64_t n) {
-        const int slot = static_cast<int>(n % stages);
-        const int64_t grp = gwarp + (n / p.n_slices) * gstride;
-        const int s = static_cast<int>(n % p.n_slices);
-        const int64_t r0 = grp * R;
-        const int nvalid = static_cast<int>(min64(R, p.M - r0));
-        const int u0 = s * p.slice_units;
-        const int nu = min(p.slice_units, p.units_per_row - u0);
-        const uint32_t bytes = static_cast<uint32_t>(nu) * T::UNIT_BYTES;
-        const uint32_t bar = smem_u32(bars + slot);
-        const uint32_t dst = smem_u32(ring + (size_t)slot * p.slot_bytes);
-        fence_proxy_async_shared();
-        mbar_arrive_expect_tx(bar, bytes * nvalid * (MODE == MODE_GATE ? 2 : 1));
-        for (int i = 0; i < nvalid; ++i)
-            bulk_g2s(dst + i * p.slice_stride, W + (size_t)(r0 + i) * p.row_bytes + (size_t)u0 * T::UNIT_BYTES,
-                     bytes, bar, policy);
-        if constexpr (MODE == MODE_GATE)
+    // issue cursor (all lanes advance it identically)
+    int64_t is_grp = g_begin;
+    int is_s = 0, is_slot = 0;
+    int64_t issued = 0;
+    auto issue_next = [&]() {
+        if (issued < total) {
+            const int64_t r0 = is_grp * R;
+            const int nvalid = static_cast<int>(min64(R, p.M - r0));
+            const int u0 = ub + is_s * KS;
+            const int nu = min(KS, ue - u0);
+            const int bytes = nu * T::UNIT_BYTES;
+            const uint32_t dst = smem_u32(ring + (size_t)is_slot * p.slot_bytes);
+            const uint8_t *src = W + (size_t)r0 * p.row_bytes + (size_t)u0 * T::UNIT_BYTES;
             for (int i = 0; i < nvalid; ++i)
-                bulk_g2s(dst + (R + i) * p.slice_stride,
-                         W2 + (size_t)(r0 + i) * p.row_bytes + (size_t)u0 * T::UNIT_BYTES, bytes, bar, policy);
+                for (int o = 16 * lane; o < bytes; o += 512)
+                    cp_async16(dst + i * p.slice_stride + o, src + (size_t)i * p.row_bytes + o);
+            if constexpr (MODE == MODE_GATE) {
+                const uint8_t *src2 = W2 + (size_t)r0 * p.row_bytes + (size_t)u0 * T::UNIT_BYTES;
+                for (int i = 0; i < nvalid; ++i)
+                    for (int o = 16 * lane; o < bytes; o += 512)
+                        cp_async16(dst + (R + i) * p.slice_stride + o, src2 + (size_t)i * p.row_bytes + o);
+            }
+            if (++is_s == n_sl) { is_s = 0; ++is_grp; }
+            if (++is_slot == stages) is_slot = 0;
+        }
+        cp_async_commit();  // one group per slot per lane, possibly empty
+        ++issued;
     };
 
-    if (lane == 0) {
-        for (int s = 0; s < stages; ++s) mbar_init(smem_u32(bars + s), 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    const int64_t n_pre = min64(stages, total);
-    if (lane == 0)
-        for (int64_t n = 0; n < n_pre; ++n) issue(n);
+    // weights do not depend on the previous kernel: start streaming them first
+    for (int s = 0; s < stages; ++s) issue_next();
 
     if constexpr (MODE != MODE_MOE) {
         pdl_launch_dependents();
@@ -430,106 +445,102 @@ __global__ void __launch_bounds__(MAX_THREADS) gemv_stream_kernel(const GemvPara
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[i][c] = 0.f;
 
-    bool ok = true;
-    int64_t n = 0;
-    for (; n < total; ++n) {
-        const int slot = static_cast<int>(n % stages);
-        const uint32_t parity = static_cast<uint32_t>((n / stages) & 1);
-        const bool got = mbar_wait_bounded(smem_u32(bars + slot), parity);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-
-        const int64_t grp = gwarp + (n / p.n_slices) * gstride;
-        const int s = static_cast<int>(n % p.n_slices);
-        const int64_t r0 = grp * R;
+    int64_t consumed = 0;
+    int c_slot = 0;
+    for (int64_t gi = 0; gi < my_groups; ++gi) {
+        const int64_t r0 = (g_begin + gi) * R;
         const int nvalid = static_cast<int>(min64(R, p.M - r0));
-        const int u0 = s * p.slice_units;
-        const int nu = min(p.slice_units, p.units_per_row - u0);
-        const uint32_t slotp = smem_u32(ring + (size_t)slot * p.slot_bytes);
-        const int item0 = u0 * T::ITEMS_PER_UNIT;  // first item of the slice along the row
-        const int n_iter = (F == FMT_Q6_K) ? 2 * nu : (nu * T::ITEMS_PER_UNIT + 31) / 32;
+        for (int s = 0; s < n_sl; ++s) {
+            cp_async_wait(static_cast<int>(issued - consumed - 1));
+            __syncwarp();
+            const int u0 = ub + s * KS;
+            const int nu = min(KS, ue - u0);
+            const uint32_t slotp = smem_u32(ring + (size_t)c_slot * p.slot_bytes);
+            const int item0 = u0 * T::ITEMS_PER_UNIT;  // first item of the slice along the row
+            const int n_iter = (F == FMT_Q6_K) ? 2 * nu : (nu * T::ITEMS_PER_UNIT + 31) / 32;
 
-        for (int iter = 0; iter < n_iter; ++iter) {
-            int it;
-            if (F == FMT_Q6_K) {
-                // lanes 8p..8p+7 take items k = 0..7 of super-block 2p + (iter & 1)
-                // of unit iter/2: the four super-blocks of one instruction start
-                // at distinct word offsets mod 4, so the warp's shared reads
-                // fall in 32 distinct banks.
-                it = 64 * (iter >> 1) + 8 * (2 * (lane >> 3) + (iter & 1)) + (lane & 7);
-            } else {
-                it = lane + 32 * iter;
-                if (it >= nu * T::ITEMS_PER_UNIT) break;
-            }
-            const int g = item0 + it;
-            WItem w[NR];
-#pragma unroll
-            for (int i = 0; i < NR; ++i) {
-                const int row_ok = (MODE == MODE_GATE) ? ((i % R) < nvalid) : (i < nvalid);
-                if (row_ok) w[i] = decode_item<F>(slotp + i * p.slice_stride, it);
-            }
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                if (MODE != MODE_PLAIN && c >= n_active) break;
-                const AItem a = load_act(act_qs + c * K, act_sc + c * items_row * 16, g);
+            for (int iter = 0; iter < n_iter; ++iter) {
+                int it;
+                if (F == FMT_Q6_K) {
+                    // lanes 8p..8p+7 take items k = 0..7 of super-block 2p + (iter & 1)
+                    // of unit iter/2: the four super-blocks of one instruction start
+                    // at distinct word offsets mod 4, so the warp's shared reads
+                    // fall in 32 distinct banks.
+                    it = 64 * (iter >> 1) + 8 * (2 * (lane >> 3) + (iter & 1)) + (lane & 7);
+                } else {
+                    it = lane + 32 * iter;
+                    if (it >= nu * T::ITEMS_PER_UNIT) break;
+                }
+                const int g = item0 + it;
+                WItem w[NR];
 #pragma unroll
                 for (int i = 0; i < NR; ++i) {
                     const int row_ok = (MODE == MODE_GATE) ? ((i % R) < nvalid) : (i < nvalid);
-                    if (!row_ok) continue;
-                    int dlo, dhi;
-                    dots(w[i], a, dlo, dhi);
-                    if constexpr (MODE == MODE_DEBUG)
-                        debug_item<F>(p.dbg + ((size_t)c * p.M + r0 + i) * (size_t)(F == FMT_Q4_0 ? K / 32 : K / 16),
-                                      g, a, dlo, dhi);
-                    else
-                        acc[i][c] += item_value<F>(w[i], a, dlo, dhi);
+                    if (row_ok) w[i] = decode_item<F>(slotp + i * p.slice_stride, it);
+                }
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    if (MODE != MODE_PLAIN && c >= n_active) break;
+                    const AItem a = load_act(act_qs + c * K, act_sc + c * items_row * 16, g);
+#pragma unroll
+                    for (int i = 0; i < NR; ++i) {
+                        const int row_ok = (MODE == MODE_GATE) ? ((i % R) < nvalid) : (i < nvalid);
+                        if (!row_ok) continue;
+                        int dlo, dhi;
+                        dots(w[i], a, dlo, dhi);
+                        if constexpr (MODE == MODE_DEBUG)
+                            debug_item<F>(p.dbg + ((size_t)c * p.M + r0 + i) * (size_t)(F == FMT_Q4_0 ? K / 32 : K / 16),
+                                          g, a, dlo, dhi);
+                        else
+                            acc[i][c] += item_value<F>(w[i], a, dlo, dhi);
+                    }
                 }
             }
+            __syncwarp();  // every lane is done with the slot before it is refilled
+            ++consumed;
+            issue_next();
+            if (++c_slot == stages) c_slot = 0;
         }
-        __syncwarp();
-        if (lane == 0 && n + stages < total) issue(n + stages);
 
-        if (s == p.n_slices - 1) {
-            if constexpr (MODE != MODE_DEBUG) {
+        // ---- group epilogue: lanes -> warp -> CTA, then outputs ----
+        if constexpr (MODE != MODE_DEBUG) {
+            float *part = partials + (size_t)(gi & 1) * S * NR * NC;
 #pragma unroll
-                for (int i = 0; i < NR; ++i)
+            for (int i = 0; i < NR; ++i)
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) acc[i][c] = warp_sum(acc[i][c]);
-#pragma unroll
-                for (int i = 0; i < R; ++i) {
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        if (lane != ((i * NC + c) & 31) || i >= nvalid || c >= n_active) continue;
-                        const int64_t row = r0 + i;
-                        if constexpr (MODE == MODE_PLAIN) {
-                            p.y[(size_t)c * p.ldy + row] = acc[i][c];
-                        } else if constexpr (MODE == MODE_GATE) {
-                            p.y[(size_t)c * p.ldy + row] = acc[i][c] * silu_f32(acc[R + i][c]);
-                        } else {
-                            const int tok = s_tok[c];
-                            uint32_t mask = s_slots[c];
-                            while (mask) {
-                                const int k = __ffs(mask) - 1;
-                                mask &= mask - 1;
-                                p.y[((size_t)tok * p.top_k + k) * p.M + row] = acc[i][c];
-                            }
+                for (int c = 0; c < NC; ++c) {
+                    const float v = warp_sum(acc[i][c]);
+                    if (lane == 0) part[(warp * NR + i) * NC + c] = v;
+                    acc[i][c] = 0.f;
+                }
+            __syncthreads();
+            if (warp == 0) {
+                for (int idx = lane; idx < R * NC; idx += 32) {
+                    const int i = idx / NC, c = idx - (idx / NC) * NC;
+                    if (i >= nvalid || c >= n_active) continue;
+                    float v = 0.f;
+                    for (int w2 = 0; w2 < S; ++w2) v += part[(w2 * NR + i) * NC + c];
+                    const int64_t row = r0 + i;
+                    if constexpr (MODE == MODE_PLAIN) {
+                        p.y[(size_t)c * p.ldy + row] = v;
+                    } else if constexpr (MODE == MODE_GATE) {
+                        float gsum = 0.f;
+                        for (int w2 = 0; w2 < S; ++w2) gsum += part[(w2 * NR + R + i) * NC + c];
+                        p.y[(size_t)c * p.ldy + row] = v * silu_f32(gsum);
+                    } else {
+                        const int tok = s_tok[c];
+                        uint32_t mask = s_slots[c];
+                        while (mask) {
+                            const int k = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            p.y[((size_t)tok * p.top_k + k) * p.M + row] = v;
                         }
                     }
                 }
             }
-#pragma unroll
-            for (int i = 0; i < NR; ++i)
-#pragma unroll
-                for (int c = 0; c < NC; ++c) acc[i][c] = 0.f;
         }
     }
-
-    if (!ok) {
-        if (lane == 0) atomicExch(fault, FAULT_WAIT_TIMEOUT);
-        // let every copy this warp still has in flight land before exiting
-        const int64_t issued = min64(total, n + stages);
-        for (int64_t m = n; m < issued; ++m)
-            (void)mbar_wait_bounded(smem_u32(bars + (m % stages)), static_cast<uint32_t>((m / stages) & 1));
-    }
+    cp_async_wait(0);  // no copy may still target shared memory at exit
 }
 
 }  // namespace qmv

@@ -74,13 +74,17 @@ __global__ void quantize_q4_0_kernel(const float *__restrict__ w, int64_t M, int
         if (a > amax) amax = a;
     }
     const float d = __fdiv_rn(amax, 7.0f);
-    const uint32_t dh = f2h_bits(d);
-    blk[0] = dh & 0xff;
-    blk[1] = dh >> 8;
-    for (int e = 0; e < 16; ++e) {
-        const int q0 = (d == 0.0f) ? 8 : clamp_round(__fdiv_rn(v[e], d), -8.0f, 7.0f) + 8;
-        const int q1 = (d == 0.0f) ? 8 : clamp_round(__fdiv_rn(v[e + 16], d), -8.0f, 7.0f) + 8;
-        blk[2 + e] = static_cast<uint8_t>(q0 | (q1 << 4));
+    // the block is only 2-byte aligned: write it as nine 16-bit words
+    uint16_t *b16 = reinterpret_cast<uint16_t *>(blk);
+    b16[0] = static_cast<uint16_t>(f2h_bits(d));
+    for (int e = 0; e < 16; e += 2) {
+        uint32_t pair = 0;
+        for (int h = 0; h < 2; ++h) {
+            const int q0 = (d == 0.0f) ? 8 : clamp_round(__fdiv_rn(v[e + h], d), -8.0f, 7.0f) + 8;
+            const int q1 = (d == 0.0f) ? 8 : clamp_round(__fdiv_rn(v[e + h + 16], d), -8.0f, 7.0f) + 8;
+            pair |= static_cast<uint32_t>(q0 | (q1 << 4)) << (8 * h);
+        }
+        b16[1 + e / 2] = static_cast<uint16_t>(pair);
     }
 }
 

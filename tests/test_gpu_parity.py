@@ -184,10 +184,11 @@ def test_tuning_variants_agree(q, t):
     y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq, 3)
     Wd, xd = dev(W), dev(xq)
     try:
-        for threads, su, st, cps in [(32, 1, 1, 1), (64, 2, 3, 0), (256, 8, 2, 0), (128, 3, 6, 2), (96, 16, 4, 0)]:
-            q.set_tuning(t, threads, su, st, cps)
+        for threads, su, st, cps, rpl in [(32, 1, 1, 1, 1), (64, 2, 3, 0, 2), (256, 8, 2, 0, 1), (128, 3, 6, 2, 0),
+                                          (96, 16, 4, 0, 2), (128, 4, 2, 3, 1)]:
+            q.set_tuning(t, threads, su, st, cps, rpl)
             y = host(q.mul_mat_vec(t, Wd, M, K, xd, 3))
-            assert_close_l1(y, y_ref, l1, f"type {t} tuning {(threads, su, st, cps)}")
+            assert_close_l1(y, y_ref, l1, f"type {t} tuning {(threads, su, st, cps, rpl)}")
     finally:
         q.set_tuning(t)
 
