@@ -430,7 +430,7 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "gemv_stream_kernel<Q4_K, ncols=1> (avg over the step's 224 launches)",
+                     "kernel": "gemv_tiles_kernel<Q4_K, ncols=1> (avg over the step's 224 launches)",
                      "peak_kind": f"{peak_kind} HBM copy bandwidth"},
         "per_shape": per_shape,
         "hbm_frac_of_measured": round(value / peak, 4),

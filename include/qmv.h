@@ -32,11 +32,12 @@
  *     path with identical results.
  *   - Threads: calls are thread-safe; the tuning overrides below are
  *     process-wide.
- *   - Waits: the Q4_0/Q4_K streaming kernel waits on shared-memory
- *     barriers for its tensor copies; every such wait is bounded (about one
- *     second).  A wait that runs out sets a sticky device fault word, the
- *     kernel drains its copies in flight and returns without writing the
- *     affected rows; qmv_device_fault() reads and clears that word.
+ *   - Waits: the kernels contain no spin-waits.  Weight copies (cp.async)
+ *     complete in hardware and are awaited with cp.async.wait_group; the
+ *     only other synchronisation is __syncwarp/__syncthreads inside a CTA and
+ *     the programmatic-dependent-launch wait on the previous grid.
+ *     qmv_device_fault() reads a sticky device word reserved for faults a
+ *     kernel detects itself; the current kernels never set it.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -166,12 +167,20 @@ int qmv_device_fault(unsigned int *code);
 
 /* ---- tuning (process-wide) -----------------------------------------------------
  * Overrides the launch geometry the library picks for the streaming GEMV of
- * `type` (0 = keep the built-in choice for that field): threads per CTA
- * (multiple of 32, <= 256), weight units per slice (Q4_0/Q4_K: lanes per row,
- * rounded to a power of two <= 32; Q6_K: 2048-value units per slice), pipeline
- * stages, resident CTAs per SM, and rows per lane (Q4_0/Q4_K: 1 or 2).  Meant
- * for tuning sweeps. */
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int rows_per_lane);
+ * `type` (0 = keep the built-in choice for that field).  Meant for tuning
+ * sweeps; results are identical for every setting.
+ *   Q4_0 / Q4_K (tile kernel): threads = most threads per CTA (multiple of 32,
+ *     <= 384); slice_units = units of 144 bytes per tile row (4, 8 or 16:
+ *     tiles of 8, 4 or 2 rows; 8 and 2 only for one plain column);
+ *     stages = tile buffers per warp (1..4); ctas_per_sm = CTAs per SM;
+ *     smem_share = a CTA takes at most 1/smem_share of an SM's shared
+ *     memory (1..4, default 2, which leaves room for the next kernel).
+ *   Q6_K (stream kernel): threads per CTA (<= 256); slice_units = 2048-value
+ *     units per slice; stages = ring slots per warp; ctas_per_sm; smem_share
+ *     unused.
+ * Returns QMV_ERR_TYPE for a non-weight type, QMV_ERR_SHAPE for values out of
+ * range. */
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share);
 
 /* Enables (1, default) or disables (0) programmatic dependent launch for the
  * library's q8_1 and GEMV kernels.  When enabled, a GEMV may start streaming

@@ -206,8 +206,9 @@ def device_fault() -> int:
 
 
 def set_tuning(qtype: int, threads: int = 0, slice_units: int = 0, stages: int = 0, ctas_per_sm: int = 0,
-               rows_per_lane: int = 0):
-    _check("qmv_set_tuning", lib().qmv_set_tuning(qtype, threads, slice_units, stages, ctas_per_sm, rows_per_lane))
+               smem_share: int = 0):
+    """Launch-geometry override for sweeps (0 keeps the default; see include/qmv.h)."""
+    _check("qmv_set_tuning", lib().qmv_set_tuning(qtype, threads, slice_units, stages, ctas_per_sm, smem_share))
 
 
 def set_pdl(enable: bool):

@@ -6,29 +6,22 @@
 #include <mutex>
 #include <tuple>
 
-#include <cudaTypedefs.h>
-
 #include "../../include/qmv.h"
-#include "gemv_units.cuh"
+#include "gemv_tiles.cuh"
 #include "kernels.h"
 
 namespace qmv {
 
-const void *gemv_stream_fn_q4_0(int mode, int nc);
-const void *gemv_stream_fn_q4_K(int mode, int nc);
 const void *gemv_stream_fn_q6_K(int mode, int nc);
+const void *gemv_tiles_fn_q4_0(int mode, int nc, int rw);
+const void *gemv_tiles_fn_q4_K(int mode, int nc, int rw);
 const void *gemv_generic_fn_q4_0(int mode);
 const void *gemv_generic_fn_q4_K(int mode);
 const void *gemv_generic_fn_q6_K(int mode);
 
 const void *gemv_stream_fn(int type, int mode, int nc)
 {
-    switch (type) {
-    case FMT_Q4_0: return gemv_stream_fn_q4_0(mode, nc);
-    case FMT_Q4_K: return gemv_stream_fn_q4_K(mode, nc);
-    case FMT_Q6_K: return gemv_stream_fn_q6_K(mode, nc);
-    default: return nullptr;
-    }
+    return type == FMT_Q6_K ? gemv_stream_fn_q6_K(mode, nc) : nullptr;
 }
 
 const void *gemv_generic_fn(int type, int mode)
@@ -59,7 +52,8 @@ static int block_bytes(int type)
 }
 static bool weight_type(int t) { return t == FMT_Q4_0 || t == FMT_Q4_K || t == FMT_Q6_K; }
 
-// Sticky fault word written by kernels whose bounded wait ran out.
+// Sticky device fault word, reserved for kernels that detect a fault themselves
+// (a bounded wait that ran out); read and cleared by qmv_device_fault.
 __device__ unsigned int g_fault_word;
 
 namespace {
@@ -70,7 +64,7 @@ constexpr size_t SMEM_RESERVE = 1024;  // static shared memory and alignment sla
 std::atomic<int> g_pdl{1};
 
 struct Tuning {
-    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, rows_per_lane{0};
+    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0};
 };
 Tuning g_tuning[3];
 
@@ -81,6 +75,7 @@ std::map<std::tuple<int, const void *, int, size_t>, int> g_occupancy;  // (dev,
 std::map<std::pair<int, const void *>, bool> g_smem_attr;
 int g_num_sms[MAX_DEVICES];
 int g_smem_optin[MAX_DEVICES];
+int g_smem_sm[MAX_DEVICES];
 unsigned int *g_fault_ptr[MAX_DEVICES];
 
 qmv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ERR_CUDA; }
@@ -89,6 +84,7 @@ struct DevInfo {
     int dev;
     int num_sms;
     size_t smem_limit;  // dynamic shared memory a CTA may use
+    size_t smem_per_sm; // shared memory of one SM
     unsigned int *fault;
 };
 
@@ -103,6 +99,10 @@ qmv_status device_info(DevInfo &d)
         if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.dev) != cudaSuccess)
             return QMV_ERR_CUDA;
         g_smem_optin[d.dev] = optin;
+        int per_sm = 0;
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d.dev) != cudaSuccess)
+            return QMV_ERR_CUDA;
+        g_smem_sm[d.dev] = per_sm;
         void *f = nullptr;
         if (cudaGetSymbolAddress(&f, g_fault_word) != cudaSuccess) return QMV_ERR_CUDA;
         g_fault_ptr[d.dev] = static_cast<unsigned int *>(f);
@@ -110,6 +110,7 @@ qmv_status device_info(DevInfo &d)
     }
     d.num_sms = g_num_sms[d.dev];
     d.smem_limit = static_cast<size_t>(g_smem_optin[d.dev]) - SMEM_RESERVE;
+    d.smem_per_sm = static_cast<size_t>(g_smem_sm[d.dev]);
     d.fault = g_fault_ptr[d.dev];
     return QMV_OK;
 }
@@ -145,46 +146,10 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Launch {
     const void *fn = nullptr;
     bool stream = false;
-    bool units = false;       // units kernel: takes two tensor maps and the fault word
-    CUtensorMap tm[2];
-    unsigned int *fault = nullptr;
     GemvParams p{};
     dim3 grid, block;
     size_t smem = 0;
 };
-
-// Chooses the kernel and its geometry.  The streaming kernel needs 16-byte
-// aligned rows and pointers and an activation area that fits in shared memory;
-// everything else goes to the generic kernel.
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-// Tensor map viewing `rows` rows of row_bytes bytes at base as a 3D array
-// [rows][row_bytes/144 units][18 eight-byte elements], with a box of
-// 18 x box_units x box_rows.
-bool encode_rows_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t row_bytes, int box_units, int box_rows)
-{
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_encode) {
-            void *fn = nullptr;
-            cudaDriverEntryPointQueryResult q;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                    cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || !fn)
-                return false;
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
-    }
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(UNIT_B / 8), static_cast<cuuint64_t>(row_bytes / UNIT_B),
-                                static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(UNIT_B), static_cast<cuuint64_t>(row_bytes)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(UNIT_B / 8), static_cast<cuuint32_t>(box_units),
-                               static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 int pow2_at_least(int v)
 {
@@ -193,76 +158,61 @@ int pow2_at_least(int v)
     return p2;
 }
 
-// Geometry of the units kernel (Q4_0 / Q4_K): KW lanes per row (power of
-// two <= 32), RT = rows-per-lane * 32/KW rows per group, a per-warp ring of `stages` slots of NM boxes
-// of RT rows x KW units, a light grid of a few CTAs per SM.  Returns false if
-// the activations do not fit in shared memory.
-bool plan_units(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t, int n_potential_experts,
+// Geometry of the tile kernel (Q4_0 / Q4_K): warp tiles of RW rows x 32/RW
+// units, a ring of `stages` tile buffers per warp; the grid covers every SM
+// (one CTA per SM unless tuned) with up to 16 warps per CTA, each warp owning a
+// balanced contiguous range of RW-row groups.  Returns false if the
+// activations do not fit in shared memory.
+bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t, int n_potential_experts,
                 Launch &L)
 {
     const Tuning &tu = g_tuning[tidx(type)];
     const int U = static_cast<int>(p.K / 256);
-    const int NM = (mode == MODE_GATE) ? 2 : 1;
-    int KW = tu.slice_units.load() ? pow2_at_least(tu.slice_units.load()) : std::min(8, pow2_at_least(U));
-    KW = std::max(1, std::min(32, KW));
-    int threads = tu.threads.load() ? tu.threads.load() : 128;
-    threads = std::max(32, std::min(MAX_THREADS, threads / 32 * 32));
+    int rw = 4;
+    if (tu.slice_units.load()) rw = 32 / std::max(4, std::min(16, pow2_at_least(tu.slice_units.load())));
+    const void *fn = type == FMT_Q4_0 ? gemv_tiles_fn_q4_0(mode, nc_t, rw) : gemv_tiles_fn_q4_K(mode, nc_t, rw);
+    if (!fn && rw != 4) {
+        rw = 4;
+        fn = type == FMT_Q4_0 ? gemv_tiles_fn_q4_0(mode, nc_t, rw) : gemv_tiles_fn_q4_K(mode, nc_t, rw);
+    }
+    if (!fn) return false;
+    const size_t packed = align_up(static_cast<size_t>(nc_t) * U * (ACT_QS_STRIDE + ACT_SC_STRIDE), 128);
+    const size_t raw = align_up(static_cast<size_t>(nc_t) * U * 8 * Q8_1_BYTES, 128);
+    const size_t tb = static_cast<size_t>(tile_bytes_rt(rw));
     int stages = tu.stages.load() ? tu.stages.load() : 2;
-    stages = std::max(1, std::min(stages, 8));
-    int rpl = tu.rows_per_lane.load() ? tu.rows_per_lane.load() : UNITS_RPL;
-    rpl = std::max(1, std::min(UNITS_RPL, rpl));
-    const int RT = rpl * 32 / KW;
-    const int64_t rows_total = (mode == MODE_MOE) ? p.M * p.n_expert : p.M;
-    if (rows_total >= (int64_t(1) << 31)) return false;
-    const size_t box = static_cast<size_t>(RT) * KW * UNIT_B;
-    const size_t slot = static_cast<size_t>(NM) * box;
-    const size_t act = align_up(static_cast<size_t>(nc_t) * U * (ACT_QS_STRIDE + ACT_SC_STRIDE), 128);
-    size_t smem = 0;
-    for (;;) {
-        const size_t warps = static_cast<size_t>(threads / 32);
-        smem = act + warps * stages * slot + warps * stages * 8 + 128;
-        if (smem <= dev.smem_limit) break;
-        if (stages > 2) --stages;
-        else if (threads > 32) threads /= 2;
-        else return false;
-    }
-    L.fn = gemv_stream_fn(type, mode, nc_t);
-    if (!L.fn) return false;
-    if (ensure_smem_attr(dev, L.fn) != QMV_OK) return false;
-    if (!encode_rows_map(&L.tm[0], p.W, rows_total, p.row_bytes, KW, RT)) return false;
-    if (mode == MODE_GATE) {
-        if (!encode_rows_map(&L.tm[1], p.W2, rows_total, p.row_bytes, KW, RT)) return false;
-    } else {
-        L.tm[1] = L.tm[0];
-    }
-    p.units_per_row = U;
-    p.slice_units = KW;
-    p.n_slices = (U + KW - 1) / KW;
-    p.stages = stages;
-    p.rpl = rpl;
-    p.n_groups = (p.M + RT - 1) / RT;
-    p.act_bytes = static_cast<uint32_t>(act);
-    p.slice_stride = static_cast<uint32_t>(KW * UNIT_B);
-    p.slot_bytes = static_cast<uint32_t>(slot);
-    int occ = occupancy(dev.dev, L.fn, threads, smem);
-    if (occ <= 0) return false;
-    const int want = tu.ctas_per_sm.load() > 0 ? tu.ctas_per_sm.load() : 2;
-    occ = std::min(occ, want);
-    // Balanced work: with W warps at most, every warp gets k = ceil(G/W) or
-    // k-1 groups; the grid is sized so the warps' shares are as equal as the
-    // granularity allows.
-    const int warps = threads / 32;
-    int64_t max_ctas = static_cast<int64_t>(occ) * dev.num_sms;
+    stages = std::max(1, std::min(TILE_MAX_STAGES, stages));
+    int max_wpc = tu.threads.load() ? tu.threads.load() / 32 : TILE_MAX_THREADS / 32;
+    max_wpc = std::max(1, std::min(TILE_MAX_THREADS / 32, max_wpc));
+    // Budget: by default half of an SM's shared memory, so that the next
+    // kernel's CTA fits beside this one and streams its first tiles early.
+    const int share = tu.smem_share.load() > 0 ? tu.smem_share.load() : 2;
+    const size_t budget = std::min(dev.smem_limit, dev.smem_per_sm / share - SMEM_RESERVE);
+    // the raw copy of the q8_1 blocks (coalesced staging) only if it fits
+    size_t act = packed + raw;
+    if (act + tb + 128 > budget) act = packed;
+    while (max_wpc > 1 && act + static_cast<size_t>(max_wpc) * stages * tb + 128 > budget) --max_wpc;
+    while (stages > 1 && act + static_cast<size_t>(max_wpc) * stages * tb + 128 > budget) --stages;
+    if (act + static_cast<size_t>(max_wpc) * stages * tb + 128 > dev.smem_limit) return false;
+    const int cps = tu.ctas_per_sm.load() > 0 ? tu.ctas_per_sm.load() : 1;
+    int64_t max_ctas = static_cast<int64_t>(cps) * dev.num_sms;
     if (mode == MODE_MOE) max_ctas = std::max<int64_t>(1, (max_ctas + n_potential_experts - 1) / n_potential_experts);
-    const int64_t max_warps = max_ctas * warps;
-    const int64_t k = (p.n_groups + max_warps - 1) / max_warps;
-    const int64_t want_warps = (p.n_groups + k - 1) / k;
-    const int64_t gx = std::min(max_ctas, (want_warps + warps - 1) / warps);
+    const int64_t G = (p.M + rw - 1) / rw;
+    // every SM first, then more warps per CTA: warps get floor or ceil of the
+    // groups per warp
+    const int64_t gx = std::min(max_ctas, G);
+    const int64_t wpc = std::min<int64_t>(max_wpc, (G + gx - 1) / gx);
+    const size_t smem = act + static_cast<size_t>(wpc) * stages * tb + 128;
+    if (ensure_smem_attr(dev, fn) != QMV_OK) return false;
+    if (occupancy(dev.dev, fn, static_cast<int>(wpc * 32), smem) <= 0) return false;
+    p.units_per_row = U;
+    p.n_groups = G;
+    p.stages = stages;
+    p.act_bytes = static_cast<uint32_t>(act);
+    p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
+    L.fn = fn;
     L.stream = true;
-    L.units = true;
-    L.fault = dev.fault;
     L.p = p;
-    L.block = dim3(threads);
+    L.block = dim3(static_cast<unsigned>(wpc * 32));
     L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)), mode == MODE_MOE ? p.n_expert + 1 : 1);
     L.smem = smem;
     return true;
@@ -274,7 +224,7 @@ qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_act
     const int nc_t = (mode == MODE_PLAIN) ? nc_active : round_nc(nc_active);
     if (type != FMT_Q6_K && p.row_bytes % 16 == 0 && p.K % 256 == 0 && reinterpret_cast<uintptr_t>(p.W) % 16 == 0 &&
         (mode != MODE_GATE || reinterpret_cast<uintptr_t>(p.W2) % 16 == 0)) {
-        if (plan_units(type, mode, dev, p, nc_t, n_potential_experts, L)) return QMV_OK;
+        if (plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L)) return QMV_OK;
     }
     const int ub = gemv_unit_bytes(type);
     bool streamable = type == FMT_Q6_K && (p.row_bytes % 16 == 0) && (p.K % unit_elems(type) == 0) &&
@@ -363,11 +313,8 @@ qmv_status launch(const Launch &L, cudaStream_t st)
     cfg.attrs = attr;
     cfg.numAttrs = g_pdl.load() ? 1 : 0;
     GemvParams p = L.p;
-    CUtensorMap tm0 = L.tm[0], tm1 = L.tm[1];
-    unsigned int *fault = L.fault;
-    void *args_units[4] = {&tm0, &tm1, &p, &fault};
     void *args[1] = {&p};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, L.units ? args_units : args);
+    cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, args);
     return cuda_status(e);
 }
 
@@ -546,18 +493,18 @@ int qmv_device_fault(unsigned int *code)
     return QMV_OK;
 }
 
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int rows_per_lane)
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
-    if (threads < 0 || threads > MAX_THREADS || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
-        ctas_per_sm < 0 || rows_per_lane < 0 || rows_per_lane > 2)
+    if (threads < 0 || threads > 512 || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
+        ctas_per_sm < 0 || smem_share < 0 || smem_share > 4)
         return QMV_ERR_SHAPE;
     Tuning &t = g_tuning[tidx(type)];
     t.threads = threads;
     t.slice_units = slice_units;
     t.stages = stages;
     t.ctas_per_sm = ctas_per_sm;
-    t.rows_per_lane = rows_per_lane;
+    t.smem_share = smem_share;
     return QMV_OK;
 }
 

@@ -80,8 +80,8 @@ struct GemvParams {
     int slice_units;
     int n_slices;
     int stages;
-    int rpl;                // units kernel: rows per lane (1 or 2)
     uint32_t act_bytes;     // shared bytes of the activation area
+    uint32_t raw_off;       // tile kernel: offset of the raw q8_1 copy inside the activation area (0: none)
     uint32_t slot_bytes;    // shared bytes of one ring slot
     uint32_t slice_stride;  // shared bytes of one row-slice inside a slot
 };

@@ -1,0 +1,350 @@
+// Warp-tile streaming GEMV for the 144-byte-unit formats (Q4_K super-blocks;
+// Q4_0 in runs of 8 blocks), sm_103a.
+//
+// Method: "llama.cpp 源码完全拆解(十四)：mul_mat_vec_q" (vec_dot_q4_0_q8_1_impl,
+// vec_dot_q4_K_q8_1_impl_vmmq), evaluated per unit by unit_dot.
+//
+// Design (GB300-specific):
+//   * Warp tiles of RW rows x UW = 32/RW units (4,608 bytes: one unit per
+//     lane).  Each lane copies 9 of the tile's 288 16-byte pieces with
+//     cp.async; every warp-wide copy instruction covers 512 contiguous bytes
+//     of one row segment, so DRAM and L2 see whole sectors, and the data never
+//     occupies registers while in flight.
+//   * Each warp owns a ring of `stages` tile buffers.  The first `stages`
+//     tiles are requested before the kernel waits for the previous grid
+//     (programmatic dependent launch), so a GEMV's first weight bytes are on
+//     their way while the kernel before it drains; afterwards the warp refills
+//     a buffer as soon as it has decoded it.  Completion is the hardware's
+//     cp.async.wait_group: the kernel has no spin-waits and cannot hang on a
+//     copy.
+//   * Tile rows are padded in shared memory so that the 8 lanes of a 128-bit
+//     read phase (RW rows of 8/RW units) hit distinct bank quads; lane (u, r)
+//     decodes unit u of row r.  The RW lanes of one unit read the same
+//     activation addresses, which shared memory serves by broadcast.
+//   * One CTA per SM by default, of up to 12 warps and at most half of the
+//     SM's shared memory (and, for one column, registers), so that the next
+//     GEMV's CTAs fit beside it and have their first tiles in flight before
+//     this one ends.  Every warp owns a balanced contiguous range of RW-row
+//     groups; a row's partial sums meet in a warp-shuffle reduction (no
+//     cross-warp traffic).
+#pragma once
+
+#include "gemv_units.cuh"
+
+namespace qmv {
+
+constexpr int TILE_MAX_THREADS = 384;
+constexpr int TILE_PIECES = 9;  // 16-byte pieces per lane per tile (32 units x 144 B / 512 B)
+constexpr int TILE_MAX_STAGES = 4;
+
+// Shared bytes per tile row: UW units plus a pad that puts the rows of one
+// 128-bit read phase on distinct bank quads (row stride / 16 = 8/RW mod 8).
+template <int RW>
+__host__ __device__ constexpr int tile_row_stride()
+{
+    return RW == 1 ? (32 / RW) * UNIT_B : (32 / RW) * UNIT_B + ((8 / RW - (32 / RW) % 8 + 8) % 8) * 16;
+}
+
+template <int RW>
+__host__ __device__ constexpr int tile_bytes()
+{
+    return RW * tile_row_stride<RW>();
+}
+
+// Host-visible geometry: bytes of one tile buffer for RW rows per tile.
+inline int tile_bytes_rt(int rw)
+{
+    switch (rw) {
+    case 2: return tile_bytes<2>();
+    case 4: return tile_bytes<4>();
+    case 8: return tile_bytes<8>();
+    default: return 0;
+    }
+}
+
+// Activation staging of the tile kernel.  Every CTA reads the same few KB of
+// q8_1 blocks right after the dependency wait, while its weight copies keep
+// L2 busy, so the reads go out as whole 128-bit pieces (one request per 16
+// bytes instead of one per 4) into a raw shared copy, which is then repacked
+// like stage_units_activations (natural-order codes, per-block scalars).
+// Falls back to stage_units_activations when xq is not 16-byte aligned or no
+// raw area was planned.
+template <int F, int NC, typename ColFn>
+__device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint8_t *smem, int n_active, ColFn src_col)
+{
+    if (p.raw_off == 0 || (reinterpret_cast<uintptr_t>(p.xq) & 15u) != 0) {
+        stage_units_activations<F, NC>(p, smem, n_active, src_col);
+        return;
+    }
+    const int U = p.units_per_row;
+    const int nblk = U * 8;   // q8_1 blocks per column
+    const int n16 = U * 18;   // 16-byte pieces per column (8 blocks x 36 bytes per unit)
+    uint8_t *raw = smem + p.raw_off;
+    for (int idx = threadIdx.x; idx < n_active * n16; idx += blockDim.x) {
+        const int c = idx / n16;
+        const int k = idx - c * n16;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.xq + (size_t)src_col(c) * p.xq_col_bytes) + k);
+        *reinterpret_cast<uint4 *>(raw + (size_t)idx * 16) = v;
+    }
+    __syncthreads();
+    uint8_t *act_qs = smem;
+    uint8_t *act_sc = smem + (size_t)NC * U * ACT_QS_STRIDE;
+    for (int idx = threadIdx.x; idx < NC * nblk; idx += blockDim.x) {
+        const int c = idx / nblk;
+        const int n = idx - c * nblk;
+        uint32_t w[9] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (c < n_active) {
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(raw + (size_t)idx * Q8_1_BYTES);
+#pragma unroll
+            for (int i = 0; i < 9; ++i) w[i] = src[i];
+        }
+        int S = 0;
+#pragma unroll
+        for (int i = 1; i < 9; ++i) S = dp4a_ss(w[i], 0x01010101u, S);
+        const int u = n >> 3, sub = n & 7;
+        uint4 *dq = reinterpret_cast<uint4 *>(act_qs + ((size_t)c * U + u) * ACT_QS_STRIDE + 32 * sub);
+        dq[0] = make_uint4(w[1], w[2], w[3], w[4]);
+        dq[1] = make_uint4(w[5], w[6], w[7], w[8]);
+        float *sc = reinterpret_cast<float *>(act_sc + ((size_t)c * U + u) * ACT_SC_STRIDE);
+        const float d8 = half_bits_to_float(w[0]);
+        if (F == FMT_Q4_K) {
+            sc[4 * (sub >> 1) + (sub & 1)] = d8;
+            sc[4 * (sub >> 1) + 2 + (sub & 1)] = d8 * static_cast<float>(S);
+        } else {
+            sc[2 * sub] = d8;
+            sc[2 * sub + 1] = half_bits_to_float(w[0] >> 16);
+        }
+    }
+}
+
+template <int F, int NC, int MODE, int RW>
+__global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEBUG) ? 2 : 1)
+    gemv_tiles_kernel(const GemvParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    __shared__ int s_tok[8];
+    __shared__ uint32_t s_slots[8];
+    __shared__ int s_cnt;
+
+    constexpr int UW = 32 / RW;                     // units per tile row
+    constexpr int SEG = UW * 9;                     // 16-byte pieces per tile row
+    constexpr int SS = tile_row_stride<RW>();       // shared bytes per tile row
+    constexpr int TB = tile_bytes<RW>();            // shared bytes per tile
+    constexpr int NM = (MODE == MODE_GATE) ? 2 : 1;  // matrices (GATE: up, gate)
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int U = p.units_per_row;
+    const int r_l = lane % RW;  // this lane's row inside a tile
+    const int u_l = lane / RW;  // this lane's unit inside a tile
+    const int n_kt = (U + UW - 1) / UW;
+    const int64_t rb = p.row_bytes;
+    const int stages = p.stages;
+
+    pdl_launch_dependents();
+
+    int n_active = p.ncols;
+    int64_t row_base = 0;  // MoE: first row of this CTA's expert
+    if constexpr (MODE == MODE_MOE) {
+        pdl_wait();  // the expert ids come from the previous grid
+        if (blockIdx.y == static_cast<unsigned>(p.n_expert)) {
+            int bad = 0;
+            for (int s = 0; s < p.n_tokens * p.top_k; ++s) {
+                const int e = p.ids[s];
+                if (e < 0 || e >= p.n_expert) {
+                    ++bad;
+                    float *ys = p.y + (size_t)s * p.M;
+                    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < p.M;
+                         r += (int64_t)gridDim.x * blockDim.x)
+                        ys[r] = 0.f;
+                }
+            }
+            if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) *p.status = bad;
+            return;
+        }
+        if (threadIdx.x == 0) {
+            int cnt = 0;
+            for (int t = 0; t < p.n_tokens; ++t) {
+                uint32_t mask = 0;
+                for (int k = 0; k < p.top_k; ++k)
+                    if (p.ids[t * p.top_k + k] == static_cast<int>(blockIdx.y)) mask |= 1u << k;
+                if (mask) { s_tok[cnt] = t; s_slots[cnt] = mask; ++cnt; }
+            }
+            s_cnt = cnt;
+        }
+        __syncthreads();
+        n_active = s_cnt;
+        if (n_active == 0) return;
+        row_base = static_cast<int64_t>(blockIdx.y) * p.M;
+    }
+
+    // every warp of the grid owns a contiguous, balanced range of row groups
+    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
+    const int64_t wtot = static_cast<int64_t>(gridDim.x) * nwarps;
+    const int64_t g_begin = (gwarp * p.n_groups) / wtot;
+    const int64_t my_groups = ((gwarp + 1) * p.n_groups) / wtot - g_begin;
+    const int64_t total = my_groups * n_kt * NM;
+
+    const uint32_t ring = smem_u32(smem + p.act_bytes) + static_cast<uint32_t>(warp * stages * TB);
+
+    // ---- copies: tile (group, k-tile, matrix) -> ring buffer, one group per tile ----
+    int64_t ld_g = g_begin;
+    int ld_kt = 0, ld_m = 0, ld_buf = 0;
+    int64_t issued = 0;
+    auto issue_tile = [&]() {
+        const uint8_t *W = (NM == 2 && ld_m) ? p.W2 : p.W;
+        const int64_t grow = ld_g * RW;  // first row of the group inside the matrix
+        const uint8_t *base = W + (row_base + grow) * rb + static_cast<int64_t>(ld_kt) * (UW * UNIT_B);
+        const int64_t rows_left = p.M - grow;
+        const int lim = 9 * min(UW, U - ld_kt * UW);  // valid pieces per tile row
+        const uint32_t dst = ring + static_cast<uint32_t>(ld_buf * TB);
+#pragma unroll
+        for (int j = 0; j < TILE_PIECES; ++j) {
+            const int i = 32 * j + lane;
+            const int seg = i / SEG;
+            const int off = i - seg * SEG;
+            if (off < lim && seg < rows_left) cp_async16(dst + seg * SS + off * 16, base + seg * rb + off * 16);
+        }
+        cp_async_commit();
+        if (++ld_m == NM) {
+            ld_m = 0;
+            if (++ld_kt == n_kt) { ld_kt = 0; ++ld_g; }
+        }
+        if (++ld_buf == stages) ld_buf = 0;
+        ++issued;
+    };
+
+    while (issued < total && issued < stages) issue_tile();  // weights first
+
+    if constexpr (MODE != MODE_MOE) pdl_wait();
+    if constexpr (MODE == MODE_MOE)
+        stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; });
+    else
+        stage_tile_activations<F, NC>(p, smem, n_active, [](int c) { return c; });
+    __syncthreads();
+
+    const uint32_t act_qs = smem_u32(smem);
+    const uint32_t act_sc = act_qs + NC * U * ACT_QS_STRIDE;
+
+    float acc[NM][NC];
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[m][c] = 0.f;
+
+    int64_t cg = g_begin;  // compute position
+    int ckt = 0, cm = 0, cbuf = 0;
+    for (int64_t t = 0; t < total; ++t) {
+        cp_async_wait(static_cast<int>(issued - t - 1));  // tile t has landed (this lane's pieces)
+        __syncwarp();                                     // ... and every lane's
+
+        const int64_t row = cg * RW + r_l;
+        const int u = ckt * UW + u_l;
+        if (u < U && row < p.M) {
+            uint32_t ub[1] = {ring + static_cast<uint32_t>(cbuf * TB) + r_l * SS + u_l * UNIT_B};
+            const bool live[1] = {true};
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                if (MODE != MODE_PLAIN && c >= n_active) break;
+                const uint32_t aq = act_qs + (c * U + u) * ACT_QS_STRIDE;
+                const uint32_t as = act_sc + (c * U + u) * ACT_SC_STRIDE;
+                float vv[1] = {0.f};
+                int32_t *dbg[1] = {nullptr};
+                if constexpr (MODE == MODE_DEBUG) {
+                    dbg[0] = p.dbg + ((size_t)c * p.M + row) * (size_t)(F == FMT_Q4_0 ? p.K / 32 : p.K / 16) +
+                             (size_t)u * (F == FMT_Q4_0 ? 8 : 16);
+                    unit_dot<F, 1, true>(ub, live, aq, as, vv, dbg);
+                } else {
+                    unit_dot<F, 1, false>(ub, live, aq, as, vv, dbg);
+                    if (NM == 2 && cm) acc[NM - 1][c] += vv[0];
+                    else acc[0][c] += vv[0];
+                }
+            }
+        }
+        __syncwarp();  // every lane is done with the buffer
+        if (issued < total) issue_tile();
+
+        const bool group_done = (ckt == n_kt - 1) && (cm == NM - 1);
+        if constexpr (MODE != MODE_DEBUG) {
+            if (group_done) {
+                // the lanes of one row are those with the same r_l (xor over the unit bits)
+#pragma unroll
+                for (int m = 0; m < NM; ++m)
+#pragma unroll
+                    for (int c = 0; c < NC; ++c)
+#pragma unroll
+                        for (int o = 16; o >= RW; o >>= 1) acc[m][c] += __shfl_xor_sync(0xffffffffu, acc[m][c], o);
+                if (u_l == 0 && row < p.M) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        if (c >= n_active) break;
+                        if constexpr (MODE == MODE_PLAIN) {
+                            p.y[(size_t)c * p.ldy + row] = acc[0][c];
+                        } else if constexpr (MODE == MODE_GATE) {
+                            p.y[(size_t)c * p.ldy + row] = acc[0][c] * silu_f32(acc[NM - 1][c]);
+                        } else {
+                            const int tok = s_tok[c];
+                            uint32_t mask = s_slots[c];
+                            while (mask) {
+                                const int k = __ffs(mask) - 1;
+                                mask &= mask - 1;
+                                p.y[((size_t)tok * p.top_k + k) * p.M + row] = acc[0][c];
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < NM; ++m)
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) acc[m][c] = 0.f;
+            }
+        }
+        if (++cm == NM) {
+            cm = 0;
+            if (++ckt == n_kt) { ckt = 0; ++cg; }
+        }
+        if (++cbuf == stages) cbuf = 0;
+    }
+}
+
+// Kernel table of the tile path for one format (instantiated only in that
+// format's translation unit).  RW = 4 serves every mode and column count;
+// RW = 2 and 8 exist for one plain column, for geometry sweeps.
+template <int F>
+const void *tiles_kernel_fn(int mode, int nc, int rw)
+{
+#define QMV_TK(NC_, MODE_, RW_) reinterpret_cast<const void *>(&gemv_tiles_kernel<F, NC_, MODE_, RW_>)
+    if (rw == 2) return (mode == MODE_PLAIN && nc == 1) ? QMV_TK(1, MODE_PLAIN, 2) : nullptr;
+    if (rw == 8) return (mode == MODE_PLAIN && nc == 1) ? QMV_TK(1, MODE_PLAIN, 8) : nullptr;
+    if (rw != 4) return nullptr;
+    if (mode == MODE_PLAIN) {
+        switch (nc) {
+        case 1: return QMV_TK(1, MODE_PLAIN, 4);
+        case 2: return QMV_TK(2, MODE_PLAIN, 4);
+        case 3: return QMV_TK(3, MODE_PLAIN, 4);
+        case 4: return QMV_TK(4, MODE_PLAIN, 4);
+        case 5: return QMV_TK(5, MODE_PLAIN, 4);
+        case 6: return QMV_TK(6, MODE_PLAIN, 4);
+        case 7: return QMV_TK(7, MODE_PLAIN, 4);
+        case 8: return QMV_TK(8, MODE_PLAIN, 4);
+        default: return nullptr;
+        }
+    }
+#define QMV_TK_MODE(MODE_)                    \
+    switch (nc) {                             \
+    case 1: return QMV_TK(1, MODE_, 4);       \
+    case 2: return QMV_TK(2, MODE_, 4);       \
+    case 4: return QMV_TK(4, MODE_, 4);       \
+    case 8: return QMV_TK(8, MODE_, 4);       \
+    default: return nullptr;                  \
+    }
+    if (mode == MODE_GATE) { QMV_TK_MODE(MODE_GATE) }
+    if (mode == MODE_MOE) { QMV_TK_MODE(MODE_MOE) }
+    if (mode == MODE_DEBUG) { QMV_TK_MODE(MODE_DEBUG) }
+#undef QMV_TK_MODE
+#undef QMV_TK
+    return nullptr;
+}
+
+}  // namespace qmv

@@ -88,6 +88,7 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_debug_subblock_sums(14, p, 4, 256, p, 0, p, nul) == 4
     # tuning knobs validate too
     assert L.qmv_set_tuning(12, 100, 0, 0, 0, 0) == 3
-    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 3) == 3
+    assert L.qmv_set_tuning(12, 544, 0, 0, 0, 0) == 3
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 5) == 3
     assert L.qmv_set_tuning(3, 0, 0, 0, 0, 0) == 2
     assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0) == 0

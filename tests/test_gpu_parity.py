@@ -177,18 +177,21 @@ def test_generic_path_for_unaligned_weights(q):
 
 
 @pytest.mark.parametrize("t", oracle.WEIGHT_TYPES)
-def test_tuning_variants_agree(q, t):
+@pytest.mark.parametrize("nc", [1, 3])
+def test_tuning_variants_agree(q, t, nc):
+    # geometry overrides (threads, units per tile row / slice, stages, CTAs per
+    # SM, shared-memory share) change the launch, never the result
     M, K = 130, 4096
     W = weights(t, M, K, 700 + t)
-    xq = oracle.quantize_q8_1(synthetic.activations_f32(701, 3, K))
-    y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq, 3)
+    xq = oracle.quantize_q8_1(synthetic.activations_f32(701, nc, K))
+    y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq, nc)
     Wd, xd = dev(W), dev(xq)
     try:
-        for threads, su, st, cps, rpl in [(32, 1, 1, 1, 1), (64, 2, 3, 0, 2), (256, 8, 2, 0, 1), (128, 3, 6, 2, 0),
-                                          (96, 16, 4, 0, 2), (128, 4, 2, 3, 1)]:
-            q.set_tuning(t, threads, su, st, cps, rpl)
-            y = host(q.mul_mat_vec(t, Wd, M, K, xd, 3))
-            assert_close_l1(y, y_ref, l1, f"type {t} tuning {(threads, su, st, cps, rpl)}")
+        for tune in [(32, 1, 1, 1, 1), (64, 2, 3, 0, 2), (256, 8, 2, 0, 1), (128, 3, 6, 2, 0), (96, 16, 4, 0, 2),
+                     (128, 4, 2, 3, 1), (384, 16, 1, 1, 4), (384, 4, 4, 2, 1)]:
+            q.set_tuning(t, *tune)
+            y = host(q.mul_mat_vec(t, Wd, M, K, xd, nc))
+            assert_close_l1(y, y_ref, l1, f"type {t} ncols {nc} tuning {tune}")
     finally:
         q.set_tuning(t)
 
