@@ -2,21 +2,21 @@
 """Benchmark: Q4_K decode GEMV on GB300.
 
 Workload (one "step"): one decode token through the quantized GEMVs of a
-Llama-7B-shaped model -- 32 layers, each with q/k/v/o (4096x4096), gate/up
-(11008x4096) and down (4096x11008) Q4_K matrices at ncols = 1 -- including the
-q8_1 quantization of every GEMV input (4 per layer: attention input, output
-projection input, FFN input, down projection input).  3.64 GB of distinct
-weights per step, far larger than the 129 MB L2, so no flush is needed.
-Weights are seeded N(0, 0.02) fp32 quantized on the device by the library's
-Q4_K quantizer (bit-identical to the CPU oracle's); activations are seeded
-N(0, 1) with 1 % outliers x20.  The step is captured once in a CUDA graph and
-replayed.
+Llama-7B-shaped model at ncols = 1 -- 32 layers, each with the q, k, v
+projections stacked into one 12288x4096 matrix, o (4096x4096), gate and up
+(11008x4096 each, one fused SwiGLU launch) and down (4096x11008, fed by the
+gate/up output) -- with the q8_1 quantization of every input fused into its
+GEMV: 128 launches and 3.64 GB of distinct Q4_K weights per step, far larger
+than the 129 MB L2, so no flush is needed.  Weights are seeded N(0, 0.02)
+fp32 quantized on the device by the library's Q4_K quantizer (bit-identical
+to the CPU oracle's); activations are seeded N(0, 1) with 1 % outliers x20.
+The step is captured once in a CUDA graph and replayed.
 
-Reported metric: weight GB/s of the whole step (value), the roofline of the
-GEMV kernel (algorithmic bytes per launch over its CUDA-event duration against
-the measured HBM copy bandwidth), microseconds per call per shape, an
-end-to-end number through the public API with host buffers, and the CPU
-oracle timed on the host cores.
+Reported: weight GB/s of the whole step (value); the roofline of the GEMV
+kernel over the step's own launches (algorithmic bytes over CUDA-event time
+against the measured HBM copy bandwidth); microseconds per call of the
+q8_1-input GEMV at the three Llama-7B shapes; an end-to-end number through
+the public API with host buffers; and the CPU oracle timed on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -36,16 +36,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Q4_K/Q6_K GEMV weight GB/s and % of GB300 HBM roofline; µs/call at ncols=1"
-WORKLOAD = "llama-7b decode step, Q4_K GEMV ncols=1: 32 layers x (q,k,v,o 4096x4096; gate,up 11008x4096; down 4096x11008)"
+WORKLOAD = ("llama-7b decode step, Q4_K GEMV ncols=1, q8_1 quantization fused into each GEMV: 32 layers x "
+            "(qkv 12288x4096 [q,k,v stacked]; o 4096x4096; gate+up 2x11008x4096 fused SwiGLU; down 4096x11008)")
 N_LAYERS = 32
 D_MODEL, D_FF = 4096, 11008
 Q4_K = 12
 QK_K, Q4_K_BYTES = 256, 144
-# matrices of one layer: (name, M, K, input index)
+# launches of one layer: (name, rows, K, matrices)
+STEP = [("qkv", 3 * D_MODEL, D_MODEL, 1), ("o", D_MODEL, D_MODEL, 1), ("gate_up", D_FF, D_MODEL, 2),
+        ("down", D_MODEL, D_FF, 1)]
+# the seven matrices of one layer, for the CPU oracle legs (same bytes as STEP)
 LAYER = [("q", D_MODEL, D_MODEL, 0), ("k", D_MODEL, D_MODEL, 0), ("v", D_MODEL, D_MODEL, 0),
          ("o", D_MODEL, D_MODEL, 1), ("gate", D_FF, D_MODEL, 2), ("up", D_FF, D_MODEL, 2),
          ("down", D_MODEL, D_FF, 3)]
-INPUT_K = [D_MODEL, D_MODEL, D_MODEL, D_FF]
 SHAPES = {"4096x4096": (D_MODEL, D_MODEL), "11008x4096": (D_FF, D_MODEL), "4096x11008": (D_MODEL, D_FF)}
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
@@ -63,8 +66,13 @@ def q8_1_bytes_unpadded(K):
 
 
 def algorithmic_bytes(M, K):
-    """W + q8_1 activations (unpadded) + fp32 outputs for one GEMV launch."""
+    """W + q8_1 activations (unpadded) + fp32 outputs for one q8_1-input GEMV launch."""
     return M * row_bytes(M, K) + q8_1_bytes_unpadded(K) + 4 * M
+
+
+def fused_bytes(M, K, nmat):
+    """W (nmat matrices) + fp32 activations + fp32 outputs for one fused-input launch."""
+    return nmat * M * row_bytes(M, K) + 4 * K + 4 * M
 
 
 def csrc_sha():
@@ -275,46 +283,55 @@ def run_gpu(args):
     q.set_pdl(True)
     stream = torch.cuda.Stream(device=device)
 
-    # ---- weights: 32 layers x 7 matrices, quantized on the device -------------------
+    # ---- weights: 32 layers x (qkv, o, gate + up, down), quantized on the device -----
     weights = []
     with torch.cuda.stream(stream):
         for layer in range(N_LAYERS):
             lw = {}
-            for mi, (name, M, K, _) in enumerate(LAYER):
-                seed = 1_000_000 + 100 * layer + mi
-                w = synthetic.device_normal_f32(seed, (M, K), 0.02, device)
-                lw[name] = q.quantize_weights(Q4_K, w, stream=stream)
-                del w
+            for si, (name, M, K, nmat) in enumerate(STEP):
+                mats = []
+                for mi in range(nmat):
+                    w = synthetic.device_normal_f32(1_000_000 + 100 * layer + 10 * si + mi, (M, K), 0.02, device)
+                    mats.append(q.quantize_weights(Q4_K, w, stream=stream))
+                    del w
+                lw[name] = mats
             weights.append(lw)
     stream.synchronize()
-    weight_bytes = sum(t.numel() for lw in weights for t in lw.values())
+    weight_bytes = sum(t.numel() for lw in weights for mats in lw.values() for t in mats)
 
-    # ---- per-step inputs (fp32 activations, host-generated, seeded) ----------------
-    xs_host = []
-    for layer in range(N_LAYERS):
-        xs_host.append([synthetic.activations_f32(2_000_000 + 10 * layer + i, 1, INPUT_K[i], outlier_frac=0.01)[0]
-                        for i in range(4)])
-    in_sizes = [INPUT_K[i] for i in range(4)] * N_LAYERS
+    # ---- per-step inputs: attention input, attention output, FFN input per layer ---------
+    n_in = 3
+    xs_host = [[synthetic.activations_f32(2_000_000 + 10 * layer + i, 1, D_MODEL, outlier_frac=0.01)[0]
+                for i in range(n_in)] for layer in range(N_LAYERS)]
     x_flat_host = torch.from_numpy(np.concatenate([x for lx in xs_host for x in lx])).pin_memory()
     x_flat = x_flat_host.to(device)
-    offs = np.concatenate([[0], np.cumsum(in_sizes)])
-    xs = [[x_flat[offs[4 * l + i]:offs[4 * l + i + 1]] for i in range(4)] for l in range(N_LAYERS)]
-    xqs = [[torch.empty((1, q.q8_1_bytes(INPUT_K[i])), dtype=torch.uint8, device=device) for i in range(4)]
-           for _ in range(N_LAYERS)]
-    out_sizes = [M for (_, M, _, _) in LAYER] * N_LAYERS
-    y_flat = torch.empty(sum(out_sizes), dtype=torch.float32, device=device)
-    y_flat_host = torch.empty(sum(out_sizes), dtype=torch.float32).pin_memory()
-    yoff = np.concatenate([[0], np.cumsum(out_sizes)])
-    ys = [[y_flat[yoff[7 * l + m]:yoff[7 * l + m + 1]].view(1, -1) for m in range(7)] for l in range(N_LAYERS)]
+    xs = [[x_flat[(n_in * l + i) * D_MODEL:(n_in * l + i + 1) * D_MODEL].view(1, -1) for i in range(n_in)]
+          for l in range(N_LAYERS)]
+    # outputs returned to the host: qkv, o, down per layer; the SwiGLU activation stays on the device
+    out_rows = [3 * D_MODEL, D_MODEL, D_MODEL]
+    y_flat = torch.empty(N_LAYERS * sum(out_rows), dtype=torch.float32, device=device)
+    y_flat_host = torch.empty(y_flat.numel(), dtype=torch.float32).pin_memory()
+    yoff = np.concatenate([[0], np.cumsum(out_rows * N_LAYERS)])
+    ys = [[y_flat[yoff[3 * l + m]:yoff[3 * l + m + 1]].view(1, -1) for m in range(3)] for l in range(N_LAYERS)]
+    acts = [torch.empty((1, D_FF), dtype=torch.float32, device=device) for _ in range(N_LAYERS)]
+
+    def launch(l, name):
+        W = weights[l][name]
+        if name == "qkv":
+            q.mul_mat_vec_f32(Q4_K, W[0], 3 * D_MODEL, D_MODEL, xs[l][0], out=ys[l][0], stream=stream)
+        elif name == "o":
+            q.mul_mat_vec_f32(Q4_K, W[0], D_MODEL, D_MODEL, xs[l][1], out=ys[l][1], stream=stream)
+        elif name == "gate_up":
+            q.mul_mat_vec_gate_up_swiglu_f32(Q4_K, W[0], W[1], D_FF, D_MODEL, xs[l][2], out=acts[l], stream=stream)
+        else:
+            q.mul_mat_vec_f32(Q4_K, W[0], D_MODEL, D_FF, acts[l], out=ys[l][2], stream=stream)
 
     def step_calls():
         for l in range(N_LAYERS):
-            for i in range(4):
-                q.quantize_q8_1(xs[l][i].view(1, -1), out=xqs[l][i], stream=stream)
-            for m, (name, M, K, inp) in enumerate(LAYER):
-                q.mul_mat_vec(Q4_K, weights[l][name], M, K, xqs[l][inp], 1, out=ys[l][m], stream=stream)
+            for name, _, _, _ in STEP:
+                launch(l, name)
 
-    launches_per_step = N_LAYERS * (4 + len(LAYER))
+    launches_per_step = N_LAYERS * len(STEP)
 
     # warm up eagerly (loads modules, caches geometry), then capture one step
     with torch.cuda.stream(stream):
@@ -325,16 +342,28 @@ def run_gpu(args):
         step_calls()
     stream.synchronize()
 
-    # per-shape GEMV-only graphs (same launch configuration, inputs pre-quantized)
-    shape_graphs = {}
-    for shape_name, (Ms, Ks) in SHAPES.items():
-        calls = [(l, m) for l in range(N_LAYERS) for m, (_, M, K, _) in enumerate(LAYER) if (M, K) == (Ms, Ks)]
+    # the step's launches grouped by kind (same calls, same configuration), for the roofline
+    kind_graphs = {}
+    for name, M, K, nmat in STEP:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for l, m in calls:
-                name, M, K, inp = LAYER[m]
-                q.mul_mat_vec(Q4_K, weights[l][name], M, K, xqs[l][inp], 1, out=ys[l][m], stream=stream)
-        shape_graphs[shape_name] = (g, len(calls))
+            for l in range(N_LAYERS):
+                launch(l, name)
+        kind_graphs[name] = g
+    # q8_1-input GEMV chains at the three Llama-7B shapes (the pages' per-call figure)
+    xq4 = q.quantize_q8_1(xs[0][0], stream=stream)
+    xq11 = q.quantize_q8_1(acts[0], stream=stream)
+    shape_w = {"4096x4096": [weights[l]["o"][0] for l in range(N_LAYERS)],
+               "11008x4096": [w for l in range(N_LAYERS) for w in weights[l]["gate_up"]],
+               "4096x11008": [weights[l]["down"][0] for l in range(N_LAYERS)]}
+    y_shape = torch.empty((1, D_FF), dtype=torch.float32, device=device)
+    shape_graphs = {}
+    for shape_name, (Ms, Ks) in SHAPES.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for W in shape_w[shape_name]:
+                q.mul_mat_vec(Q4_K, W, Ms, Ks, xq4 if Ks == D_MODEL else xq11, 1, out=y_shape[:, :Ms], stream=stream)
+        shape_graphs[shape_name] = (g, len(shape_w[shape_name]))
     stream.synchronize()
 
     # ---- timed region: the step ----------------------------------------------------
@@ -357,12 +386,7 @@ def run_gpu(args):
     step_ms = max_over_ranks(step_ms, world, device)
     value = world * weight_bytes / (step_ms * 1e-3) / 1e9
 
-    # ---- dominant kernel: GEMV-only timing per shape (CUDA events on the stream) -------
-    per_shape = {}
-    tot_bytes, tot_time, tot_launches = 0.0, 0.0, 0
-    reps = max(3, min(20, args.steps // 5 or 3))
-    for shape_name, (g, n) in shape_graphs.items():
-        Ms, Ks = SHAPES[shape_name]
+    def time_graph(g, n_calls, reps):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -374,13 +398,27 @@ def run_gpu(args):
                 g.replay()
             e1.record(stream)
             stream.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * n)
-        b = algorithmic_bytes(Ms, Ks)
+        return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
+
+    reps = max(3, min(20, args.steps // 5 or 3))
+    # ---- dominant kernel: the step's GEMV launches by kind (CUDA events on the stream) --
+    kinds = {}
+    tot_bytes, tot_time = 0.0, 0.0
+    for name, M, K, nmat in STEP:
+        us = time_graph(kind_graphs[name], N_LAYERS, reps)
+        b = fused_bytes(M, K, nmat)
+        kinds[name] = {"rows": M, "K": K, "matrices": nmat, "us_per_call": round(us, 3),
+                       "weight_gbs": round(nmat * M * row_bytes(M, K) / us / 1e3, 1),
+                       "algorithmic_gbs": round(b / us / 1e3, 1)}
+        tot_bytes += b * N_LAYERS
+        tot_time += us * N_LAYERS
+    per_shape = {}
+    for shape_name, (g, n) in shape_graphs.items():
+        Ms, Ks = SHAPES[shape_name]
+        us = time_graph(g, n, reps)
         per_shape[shape_name] = {"us_per_call": round(us, 3), "weight_gbs": round(Ms * row_bytes(Ms, Ks) / us / 1e3, 1),
-                                 "algorithmic_gbs": round(b / us / 1e3, 1), "launches_timed": reps * n}
-        tot_bytes += b * n
-        tot_time += us * n
-        tot_launches += n
+                                 "algorithmic_gbs": round(algorithmic_bytes(Ms, Ks) / us / 1e3, 1),
+                                 "launches_timed": reps * n, "input": "q8_1"}
     peak, peak_kind = measured_peaks()
     achieved = tot_bytes / tot_time / 1e3  # GB/s
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["csrc_sha"] == csrc_sha() else None
@@ -425,14 +463,15 @@ def run_gpu(args):
         "vs_baseline": None, "dtype": "int8/fp32",
         "data": "synthetic: seeded N(0,0.02) weights quantized to Q4_K on device; N(0,1) activations, 1% outliers x20",
         "config": {"workload": WORKLOAD, "ncols": 1, "layers": N_LAYERS, "weight_bytes_per_step": weight_bytes,
-                   "gemv_launches_per_step": N_LAYERS * len(LAYER), "quantize_launches_per_step": N_LAYERS * 4,
+                   "gemv_launches_per_step": launches_per_step, "quantize_launches_per_step": 0,
                    "l2": "no flush: 3.64 GB of distinct weights per step > 129 MB L2",
                    "execution": "CUDA graph of the step, programmatic dependent launch between kernels",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "gemv_tiles_kernel<Q4_K, ncols=1> (avg over the step's 224 launches)",
+                     "kernel": "gemv_tiles_kernel<Q4_K, ncols=1, fp32 input> (the step's 128 launches by kind)",
                      "peak_kind": f"{peak_kind} HBM copy bandwidth"},
+        "step_kernels": kinds,
         "per_shape": per_shape,
         "hbm_frac_of_measured": round(value / peak, 4),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -446,8 +485,10 @@ def run_gpu(args):
 
 
 def run_kernel_only(args):
-    """A few GEMV launches of one shape (for profiler captures): two distinct
-    weight copies alternate so consecutive launches do not hit in L2."""
+    """A few GEMV launches of one shape (for profiler captures): four distinct
+    weight copies rotate so consecutive launches do not hit in L2.  A config
+    shape (e.g. 4096x11008) runs the q8_1-input GEMV; a step kind (qkv, o,
+    gate_up, down) runs the step's fused fp32-input launch."""
     import torch
 
     import synthetic
@@ -456,19 +497,31 @@ def run_kernel_only(args):
     __graft_entry__.build()
     import quantized_decode_gemv_qmv_gb300 as q
 
-    if args.kernel_only not in SHAPES:
-        raise SystemExit(f"unknown shape {args.kernel_only}; choose from {list(SHAPES)}")
-    M, K = SHAPES[args.kernel_only]
     torch.cuda.set_device(0)
-    Ws = [q.quantize_weights(Q4_K, synthetic.device_normal_f32(7 + i, (M, K), 0.02, "cuda")) for i in range(4)]
+    kinds = {name: (M, K, nmat) for name, M, K, nmat in STEP}
+    if args.kernel_only in SHAPES:
+        M, K = SHAPES[args.kernel_only]
+        nmat = 1
+    elif args.kernel_only in kinds:
+        M, K, nmat = kinds[args.kernel_only]
+    else:
+        raise SystemExit(f"unknown shape {args.kernel_only}; choose from {list(SHAPES) + list(kinds)}")
+    Ws = [[q.quantize_weights(Q4_K, synthetic.device_normal_f32(7 + 2 * i + m, (M, K), 0.02, "cuda"))
+           for m in range(nmat)] for i in range(4)]
     x = torch.from_numpy(synthetic.activations_f32(9, 1, K, outlier_frac=0.01)).cuda()
     xq = q.quantize_q8_1(x)
     y = torch.empty((1, M), dtype=torch.float32, device="cuda")
     for i in range(args.launches):
-        q.mul_mat_vec(Q4_K, Ws[i % len(Ws)], M, K, xq, 1, out=y)
+        W = Ws[i % len(Ws)]
+        if args.kernel_only in SHAPES:
+            q.mul_mat_vec(Q4_K, W[0], M, K, xq, 1, out=y)
+        elif nmat == 2:
+            q.mul_mat_vec_gate_up_swiglu_f32(Q4_K, W[0], W[1], M, K, x, out=y)
+        else:
+            q.mul_mat_vec_f32(Q4_K, W[0], M, K, x, out=y)
     torch.cuda.synchronize()
     print(json.dumps({"kernel_only": args.kernel_only, "launches": args.launches,
-                      "weight_bytes_per_launch": int(Ws[0].numel())}))
+                      "weight_bytes_per_launch": int(sum(w.numel() for w in Ws[0]))}))
     return 0
 
 
@@ -480,7 +533,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=6.0, help="CPU-baseline timing budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-only", default=None, help="profiling aid: only GEMV launches of one shape")
+    ap.add_argument("--kernel-only", default=None, help="profiling aid: only GEMV launches of one shape or step kind")
     ap.add_argument("--launches", type=int, default=8)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps

@@ -149,6 +149,30 @@ int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int
                        const void *xq, const int32_t *ids, int n_tokens, int top_k, float *y,
                        int32_t *dev_status, void *stream);
 
+/* ---- GEMV with the activation quantization fused in ---------------------------
+ * The same products with fp32 activations: x holds ncols columns of K floats
+ * (MoE: one column per token), column c at x + c*ldx (ldx >= K, x 4-byte
+ * aligned; 16-byte alignment of x and of ldx*4 enables 128-bit loads).  Each
+ * CTA quantizes x to q8_1 in shared memory with the arithmetic of
+ * qmv_quantize_q8_1 (mul_mat_vec_q page, sections "激活的量化" and "PDL":
+ * here the quantize pass is not a separate kernel at all), so y is
+ * bit-identical to qmv_quantize_q8_1 followed by the q8_1-input call, with one
+ * kernel launch instead of two.  Available for Q4_0 and Q4_K with K a
+ * multiple of 256 and W (and W_gate) 16-byte aligned; otherwise returns
+ * QMV_ERR_TYPE (Q6_K), QMV_ERR_SHAPE or QMV_ERR_ALIGN before launching, and
+ * the q8_1-input calls apply.  Arguments, limits, outputs and error behaviour
+ * are otherwise those of the calls above. */
+int qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const float *x, int64_t ldx,
+                        int ncols, float *y, void *stream);
+
+int qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void *W_up, int64_t M,
+                                       int64_t K, const float *x, int64_t ldx, int ncols, float *y,
+                                       void *stream);
+
+int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M, int64_t K,
+                           const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k,
+                           float *y, int32_t *dev_status, void *stream);
+
 /* ---- verification --------------------------------------------------------------
  * The exact int32 intermediates of the block formulas, computed by the same
  * device code as qmv_mul_mat_vec (for bit-exact parity tests).  out is

@@ -27,7 +27,8 @@ MAX_COLS = 8
 EXPORTS = (
     "qmv_status_str", "qmv_version", "qmv_row_bytes", "qmv_q8_1_padded_k", "qmv_q8_1_bytes",
     "qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec", "qmv_mul_mat_vec_gate_up_swiglu",
-    "qmv_mul_mat_vec_id", "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_pdl",
+    "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32", "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32",
+    "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_pdl",
 )
 
 
@@ -69,12 +70,17 @@ def lib():
         L.qmv_mul_mat_vec.argtypes = [_int, _vp, _i64, _i64, _vp, _int, _vp, _vp]
         L.qmv_mul_mat_vec_gate_up_swiglu.argtypes = [_int, _vp, _vp, _i64, _i64, _vp, _int, _vp, _vp]
         L.qmv_mul_mat_vec_id.argtypes = [_int, _vp, _i64, _i64, _i64, _vp, _vp, _int, _int, _vp, _vp, _vp]
+        L.qmv_mul_mat_vec_f32.argtypes = [_int, _vp, _i64, _i64, _vp, _i64, _int, _vp, _vp]
+        L.qmv_mul_mat_vec_gate_up_swiglu_f32.argtypes = [_int, _vp, _vp, _i64, _i64, _vp, _i64, _int, _vp, _vp]
+        L.qmv_mul_mat_vec_id_f32.argtypes = [_int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _int, _vp, _vp,
+                                             _vp]
         L.qmv_debug_subblock_sums.argtypes = [_int, _vp, _i64, _i64, _vp, _int, _vp, _vp]
         L.qmv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.qmv_set_tuning.argtypes = [_int, _int, _int, _int, _int, _int]
         L.qmv_set_pdl.argtypes = [_int]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
-                     "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_debug_subblock_sums",
+                     "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
+                     "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_pdl"):
             getattr(L, name).restype = _int
         _lib = L
@@ -185,6 +191,60 @@ def mul_mat_vec_id(qtype: int, W, n_expert: int, M: int, K: int, xq, ids, out=No
     _check("qmv_mul_mat_vec_id",
            lib().qmv_mul_mat_vec_id(qtype, _ptr(W), n_expert, M, K, _ptr(xq), _ptr(ids), n_tokens, top_k,
                                     _ptr(out), _ptr(status), _stream_handle(stream)))
+    return out
+
+
+# ---- GEMV with fp32 activations (quantization fused into the GEMV) ---------------
+def _x2d(x):
+    import torch
+
+    x2 = x.unsqueeze(0) if x.dim() == 1 else x
+    if not x2.is_cuda or x2.dtype != torch.float32:
+        raise ValueError("x must be a float32 CUDA tensor")
+    if x2.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    return x2
+
+
+def mul_mat_vec_f32(qtype: int, W, M: int, K: int, x, out=None, stream=None):
+    """y[ncols][M] = W . x for fp32 x [ncols][K] (rows may be strided)."""
+    import torch
+
+    x2 = _x2d(x)
+    ncols = x2.shape[0]
+    if out is None:
+        out = torch.empty((ncols, M), dtype=torch.float32, device=W.device)
+    _check("qmv_mul_mat_vec_f32", lib().qmv_mul_mat_vec_f32(qtype, _ptr(W), M, K, _ptr(x2), x2.stride(0), ncols,
+                                                            _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mul_mat_vec_gate_up_swiglu_f32(qtype: int, W_gate, W_up, M: int, K: int, x, out=None, stream=None):
+    """y[ncols][M] = (W_up . x) * silu(W_gate . x) for fp32 x [ncols][K]."""
+    import torch
+
+    x2 = _x2d(x)
+    ncols = x2.shape[0]
+    if out is None:
+        out = torch.empty((ncols, M), dtype=torch.float32, device=W_up.device)
+    _check("qmv_mul_mat_vec_gate_up_swiglu_f32",
+           lib().qmv_mul_mat_vec_gate_up_swiglu_f32(qtype, _ptr(W_gate), _ptr(W_up), M, K, _ptr(x2), x2.stride(0),
+                                                    ncols, _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mul_mat_vec_id_f32(qtype: int, W, n_expert: int, M: int, K: int, x, ids, out=None, status=None, stream=None):
+    """Expert-indexed GEMV with fp32 tokens x [n_tokens][K]: y[t][k][M] = W[ids[t][k]] . x[t]."""
+    import torch
+
+    x2 = _x2d(x)
+    _need_cuda(ids, "ids", torch.int32)
+    n_tokens, top_k = ids.shape
+    if out is None:
+        out = torch.empty((n_tokens, top_k, M), dtype=torch.float32, device=W.device)
+    _check("qmv_mul_mat_vec_id_f32",
+           lib().qmv_mul_mat_vec_id_f32(qtype, _ptr(W), n_expert, M, K, _ptr(x2), x2.stride(0), _ptr(ids), n_tokens,
+                                        top_k, _ptr(out), _ptr(status), _stream_handle(stream)))
     return out
 
 

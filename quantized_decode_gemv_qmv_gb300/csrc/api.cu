@@ -187,9 +187,10 @@ bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t,
     // kernel's CTA fits beside this one and streams its first tiles early.
     const int share = tu.smem_share.load() > 0 ? tu.smem_share.load() : 2;
     const size_t budget = std::min(dev.smem_limit, dev.smem_per_sm / share - SMEM_RESERVE);
-    // the raw copy of the q8_1 blocks (coalesced staging) only if it fits
+    // the raw copy of the q8_1 blocks (coalesced staging) only if it fits; fp32
+    // input is quantized straight into the packed layout
     size_t act = packed + raw;
-    if (act + tb + 128 > budget) act = packed;
+    if (p.xf != nullptr || act + tb + 128 > budget) act = packed;
     while (max_wpc > 1 && act + static_cast<size_t>(max_wpc) * stages * tb + 128 > budget) --max_wpc;
     while (stages > 1 && act + static_cast<size_t>(max_wpc) * stages * tb + 128 > budget) --stages;
     if (act + static_cast<size_t>(max_wpc) * stages * tb + 128 > dev.smem_limit) return false;
@@ -216,6 +217,30 @@ bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t,
     L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)), mode == MODE_MOE ? p.n_expert + 1 : 1);
     L.smem = smem;
     return true;
+}
+
+// Host checks of the fused fp32-input path (before any CUDA call): the tile
+// kernel only, i.e. Q4_0 / Q4_K, K % 256 == 0, 16-byte aligned weights.
+qmv_status check_f32(int type, const void *W, const void *W2, int64_t K, int64_t ldx)
+{
+    if (type == FMT_Q6_K) return QMV_ERR_TYPE;
+    if (K % 256 != 0 || ldx < K) return QMV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(W) % 16 != 0 || (W2 && reinterpret_cast<uintptr_t>(W2) % 16 != 0))
+        return QMV_ERR_ALIGN;
+    return QMV_OK;
+}
+
+qmv_status plan_f32(int type, int mode, const DevInfo &dev, GemvParams p, int nc_active, int n_potential_experts,
+                    Launch &L)
+{
+    const int nc_t = (mode == MODE_PLAIN) ? nc_active : round_nc(nc_active);
+    if (type == FMT_Q6_K) return QMV_ERR_TYPE;
+    if (p.K % 256 != 0 || p.row_bytes % 16 != 0) return QMV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(p.W) % 16 != 0 ||
+        (mode == MODE_GATE && reinterpret_cast<uintptr_t>(p.W2) % 16 != 0))
+        return QMV_ERR_ALIGN;
+    if (!plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L)) return QMV_ERR_SHAPE;
+    return QMV_OK;
 }
 
 qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_active, int n_potential_experts,
@@ -458,6 +483,74 @@ int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int
     const int potential = static_cast<int>(std::min<int64_t>(n_expert, static_cast<int64_t>(n_tokens) * top_k));
     Launch L;
     if ((s = plan(type, MODE_MOE, dev, p, n_tokens, potential, L)) != QMV_OK) return s;
+    return launch(L, static_cast<cudaStream_t>(stream));
+}
+
+int qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const float *x, int64_t ldx, int ncols,
+                        float *y, void *stream)
+{
+    qmv_status s = check_common(type, W, M, K, x, y);
+    if (s != QMV_OK) return s;
+    if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    if ((s = check_f32(type, W, nullptr, K, ldx)) != QMV_OK) return s;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W, M, K, nullptr, ncols);
+    p.xf = x;
+    p.ldx = ldx;
+    p.y = y;
+    Launch L;
+    if ((s = plan_f32(type, MODE_PLAIN, dev, p, ncols, 1, L)) != QMV_OK) return s;
+    return launch(L, static_cast<cudaStream_t>(stream));
+}
+
+int qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void *W_up, int64_t M, int64_t K,
+                                       const float *x, int64_t ldx, int ncols, float *y, void *stream)
+{
+    qmv_status s = check_common(type, W_up, M, K, x, y);
+    if (s != QMV_OK) return s;
+    if (!W_gate) return QMV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(W_gate) % 2) return QMV_ERR_ALIGN;
+    if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    if ((s = check_f32(type, W_up, W_gate, K, ldx)) != QMV_OK) return s;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W_up, M, K, nullptr, ncols);
+    p.W2 = static_cast<const uint8_t *>(W_gate);
+    p.xf = x;
+    p.ldx = ldx;
+    p.y = y;
+    Launch L;
+    if ((s = plan_f32(type, MODE_GATE, dev, p, ncols, 1, L)) != QMV_OK) return s;
+    return launch(L, static_cast<cudaStream_t>(stream));
+}
+
+int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const float *x,
+                           int64_t ldx, const int32_t *ids, int n_tokens, int top_k, float *y, int32_t *dev_status,
+                           void *stream)
+{
+    qmv_status s = check_common(type, W, M, K, x, y);
+    if (s != QMV_OK) return s;
+    if (!ids) return QMV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(ids) % 4 || reinterpret_cast<uintptr_t>(dev_status) % 4) return QMV_ERR_ALIGN;
+    if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
+    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
+    if ((s = check_f32(type, W, nullptr, K, ldx)) != QMV_OK) return s;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W, M, K, nullptr, n_tokens);
+    p.xf = x;
+    p.ldx = ldx;
+    p.y = y;
+    p.ids = ids;
+    p.status = dev_status;
+    p.n_tokens = n_tokens;
+    p.top_k = top_k;
+    p.n_expert = static_cast<int>(n_expert);
+    p.expert_bytes = M * p.row_bytes;
+    const int potential = static_cast<int>(std::min<int64_t>(n_expert, static_cast<int64_t>(n_tokens) * top_k));
+    Launch L;
+    if ((s = plan_f32(type, MODE_MOE, dev, p, n_tokens, potential, L)) != QMV_OK) return s;
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 

@@ -207,6 +207,37 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// ---- loads of inputs written by the previous grid ---------------------------
+// Activations (and ids) may be produced by the kernel this one overlaps under
+// programmatic dependent launch, so they are read after the dependency wait
+// through L2 (ld.global.cg), never through the read-only path that assumes the
+// data is constant for the kernel's lifetime.
+
+__device__ __forceinline__ uint4 ld_cg_u4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_cg_f4(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
 // ---- per-thread asynchronous copies (cp.async, 16 bytes) --------------------
 
 // 16-byte global -> shared copy that bypasses registers and L1 (.cg); both

@@ -63,6 +63,8 @@ struct GemvParams {
     const uint8_t *W;    // weights (MoE: expert 0); GATE: the up matrix
     const uint8_t *W2;   // GATE: the gate matrix
     const uint8_t *xq;   // q8_1 activations, column c at xq + c*xq_col_bytes
+    const float *xf;     // fp32 activations quantized in place (tile kernel), column c at xf + c*ldx; or null
+    int64_t ldx;
     float *y;            // PLAIN/GATE: y[c*ldy + r]; MOE: y[(t*top_k + k)*M + r]
     int32_t *dbg;        // DEBUG: per-sub-block int sums
     const int32_t *ids;  // MOE: [n_tokens][top_k]

@@ -30,12 +30,14 @@
 #pragma once
 
 #include "gemv_units.cuh"
+#include "q8_1.cuh"
 
 namespace qmv {
 
 constexpr int TILE_MAX_THREADS = 384;
 constexpr int TILE_PIECES = 9;  // 16-byte pieces per lane per tile (32 units x 144 B / 512 B)
 constexpr int TILE_MAX_STAGES = 4;
+constexpr int STAGE_BATCH = 4;  // activation loads in flight per thread while staging
 
 // Shared bytes per tile row: UW units plus a pad that puts the rows of one
 // 128-bit read phase on distinct bank quads (row stride / 16 = 8/RW mod 8).
@@ -69,9 +71,68 @@ inline int tile_bytes_rt(int rw)
 // like stage_units_activations (natural-order codes, per-block scalars).
 // Falls back to stage_units_activations when xq is not 16-byte aligned or no
 // raw area was planned.
+//
+// With fp32 input (p.xf) the activations are quantized here, straight into the
+// repacked layout, with the q8_1 block arithmetic of the standalone quantizer
+// (q8_1.cuh): the staged values, and so y, are bit-identical to quantizing
+// first and passing the q8_1 blocks.
 template <int F, int NC, typename ColFn>
 __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint8_t *smem, int n_active, ColFn src_col)
 {
+    if (p.xf != nullptr) {
+        const int U = p.units_per_row;
+        const int nblk = U * 8;                 // q8_1 blocks per column (K = 256 U)
+        const int tasks = n_active * nblk * 4;  // 4 lanes per block
+        const bool vec = ((reinterpret_cast<uintptr_t>(p.xf) | static_cast<uintptr_t>(p.ldx * 4)) & 15u) == 0;
+        uint8_t *act_qs = smem;
+        uint8_t *act_sc = smem + (size_t)NC * U * ACT_QS_STRIDE;
+        const int rounds = (tasks + blockDim.x - 1) / blockDim.x;  // the same for every thread
+        // STAGE_BATCH rounds of loads in flight before any is consumed: one
+        // L2 round trip per batch, not per round
+        for (int r0 = 0; r0 < rounds; r0 += STAGE_BATCH) {
+            float v[STAGE_BATCH][8];
+#pragma unroll
+            for (int r = 0; r < STAGE_BATCH; ++r) {
+                const int t = (r0 + r) * blockDim.x + threadIdx.x;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[r][i] = 0.f;
+                if (r0 + r < rounds && t < tasks) {
+                    const int c = t / (nblk * 4);
+                    const int rem = t - c * nblk * 4;
+                    q8_1_load8(p.xf + (size_t)src_col(c) * p.ldx, (int64_t)(rem >> 2) * QK8_1 + 8 * (rem & 3), p.K,
+                               vec, v[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < STAGE_BATCH; ++r) {
+                if (r0 + r >= rounds) break;  // uniform: every lane reaches the group reductions
+                const int t = (r0 + r) * blockDim.x + threadIdx.x;
+                uint32_t w0, w1, ds;
+                int S;
+                q8_1_block_group4(v[r], w0, w1, ds, S);
+                if (t < tasks) {
+                    const int c = t / (nblk * 4);
+                    const int rem = t - c * nblk * 4;
+                    const int n = rem >> 2, j = rem & 3;
+                    const int u = n >> 3, sub = n & 7;
+                    uint2 *dq = reinterpret_cast<uint2 *>(act_qs + ((size_t)c * U + u) * ACT_QS_STRIDE + 32 * sub + 8 * j);
+                    *dq = make_uint2(w0, w1);
+                    if (j == 0) {
+                        float *sc = reinterpret_cast<float *>(act_sc + ((size_t)c * U + u) * ACT_SC_STRIDE);
+                        const float d8 = half_bits_to_float(ds);
+                        if (F == FMT_Q4_K) {
+                            sc[4 * (sub >> 1) + (sub & 1)] = d8;
+                            sc[4 * (sub >> 1) + 2 + (sub & 1)] = d8 * static_cast<float>(S);
+                        } else {
+                            sc[2 * sub] = d8;
+                            sc[2 * sub + 1] = half_bits_to_float(ds >> 16);
+                        }
+                    }
+                }
+            }
+        }
+        return;
+    }
     if (p.raw_off == 0 || (reinterpret_cast<uintptr_t>(p.xq) & 15u) != 0) {
         stage_units_activations<F, NC>(p, smem, n_active, src_col);
         return;
@@ -80,11 +141,23 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
     const int nblk = U * 8;   // q8_1 blocks per column
     const int n16 = U * 18;   // 16-byte pieces per column (8 blocks x 36 bytes per unit)
     uint8_t *raw = smem + p.raw_off;
-    for (int idx = threadIdx.x; idx < n_active * n16; idx += blockDim.x) {
-        const int c = idx / n16;
-        const int k = idx - c * n16;
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.xq + (size_t)src_col(c) * p.xq_col_bytes) + k);
-        *reinterpret_cast<uint4 *>(raw + (size_t)idx * 16) = v;
+    const int total16 = n_active * n16;
+    for (int base = 0; base < total16; base += STAGE_BATCH * blockDim.x) {  // STAGE_BATCH loads in flight
+        uint4 v[STAGE_BATCH];
+#pragma unroll
+        for (int r = 0; r < STAGE_BATCH; ++r) {
+            const int idx = base + r * blockDim.x + threadIdx.x;
+            if (idx < total16) {
+                const int c = idx / n16;
+                const int k = idx - c * n16;
+                v[r] = ld_cg_u4(p.xq + (size_t)src_col(c) * p.xq_col_bytes + (size_t)k * 16);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < STAGE_BATCH; ++r) {
+            const int idx = base + r * blockDim.x + threadIdx.x;
+            if (idx < total16) *reinterpret_cast<uint4 *>(raw + (size_t)idx * 16) = v[r];
+        }
     }
     __syncthreads();
     uint8_t *act_qs = smem;

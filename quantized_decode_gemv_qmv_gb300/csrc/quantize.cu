@@ -4,57 +4,41 @@
 // (__fdiv_rn, __fmul_rn, __fadd_rn: never fused or reassociated), C roundf
 // (halfway cases away from zero) and round-to-nearest-even half conversion,
 // so the bytes are a deterministic function of the input floats.
-#include "common.cuh"
 #include "kernels.h"
+#include "q8_1.cuh"
 
 namespace qmv {
 
-__device__ __forceinline__ int clamp_round(float z, float lo, float hi)
-{
-    float r = roundf(z);
-    if (r < lo) r = lo;
-    if (r > hi) r = hi;
-    return static_cast<int>(r);
-}
-
-__device__ __forceinline__ uint32_t f2h_bits(float f)
-{
-    return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(f)));
-}
-
-__device__ __forceinline__ float h2f(uint32_t bits)
-{
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
-}
-
 // ---- q8_1 ------------------------------------------------------------------
-// "llama.cpp 源码完全拆解(十四)：mul_mat_vec_q", quantize_q8_1 kernel: one warp
-// per 32-value block, amax and the code sum reduced by warp shuffles.  Values
-// past K read as zero (the 512-padding).  s = half(d * sum(q)).
+// "llama.cpp 源码完全拆解(十四)：mul_mat_vec_q", quantize_q8_1 kernel, with the
+// block arithmetic of q8_1.cuh (shared with the GEMVs that quantize their fp32
+// input in place): 4 lanes per 32-value block, 8 values per lane.  Values past
+// K read as zero (the 512-padding).
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restrict__ x, int64_t K, int64_t ldx,
                                                             int64_t nb_pad, int64_t n_blocks,
                                                             uint8_t *__restrict__ xq)
 {
     pdl_launch_dependents();
     pdl_wait();  // x may be the output of the previous kernel
-    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (gw >= n_blocks) return;  // uniform per warp
-    const int lane = threadIdx.x & 31;
-    const int64_t c = gw / nb_pad;
-    const int64_t k = (gw - c * nb_pad) * QK8_1 + lane;
-    const float v = k < K ? x[c * ldx + k] : 0.0f;
-    const float amax = warp_max(fabsf(v));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const int q = (d == 0.0f) ? 0 : clamp_round(__fdiv_rn(v, d), -127.0f, 127.0f);
-    const int sum = warp_sum_int(q);
-    // pack four codes per 32-bit store
-    const uint32_t b0 = static_cast<uint32_t>(q) & 0xffu;
-    const uint32_t b1 = static_cast<uint32_t>(__shfl_down_sync(0xffffffffu, q, 1)) & 0xffu;
-    const uint32_t b2 = static_cast<uint32_t>(__shfl_down_sync(0xffffffffu, q, 2)) & 0xffu;
-    const uint32_t b3 = static_cast<uint32_t>(__shfl_down_sync(0xffffffffu, q, 3)) & 0xffu;
-    uint32_t *blk = reinterpret_cast<uint32_t *>(xq + gw * Q8_1_BYTES);
-    if ((lane & 3) == 0) blk[1 + (lane >> 2)] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-    if (lane == 0) blk[0] = f2h_bits(d) | (f2h_bits(__fmul_rn(d, static_cast<float>(sum))) << 16);
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t blk = t >> 2;
+    const int j = static_cast<int>(t & 3);
+    const bool ok = blk < n_blocks;  // every lane still joins the group reductions
+    const int64_t b = ok ? blk : 0;
+    const int64_t c = b / nb_pad;
+    const int64_t k = (b - c * nb_pad) * QK8_1 + 8 * j;
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) | static_cast<uintptr_t>(ldx * 4)) & 15u) == 0;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (ok) q8_1_load8(x + c * ldx, k, K, vec, v);
+    uint32_t w0, w1, ds;
+    int sum;
+    q8_1_block_group4(v, w0, w1, ds, sum);
+    if (ok) {
+        uint32_t *o = reinterpret_cast<uint32_t *>(xq + b * Q8_1_BYTES);
+        o[1 + 2 * j] = w0;
+        o[2 + 2 * j] = w1;
+        if (j == 0) o[0] = ds;
+    }
 }
 
 // ---- Q4_0 --------------------------------------------------------------------
@@ -208,7 +192,7 @@ cudaError_t launch_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t l
     const int64_t nb_pad = (K + ROW_PAD - 1) / ROW_PAD * ROW_PAD / QK8_1;
     const int64_t n_blocks = nb_pad * ncols;
     const int threads = 256;
-    const int64_t grid = (n_blocks * 32 + threads - 1) / threads;
+    const int64_t grid = (n_blocks * 4 + threads - 1) / threads;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
