@@ -12,16 +12,21 @@
 
 namespace qmv {
 
-const void *gemv_stream_fn_q6_K(int mode, int nc);
 const void *gemv_tiles_fn_q4_0(int mode, int nc, int rw);
 const void *gemv_tiles_fn_q4_K(int mode, int nc, int rw);
+const void *gemv_tiles_fn_q6_K(int mode, int nc, int rw);
 const void *gemv_generic_fn_q4_0(int mode);
 const void *gemv_generic_fn_q4_K(int mode);
 const void *gemv_generic_fn_q6_K(int mode);
 
-const void *gemv_stream_fn(int type, int mode, int nc)
+const void *gemv_tiles_fn(int type, int mode, int nc, int rw)
 {
-    return type == FMT_Q6_K ? gemv_stream_fn_q6_K(mode, nc) : nullptr;
+    switch (type) {
+    case FMT_Q4_0: return gemv_tiles_fn_q4_0(mode, nc, rw);
+    case FMT_Q4_K: return gemv_tiles_fn_q4_K(mode, nc, rw);
+    case FMT_Q6_K: return gemv_tiles_fn_q6_K(mode, nc, rw);
+    default: return nullptr;
+    }
 }
 
 const void *gemv_generic_fn(int type, int mode)
@@ -34,17 +39,6 @@ const void *gemv_generic_fn(int type, int mode)
     }
 }
 
-int gemv_unit_bytes(int type)
-{
-    switch (type) {
-    case FMT_Q4_0: return FmtTraits<FMT_Q4_0>::UNIT_BYTES;
-    case FMT_Q4_K: return FmtTraits<FMT_Q4_K>::UNIT_BYTES;
-    case FMT_Q6_K: return FmtTraits<FMT_Q6_K>::UNIT_BYTES;
-    default: return 0;
-    }
-}
-
-static int unit_elems(int type) { return type == FMT_Q6_K ? 2048 : 256; }
 static int block_elems(int type) { return type == FMT_Q4_0 ? QK4_0 : QK_K; }
 static int block_bytes(int type)
 {
@@ -64,7 +58,7 @@ constexpr size_t SMEM_RESERVE = 1024;  // static shared memory and alignment sla
 std::atomic<int> g_pdl{1};
 
 struct Tuning {
-    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0};
+    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0}, flags{0};
 };
 Tuning g_tuning[3];
 
@@ -158,10 +152,18 @@ int pow2_at_least(int v)
     return p2;
 }
 
-// Geometry of the tile kernel (Q4_0 / Q4_K): warp tiles of RW rows x 32/RW
-// units, a ring of `stages` tile buffers per warp; the grid covers every SM
-// (one CTA per SM unless tuned) with up to 16 warps per CTA, each warp owning a
-// balanced contiguous range of RW-row groups.  Returns false if the
+// Rows the tile kernel takes: whole 16-byte pieces per row and whole tile
+// units (Q4_0 / Q4_K: K % 256 == 0; Q6_K: K % 2048 == 0, eight 210-byte
+// super-blocks per tile row), 16-byte aligned weights.
+bool tile_shape_ok(int type, int64_t K, int64_t row_bytes)
+{
+    return row_bytes % 16 == 0 && K % (type == FMT_Q6_K ? 2048 : 256) == 0;
+}
+
+// Geometry of the tile kernel: warp tiles of RW rows x 32/RW units, a ring of
+// `stages` tile buffers per warp; the grid covers every SM (one CTA per SM
+// unless tuned) with up to 12 warps per CTA, every warp owning a balanced
+// contiguous range of RW-row groups.  Returns false if the
 // activations do not fit in shared memory.
 bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t, int n_potential_experts,
                 Launch &L)
@@ -170,46 +172,54 @@ bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t,
     const int U = static_cast<int>(p.K / 256);
     int rw = 4;
     if (tu.slice_units.load()) rw = 32 / std::max(4, std::min(16, pow2_at_least(tu.slice_units.load())));
-    const void *fn = type == FMT_Q4_0 ? gemv_tiles_fn_q4_0(mode, nc_t, rw) : gemv_tiles_fn_q4_K(mode, nc_t, rw);
+    const void *fn = gemv_tiles_fn(type, mode, nc_t, rw);
     if (!fn && rw != 4) {
         rw = 4;
-        fn = type == FMT_Q4_0 ? gemv_tiles_fn_q4_0(mode, nc_t, rw) : gemv_tiles_fn_q4_K(mode, nc_t, rw);
+        fn = gemv_tiles_fn(type, mode, nc_t, rw);
     }
     if (!fn) return false;
-    const size_t packed = align_up(static_cast<size_t>(nc_t) * U * (ACT_QS_STRIDE + ACT_SC_STRIDE), 128);
+    const int sc_stride = type == FMT_Q6_K ? act_sc_stride<FMT_Q6_K>() : act_sc_stride<FMT_Q4_K>();
+    const size_t packed = align_up(static_cast<size_t>(nc_t) * U * (ACT_QS_STRIDE + sc_stride), 128);
     const size_t raw = align_up(static_cast<size_t>(nc_t) * U * 8 * Q8_1_BYTES, 128);
-    const size_t tb = static_cast<size_t>(tile_bytes_rt(rw));
+    const size_t tb = static_cast<size_t>(tile_bytes_rt(type, rw));
     int stages = tu.stages.load() ? tu.stages.load() : 2;
     stages = std::max(1, std::min(TILE_MAX_STAGES, stages));
     int max_wpc = tu.threads.load() ? tu.threads.load() / 32 : TILE_MAX_THREADS / 32;
     max_wpc = std::max(1, std::min(TILE_MAX_THREADS / 32, max_wpc));
-    // Budget: by default half of an SM's shared memory, so that the next
-    // kernel's CTA fits beside this one and streams its first tiles early.
-    const int share = tu.smem_share.load() > 0 ? tu.smem_share.load() : 2;
-    const size_t budget = std::min(dev.smem_limit, dev.smem_per_sm / share - SMEM_RESERVE);
-    // the raw copy of the q8_1 blocks (coalesced staging) only if it fits; fp32
-    // input is quantized straight into the packed layout
-    size_t act = packed + raw;
-    if (p.xf != nullptr || act + tb + 128 > budget) act = packed;
-    while (max_wpc > 1 && act + static_cast<size_t>(max_wpc) * stages * tb + 128 > budget) --max_wpc;
-    while (stages > 1 && act + static_cast<size_t>(max_wpc) * stages * tb + 128 > budget) --stages;
-    if (act + static_cast<size_t>(max_wpc) * stages * tb + 128 > dev.smem_limit) return false;
+
+    // grid: every SM first (MoE: the SMs shared among the experts that may be
+    // picked), then more warps per CTA; warps own whole row groups
     const int cps = tu.ctas_per_sm.load() > 0 ? tu.ctas_per_sm.load() : 1;
     int64_t max_ctas = static_cast<int64_t>(cps) * dev.num_sms;
     if (mode == MODE_MOE) max_ctas = std::max<int64_t>(1, (max_ctas + n_potential_experts - 1) / n_potential_experts);
     const int64_t G = (p.M + rw - 1) / rw;
-    // every SM first, then more warps per CTA: warps get floor or ceil of the
-    // groups per warp
     const int64_t gx = std::min(max_ctas, G);
-    const int64_t wpc = std::min<int64_t>(max_wpc, (G + gx - 1) / gx);
-    const size_t smem = act + static_cast<size_t>(wpc) * stages * tb + 128;
+    max_wpc = static_cast<int>(std::min<int64_t>(max_wpc, (G + gx - 1) / gx));
+    // Budget: by default half of an SM's shared memory, so that the next
+    // kernel's CTA fits beside this one and streams its first tiles early.
+    // Warps and stages are fixed from the packed activations alone, so the
+    // fp32-input and q8_1-input launches of a shape share one geometry (and
+    // produce bit-identical results).
+    const int share = tu.smem_share.load() > 0 ? tu.smem_share.load() : 2;
+    const size_t budget = std::min(dev.smem_limit, dev.smem_per_sm / share - SMEM_RESERVE);
+    auto need = [&](int w, int st, size_t act) { return act + static_cast<size_t>(w) * st * tb + 128; };
+    while (max_wpc > 1 && need(max_wpc, stages, packed) > budget) --max_wpc;
+    while (stages > 1 && need(max_wpc, stages, packed) > budget) --stages;
+    if (need(max_wpc, stages, packed) > dev.smem_limit) return false;
+    // the raw copy of the q8_1 blocks (coalesced staging) only if it still fits;
+    // fp32 input is quantized straight into the packed layout
+    size_t act = packed;
+    if (p.xf == nullptr && need(max_wpc, stages, packed + raw) <= budget) act = packed + raw;
+    const int wpc = max_wpc;
+    const size_t smem = need(wpc, stages, act);
     if (ensure_smem_attr(dev, fn) != QMV_OK) return false;
-    if (occupancy(dev.dev, fn, static_cast<int>(wpc * 32), smem) <= 0) return false;
+    if (occupancy(dev.dev, fn, wpc * 32, smem) <= 0) return false;
     p.units_per_row = U;
     p.n_groups = G;
     p.stages = stages;
     p.act_bytes = static_cast<uint32_t>(act);
     p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
+    p.flags = static_cast<uint32_t>(tu.flags.load());
     L.fn = fn;
     L.stream = true;
     L.p = p;
@@ -220,11 +230,11 @@ bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t,
 }
 
 // Host checks of the fused fp32-input path (before any CUDA call): the tile
-// kernel only, i.e. Q4_0 / Q4_K, K % 256 == 0, 16-byte aligned weights.
+// kernel only (Q4_0 / Q4_K: K % 256 == 0; Q6_K: K % 2048 == 0), 16-byte aligned
+// weights.
 qmv_status check_f32(int type, const void *W, const void *W2, int64_t K, int64_t ldx)
 {
-    if (type == FMT_Q6_K) return QMV_ERR_TYPE;
-    if (K % 256 != 0 || ldx < K) return QMV_ERR_SHAPE;
+    if (K % (type == FMT_Q6_K ? 2048 : 256) != 0 || ldx < K) return QMV_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(W) % 16 != 0 || (W2 && reinterpret_cast<uintptr_t>(W2) % 16 != 0))
         return QMV_ERR_ALIGN;
     return QMV_OK;
@@ -234,8 +244,7 @@ qmv_status plan_f32(int type, int mode, const DevInfo &dev, GemvParams p, int nc
                     Launch &L)
 {
     const int nc_t = (mode == MODE_PLAIN) ? nc_active : round_nc(nc_active);
-    if (type == FMT_Q6_K) return QMV_ERR_TYPE;
-    if (p.K % 256 != 0 || p.row_bytes % 16 != 0) return QMV_ERR_SHAPE;
+    if (!tile_shape_ok(type, p.K, p.row_bytes)) return QMV_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(p.W) % 16 != 0 ||
         (mode == MODE_GATE && reinterpret_cast<uintptr_t>(p.W2) % 16 != 0))
         return QMV_ERR_ALIGN;
@@ -247,69 +256,9 @@ qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_act
                 Launch &L)
 {
     const int nc_t = (mode == MODE_PLAIN) ? nc_active : round_nc(nc_active);
-    if (type != FMT_Q6_K && p.row_bytes % 16 == 0 && p.K % 256 == 0 && reinterpret_cast<uintptr_t>(p.W) % 16 == 0 &&
+    if (tile_shape_ok(type, p.K, p.row_bytes) && reinterpret_cast<uintptr_t>(p.W) % 16 == 0 &&
         (mode != MODE_GATE || reinterpret_cast<uintptr_t>(p.W2) % 16 == 0)) {
         if (plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L)) return QMV_OK;
-    }
-    const int ub = gemv_unit_bytes(type);
-    bool streamable = type == FMT_Q6_K && (p.row_bytes % 16 == 0) && (p.K % unit_elems(type) == 0) &&
-                      (reinterpret_cast<uintptr_t>(p.W) % 16 == 0) &&
-                      (mode != MODE_GATE || reinterpret_cast<uintptr_t>(p.W2) % 16 == 0);
-    const size_t act = align_up(static_cast<size_t>(nc_t) * p.K * 3 / 2, 128);
-    if (act + 4096 > dev.smem_limit) streamable = false;
-
-    if (streamable) {
-        const Tuning &tu = g_tuning[tidx(type)];
-        int threads = tu.threads.load() ? tu.threads.load() : 128;
-        int slice_units = tu.slice_units.load() ? tu.slice_units.load() : (type == FMT_Q6_K ? 1 : 4);
-        int stages = tu.stages.load() ? tu.stages.load() : (type == FMT_Q6_K ? 2 : 4);
-        const int units_per_row = p.K / unit_elems(type);
-        threads = std::max(32, std::min(MAX_THREADS, threads / 32 * 32));
-        threads = std::min(threads, 32 * units_per_row);  // every warp of the K-split gets >= 1 unit
-        slice_units = std::max(1, std::min(slice_units, units_per_row));
-        stages = std::max(1, std::min(stages, 8));
-        size_t smem = 0;
-        for (;;) {
-            const size_t warps = static_cast<size_t>(threads / 32);
-            const size_t slot = static_cast<size_t>(NR) * slice_units * ub;
-            // activations | rings | 16 B over-read pad | partial sums | alignment slack
-            smem = act + warps * stages * slot + 16 + 2 * warps * NR * nc_t * 4 + 128;
-            if (smem <= dev.smem_limit) break;
-            if (stages > 2) --stages;
-            else if (slice_units > 1) slice_units = (slice_units + 1) / 2;
-            else if (threads > 32) threads /= 2;
-            else { streamable = false; break; }
-        }
-        if (streamable) {
-            L.fn = gemv_stream_fn(type, mode, nc_t);
-            if (!L.fn) return QMV_ERR_NCOLS;
-            if (ensure_smem_attr(dev, L.fn) != QMV_OK) return QMV_ERR_CUDA;
-            const int R = (mode == MODE_GATE) ? NR / 2 : NR;
-            p.units_per_row = units_per_row;
-            p.slice_units = slice_units;
-            p.n_slices = (units_per_row + slice_units - 1) / slice_units;
-            p.stages = stages;
-            p.n_groups = (p.M + R - 1) / R;
-            p.act_bytes = static_cast<uint32_t>(act);
-            p.slice_stride = static_cast<uint32_t>(slice_units * ub);
-            p.slot_bytes = static_cast<uint32_t>(NR) * p.slice_stride;
-            int occ = occupancy(dev.dev, L.fn, threads, smem);
-            if (occ <= 0) return QMV_ERR_CUDA;
-            // A light grid: a few CTAs per SM leave room for the next kernel's
-            // CTAs, which start streaming their weights while this one drains.
-            const int want = tu.ctas_per_sm.load() > 0 ? tu.ctas_per_sm.load() : 2;
-            occ = std::min(occ, want);
-            const int64_t cap = static_cast<int64_t>(occ) * dev.num_sms;
-            int64_t gx = std::min(p.n_groups, cap);
-            if (mode == MODE_MOE)
-                gx = std::min(p.n_groups, std::max<int64_t>(1, (cap + n_potential_experts - 1) / n_potential_experts));
-            L.stream = true;
-            L.p = p;
-            L.block = dim3(threads);
-            L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)), mode == MODE_MOE ? p.n_expert + 1 : 1);
-            L.smem = smem;
-            return QMV_OK;
-        }
     }
     L.fn = gemv_generic_fn(type, mode);
     if (!L.fn) return QMV_ERR_TYPE;
@@ -586,11 +535,12 @@ int qmv_device_fault(unsigned int *code)
     return QMV_OK;
 }
 
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share)
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share,
+                   int flags)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
-    if (threads < 0 || threads > 512 || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
-        ctas_per_sm < 0 || smem_share < 0 || smem_share > 4)
+    if (threads < 0 || threads > TILE_MAX_THREADS || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
+        ctas_per_sm < 0 || smem_share < 0 || smem_share > 4 || flags < 0 || flags > 1)
         return QMV_ERR_SHAPE;
     Tuning &t = g_tuning[tidx(type)];
     t.threads = threads;
@@ -598,6 +548,7 @@ int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_
     t.stages = stages;
     t.ctas_per_sm = ctas_per_sm;
     t.smem_share = smem_share;
+    t.flags = flags;
     return QMV_OK;
 }
 

@@ -1,13 +1,13 @@
 // Generic quantized GEMV: any K that is a multiple of the block size, any
 // 2-byte aligned W, activations read straight from global memory.  Used for
-// shapes the streaming kernel cannot take (rows whose byte size is not a
-// multiple of 16, e.g. Q4_0 with K % 256 != 0 or Q6_K with K % 2048 != 0;
-// activations larger than the shared-memory budget).  One warp per output
+// shapes the tile kernel cannot take (rows whose byte size is not a multiple
+// of 16, e.g. Q4_0 with K % 256 != 0 or Q6_K with K % 2048 != 0; misaligned
+// W; activations larger than the shared-memory budget).  One warp per output
 // row, lanes over blocks, byte-granular loads; the arithmetic is the same
 // block formula as the streaming kernel, integer sums by dp4a.
 #pragma once
 
-#include "gemv_stream.cuh"
+#include "gemv_params.cuh"
 
 namespace qmv {
 

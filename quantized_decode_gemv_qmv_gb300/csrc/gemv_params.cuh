@@ -1,0 +1,42 @@
+// Launch parameters shared by the GEMV kernels (tile kernel, generic kernel).
+#pragma once
+
+#include "common.cuh"
+
+namespace qmv {
+
+enum Mode { MODE_PLAIN = 0, MODE_GATE = 1, MODE_MOE = 2, MODE_DEBUG = 3 };
+
+struct GemvParams {
+    const uint8_t *W;    // weights (MoE: expert 0); GATE: the up matrix
+    const uint8_t *W2;   // GATE: the gate matrix
+    const uint8_t *xq;   // q8_1 activations, column c at xq + c*xq_col_bytes
+    const float *xf;     // fp32 activations quantized in place (tile kernel), column c at xf + c*ldx; or null
+    int64_t ldx;
+    float *y;            // PLAIN/GATE: y[c*ldy + r]; MOE: y[(t*top_k + k)*M + r]
+    int32_t *dbg;        // DEBUG: per-sub-block int sums
+    const int32_t *ids;  // MOE: [n_tokens][top_k]
+    int32_t *status;     // MOE: number of invalid ids (nullable)
+    int64_t M;
+    int64_t ldy;
+    int64_t row_bytes;
+    int64_t xq_col_bytes;
+    int64_t expert_bytes;
+    int64_t n_groups;    // tile kernel: ceil(M / rows per tile)
+    int K;
+    int ncols;           // active columns (PLAIN/GATE/DEBUG)
+    int n_tokens, top_k, n_expert;
+    int units_per_row;   // tile kernel: K / 256
+    int stages;          // tile kernel: tile buffers per warp
+    uint32_t act_bytes;  // tile kernel: shared bytes of the activation area
+    uint32_t raw_off;    // tile kernel: offset of the raw q8_1 copy inside the activation area (0: none)
+    uint32_t flags;      // tile kernel: TILE_FLAG_* launch options
+};
+
+// SwiGLU's gate nonlinearity, silu(g) = g / (1 + e^-g) (CUDA expf).
+__device__ __forceinline__ float silu_f32(float g)
+{
+    return g / (1.0f + expf(-g));
+}
+
+}  // namespace qmv

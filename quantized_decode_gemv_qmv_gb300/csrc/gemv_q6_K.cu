@@ -1,40 +1,12 @@
-// GEMV instantiations for q6_K: streaming kernel for every column count and
-// mode, and the generic fallback.
+// GEMV instantiations for q6_K: the tile kernel for every column count and mode
+// (gemv_tiles.cuh), and the generic fallback.
 #include "gemv_generic.cuh"
+#include "gemv_tiles.cuh"
 #include "kernels.h"
 
 namespace qmv {
 
-const void *gemv_stream_fn_q6_K(int mode, int nc)
-{
-    constexpr int F = FMT_Q6_K;
-    if (mode == MODE_PLAIN) {
-        switch (nc) {
-        case 1: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 1, MODE_PLAIN>);
-        case 2: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 2, MODE_PLAIN>);
-        case 3: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 3, MODE_PLAIN>);
-        case 4: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 4, MODE_PLAIN>);
-        case 5: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 5, MODE_PLAIN>);
-        case 6: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 6, MODE_PLAIN>);
-        case 7: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 7, MODE_PLAIN>);
-        case 8: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 8, MODE_PLAIN>);
-        default: return nullptr;
-        }
-    }
-#define QMV_MODE_CASES(MODE)                                                                     \
-    switch (nc) {                                                                                \
-    case 1: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 1, MODE>);             \
-    case 2: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 2, MODE>);             \
-    case 4: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 4, MODE>);             \
-    case 8: return reinterpret_cast<const void *>(&gemv_stream_kernel<F, 8, MODE>);             \
-    default: return nullptr;                                                                     \
-    }
-    if (mode == MODE_GATE) { QMV_MODE_CASES(MODE_GATE) }
-    if (mode == MODE_MOE) { QMV_MODE_CASES(MODE_MOE) }
-    if (mode == MODE_DEBUG) { QMV_MODE_CASES(MODE_DEBUG) }
-#undef QMV_MODE_CASES
-    return nullptr;
-}
+const void *gemv_tiles_fn_q6_K(int mode, int nc, int rw) { return tiles_kernel_fn<FMT_Q6_K>(mode, nc, rw); }
 
 const void *gemv_generic_fn_q6_K(int mode)
 {

@@ -35,31 +35,41 @@
 namespace qmv {
 
 constexpr int TILE_MAX_THREADS = 384;
-constexpr int TILE_PIECES = 9;  // 16-byte pieces per lane per tile (32 units x 144 B / 512 B)
 constexpr int TILE_MAX_STAGES = 4;
 constexpr int STAGE_BATCH = 4;  // activation loads in flight per thread while staging
+constexpr uint32_t TILE_FLAG_L2_PREFETCH = 1u;  // prefetch each warp's whole weight range into L2 before the wait
 
-// Shared bytes per tile row: UW units plus a pad that puts the rows of one
-// 128-bit read phase on distinct bank quads (row stride / 16 = 8/RW mod 8).
-template <int RW>
-__host__ __device__ constexpr int tile_row_stride()
-{
-    return RW == 1 ? (32 / RW) * UNIT_B : (32 / RW) * UNIT_B + ((8 / RW - (32 / RW) % 8 + 8) % 8) * 16;
-}
+// Tile geometry for format F and RW rows per tile: UW = 32/RW units per tile
+// row (one per lane), the row segment SEG 16-byte pieces long, PER_LANE copy
+// instructions per lane.  Rows are padded in shared memory (stride SS):
+//   Q4_0 / Q4_K (144-byte units): SS/16 = 8/RW mod 8, so the 8 lanes of a
+//     128-bit read phase (RW rows of 8/RW units) hit distinct bank quads;
+//   Q6_K (210-byte units, RW = 4): SS = 1,696 bytes = 32 mod 128, which spreads
+//     the 32 lanes' 32-bit word reads of 2-byte aligned super-blocks over the
+//     banks (at most 2-way, 1.5 on average) and leaves room for the
+//     over-read of the last super-block of a row.
+template <int F, int RW>
+struct TileGeom {
+    static constexpr int UW = 32 / RW;
+    static constexpr int UNIT = unit_bytes<F>();
+    static_assert((UW * UNIT) % 16 == 0, "a tile row segment must be whole 16-byte pieces");
+    static_assert(F != FMT_Q6_K || RW == 4, "Q6_K tiles are 4 rows x 8 super-blocks");
+    static constexpr int SEG = UW * UNIT / 16;
+    static constexpr int PIECES = RW * SEG;
+    static constexpr int PER_LANE = (PIECES + 31) / 32;
+    static constexpr int SS = F == FMT_Q6_K ? UW * UNIT + 16
+                              : (RW == 1 ? UW * UNIT : UW * UNIT + ((8 / RW - UW % 8 + 8) % 8) * 16);
+    static constexpr int TB = RW * SS;
+};
 
-template <int RW>
-__host__ __device__ constexpr int tile_bytes()
+// Host-visible geometry: bytes of one tile buffer (0: no such tile).
+inline int tile_bytes_rt(int type, int rw)
 {
-    return RW * tile_row_stride<RW>();
-}
-
-// Host-visible geometry: bytes of one tile buffer for RW rows per tile.
-inline int tile_bytes_rt(int rw)
-{
+    if (type == FMT_Q6_K) return rw == 4 ? TileGeom<FMT_Q6_K, 4>::TB : 0;
     switch (rw) {
-    case 2: return tile_bytes<2>();
-    case 4: return tile_bytes<4>();
-    case 8: return tile_bytes<8>();
+    case 2: return TileGeom<FMT_Q4_K, 2>::TB;
+    case 4: return TileGeom<FMT_Q4_K, 4>::TB;
+    case 8: return TileGeom<FMT_Q4_K, 8>::TB;
     default: return 0;
     }
 }
@@ -108,8 +118,11 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
                 if (r0 + r >= rounds) break;  // uniform: every lane reaches the group reductions
                 const int t = (r0 + r) * blockDim.x + threadIdx.x;
                 uint32_t w0, w1, ds;
-                int S;
-                q8_1_block_group4(v[r], w0, w1, ds, S);
+                int S, part;
+                q8_1_block_group4(v[r], w0, w1, ds, S, part);
+                // half sums: codes 0..15 (lanes 0, 1 of the group), 16..31 (lanes 2, 3)
+                const int half = part + __shfl_xor_sync(0xffffffffu, part, 1);
+                const int other = __shfl_xor_sync(0xffffffffu, half, 2);
                 if (t < tasks) {
                     const int c = t / (nblk * 4);
                     const int rem = t - c * nblk * 4;
@@ -117,17 +130,8 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
                     const int u = n >> 3, sub = n & 7;
                     uint2 *dq = reinterpret_cast<uint2 *>(act_qs + ((size_t)c * U + u) * ACT_QS_STRIDE + 32 * sub + 8 * j);
                     *dq = make_uint2(w0, w1);
-                    if (j == 0) {
-                        float *sc = reinterpret_cast<float *>(act_sc + ((size_t)c * U + u) * ACT_SC_STRIDE);
-                        const float d8 = half_bits_to_float(ds);
-                        if (F == FMT_Q4_K) {
-                            sc[4 * (sub >> 1) + (sub & 1)] = d8;
-                            sc[4 * (sub >> 1) + 2 + (sub & 1)] = d8 * static_cast<float>(S);
-                        } else {
-                            sc[2 * sub] = d8;
-                            sc[2 * sub + 1] = half_bits_to_float(ds >> 16);
-                        }
-                    }
+                    if (j == 0)
+                        store_act_scalars<F>(act_sc + ((size_t)c * U + u) * act_sc_stride<F>(), sub, ds, S, half, other);
                 }
             }
         }
@@ -171,22 +175,16 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
 #pragma unroll
             for (int i = 0; i < 9; ++i) w[i] = src[i];
         }
-        int S = 0;
+        int S_lo = 0, S_hi = 0;
 #pragma unroll
-        for (int i = 1; i < 9; ++i) S = dp4a_ss(w[i], 0x01010101u, S);
+        for (int i = 1; i < 5; ++i) S_lo = dp4a_ss(w[i], 0x01010101u, S_lo);
+#pragma unroll
+        for (int i = 5; i < 9; ++i) S_hi = dp4a_ss(w[i], 0x01010101u, S_hi);
         const int u = n >> 3, sub = n & 7;
         uint4 *dq = reinterpret_cast<uint4 *>(act_qs + ((size_t)c * U + u) * ACT_QS_STRIDE + 32 * sub);
         dq[0] = make_uint4(w[1], w[2], w[3], w[4]);
         dq[1] = make_uint4(w[5], w[6], w[7], w[8]);
-        float *sc = reinterpret_cast<float *>(act_sc + ((size_t)c * U + u) * ACT_SC_STRIDE);
-        const float d8 = half_bits_to_float(w[0]);
-        if (F == FMT_Q4_K) {
-            sc[4 * (sub >> 1) + (sub & 1)] = d8;
-            sc[4 * (sub >> 1) + 2 + (sub & 1)] = d8 * static_cast<float>(S);
-        } else {
-            sc[2 * sub] = d8;
-            sc[2 * sub + 1] = half_bits_to_float(w[0] >> 16);
-        }
+        store_act_scalars<F>(act_sc + ((size_t)c * U + u) * act_sc_stride<F>(), sub, w[0], S_lo + S_hi, S_lo, S_hi);
     }
 }
 
@@ -200,10 +198,12 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     __shared__ uint32_t s_slots[8];
     __shared__ int s_cnt;
 
-    constexpr int UW = 32 / RW;                     // units per tile row
-    constexpr int SEG = UW * 9;                     // 16-byte pieces per tile row
-    constexpr int SS = tile_row_stride<RW>();       // shared bytes per tile row
-    constexpr int TB = tile_bytes<RW>();            // shared bytes per tile
+    using G = TileGeom<F, RW>;
+    constexpr int UW = G::UW;                        // units per tile row
+    constexpr int SEG = G::SEG;                      // 16-byte pieces per tile row
+    constexpr int SS = G::SS;                        // shared bytes per tile row
+    constexpr int TB = G::TB;                        // shared bytes per tile
+    constexpr int UNIT = G::UNIT;                    // bytes per unit
     constexpr int NM = (MODE == MODE_GATE) ? 2 : 1;  // matrices (GATE: up, gate)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     }
 
     // every warp of the grid owns a contiguous, balanced range of row groups
+    // (whole groups: a row's partial sums never leave the warp)
     const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
     const int64_t wtot = static_cast<int64_t>(gridDim.x) * nwarps;
     const int64_t g_begin = (gwarp * p.n_groups) / wtot;
@@ -268,16 +269,17 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     auto issue_tile = [&]() {
         const uint8_t *W = (NM == 2 && ld_m) ? p.W2 : p.W;
         const int64_t grow = ld_g * RW;  // first row of the group inside the matrix
-        const uint8_t *base = W + (row_base + grow) * rb + static_cast<int64_t>(ld_kt) * (UW * UNIT_B);
+        const uint8_t *base = W + (row_base + grow) * rb + static_cast<int64_t>(ld_kt) * (UW * UNIT);
         const int64_t rows_left = p.M - grow;
-        const int lim = 9 * min(UW, U - ld_kt * UW);  // valid pieces per tile row
+        const int lim = min(UW, U - ld_kt * UW) * UNIT / 16;  // valid pieces per tile row
         const uint32_t dst = ring + static_cast<uint32_t>(ld_buf * TB);
 #pragma unroll
-        for (int j = 0; j < TILE_PIECES; ++j) {
+        for (int j = 0; j < G::PER_LANE; ++j) {
             const int i = 32 * j + lane;
             const int seg = i / SEG;
             const int off = i - seg * SEG;
-            if (off < lim && seg < rows_left) cp_async16(dst + seg * SS + off * 16, base + seg * rb + off * 16);
+            if (i < G::PIECES && off < lim && seg < rows_left)
+                cp_async16(dst + seg * SS + off * 16, base + seg * rb + off * 16);
         }
         cp_async_commit();
         if (++ld_m == NM) {
@@ -289,6 +291,19 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     };
 
     while (issued < total && issued < stages) issue_tile();  // weights first
+    if ((p.flags & TILE_FLAG_L2_PREFETCH) && lane == 0 && total > 0) {
+        // this warp's rows are contiguous bytes: ask L2 for them now, so the
+        // refills after the wait hit in L2
+        const int64_t r0 = g_begin * RW;
+        const int64_t r1 = min64((g_begin + my_groups) * RW, p.M);
+        for (int m = 0; m < NM; ++m) {
+            const uint8_t *b = ((NM == 2 && m) ? p.W2 : p.W) + (row_base + r0) * rb;
+            for (int64_t off = 0, len = (r1 - r0) * rb; off < len; off += 32768) {
+                const uint32_t sz = static_cast<uint32_t>(min64(32768, len - off));
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b + off), "r"(sz) : "memory");
+            }
+        }
+    }
 
     if constexpr (MODE != MODE_MOE) pdl_wait();
     if constexpr (MODE == MODE_MOE)
@@ -315,13 +330,13 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         const int64_t row = cg * RW + r_l;
         const int u = ckt * UW + u_l;
         if (u < U && row < p.M) {
-            uint32_t ub[1] = {ring + static_cast<uint32_t>(cbuf * TB) + r_l * SS + u_l * UNIT_B};
+            uint32_t ub[1] = {ring + static_cast<uint32_t>(cbuf * TB) + r_l * SS + u_l * UNIT};
             const bool live[1] = {true};
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
                 if (MODE != MODE_PLAIN && c >= n_active) break;
                 const uint32_t aq = act_qs + (c * U + u) * ACT_QS_STRIDE;
-                const uint32_t as = act_sc + (c * U + u) * ACT_SC_STRIDE;
+                const uint32_t as = act_sc + (c * U + u) * act_sc_stride<F>();
                 float vv[1] = {0.f};
                 int32_t *dbg[1] = {nullptr};
                 if constexpr (MODE == MODE_DEBUG) {
@@ -383,13 +398,15 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 
 // Kernel table of the tile path for one format (instantiated only in that
 // format's translation unit).  RW = 4 serves every mode and column count;
-// RW = 2 and 8 exist for one plain column, for geometry sweeps.
+// for Q4_0 / Q4_K, RW = 2 and 8 exist for one plain column, for geometry sweeps.
 template <int F>
 const void *tiles_kernel_fn(int mode, int nc, int rw)
 {
 #define QMV_TK(NC_, MODE_, RW_) reinterpret_cast<const void *>(&gemv_tiles_kernel<F, NC_, MODE_, RW_>)
-    if (rw == 2) return (mode == MODE_PLAIN && nc == 1) ? QMV_TK(1, MODE_PLAIN, 2) : nullptr;
-    if (rw == 8) return (mode == MODE_PLAIN && nc == 1) ? QMV_TK(1, MODE_PLAIN, 8) : nullptr;
+    if constexpr (F != FMT_Q6_K) {
+        if (rw == 2) return (mode == MODE_PLAIN && nc == 1) ? QMV_TK(1, MODE_PLAIN, 2) : nullptr;
+        if (rw == 8) return (mode == MODE_PLAIN && nc == 1) ? QMV_TK(1, MODE_PLAIN, 8) : nullptr;
+    }
     if (rw != 4) return nullptr;
     if (mode == MODE_PLAIN) {
         switch (nc) {

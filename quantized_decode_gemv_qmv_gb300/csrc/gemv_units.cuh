@@ -1,10 +1,11 @@
-// Per-unit arithmetic of the 144-byte-unit formats (Q4_K super-blocks; Q4_0
-// in runs of 8 blocks), shared by the tile kernel (gemv_tiles.cuh).
+// Per-unit arithmetic of the tile kernel (gemv_tiles.cuh): a unit is 256
+// weights -- a Q4_K super-block (144 bytes), 8 Q4_0 blocks (144 bytes) or a
+// Q6_K super-block (210 bytes).
 //
 // Method: "llama.cpp 源码完全拆解(十四)：mul_mat_vec_q" (vec_dot_q4_0_q8_1_impl,
-// vec_dot_q4_K_q8_1_impl_vmmq): int8 dot products per block scaled by the
-// block scales, with the page's constant corrections (Q4_0: -8*s; Q4_K:
-// -dmin*m*d8*sum(qy)).
+// vec_dot_q4_K_q8_1_impl_vmmq and the Q6_K snippet): int8 dot products per
+// block scaled by the block scales, with the page's constant corrections
+// (Q4_0: -8*s; Q4_K: -dmin*m*d8*sum(qy); Q6_K: -32*sum(qy) per sub-block).
 //
 // GB300 choices: one lane decodes a whole unit (one header decode per 256
 // weights, the 6-bit scales/mins of all 8 sub-blocks unpacked word-parallel),
@@ -14,13 +15,68 @@
 // 8 lanes of a read phase hit distinct bank quads (units 272 / 80 bytes apart).
 #pragma once
 
-#include "gemv_stream.cuh"
+#include "gemv_params.cuh"
 
 namespace qmv {
 
-constexpr int UNIT_B = 144;         // bytes of a unit (both formats)
+constexpr int UNIT_B = 144;         // bytes of a Q4_0 / Q4_K unit
 constexpr int ACT_QS_STRIDE = 272;  // shared bytes per unit of staged activation codes (256 + pad)
-constexpr int ACT_SC_STRIDE = 80;   // shared bytes per unit of staged activation scalars (64 + pad)
+constexpr int ACT_SC_STRIDE = 80;   // Q4_0 / Q4_K: shared bytes per unit of staged activation scalars (64 + pad)
+
+template <int F>
+__host__ __device__ constexpr int unit_bytes()
+{
+    return F == FMT_Q6_K ? Q6_K_BYTES : UNIT_B;
+}
+
+// Staged scalars per unit: Q4_K {d8[2j], d8[2j+1], D[2j], D[2j+1]} per qs chunk j
+// with D = d8 * sum(qy over the 32-value block); Q4_0 {d8[t], s8[t]} per block;
+// Q6_K d8[0..7] then the 16-value half sums S16[0..15] (int).
+template <int F>
+__host__ __device__ constexpr int act_sc_stride()
+{
+    return F == FMT_Q6_K ? 96 : ACT_SC_STRIDE;
+}
+
+// Writes the scalars of q8_1 block `sub` (0..7) of a unit: ds = (half d | half
+// s << 16) as stored, S = the block's code sum, S_lo / S_hi = the sums of its
+// codes 0..15 / 16..31.
+template <int F>
+__device__ __forceinline__ void store_act_scalars(uint8_t *sc_unit, int sub, uint32_t ds, int S, int S_lo, int S_hi)
+{
+    float *sc = reinterpret_cast<float *>(sc_unit);
+    const float d8 = half_bits_to_float(ds);
+    if constexpr (F == FMT_Q4_K) {
+        sc[4 * (sub >> 1) + (sub & 1)] = d8;
+        sc[4 * (sub >> 1) + 2 + (sub & 1)] = d8 * static_cast<float>(S);
+    } else if constexpr (F == FMT_Q4_0) {
+        sc[2 * sub] = d8;
+        sc[2 * sub + 1] = half_bits_to_float(ds >> 16);
+    } else {
+        sc[sub] = d8;
+        int *s16 = reinterpret_cast<int *>(sc + 8);
+        s16[2 * sub] = S_lo;
+        s16[2 * sub + 1] = S_hi;
+    }
+}
+
+// NW consecutive 32-bit words starting at a 2-byte aligned shared address: the
+// covering aligned words are read once each and funnel-shifted pairwise (Q6_K
+// super-blocks are 210 bytes, so they start on 2-byte boundaries).  Reads the
+// aligned words [a & ~3, (a & ~3) + 4*(NW+1)).
+template <int NW>
+__device__ __forceinline__ void lds_run_u2(uint32_t a, uint32_t (&out)[NW])
+{
+    const uint32_t base = a & ~3u;
+    const uint32_t sh = (a & 2u) << 3;  // 0 or 16 bits
+    uint32_t prev = lds32(base);
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+        const uint32_t nxt = lds32(base + 4u * (k + 1));
+        out[k] = __funnelshift_r(prev, nxt, sh);
+        prev = nxt;
+    }
+}
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
 {
@@ -34,12 +90,9 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }
 
-// Activation staging (4-byte loads; any 4-byte aligned xq).  Per column and unit u (256 values):
-// the 256 codes in natural order at c*U*272 + u*272, and 16 scalars at
-// sc + (c*U + u)*80:
-//   Q4_K: per sub-block pair j (= 32-byte qs chunk j): {d8[2j], d8[2j+1], D[2j], D[2j+1]}
-//         with D = d8 * sum(qy over the 32-value sub-block);
-//   Q4_0: per block t: {d8[t], s8[t]}.
+// Activation staging (4-byte loads; any 4-byte aligned xq): per column and unit
+// u the 256 codes in natural order at c*U*272 + u*272, then the unit's scalars
+// (store_act_scalars) at sc + (c*U + u)*act_sc_stride, sc = NC*U*272.
 template <int F, int NC, typename ColFn>
 __device__ __forceinline__ void stage_units_activations(const GemvParams &p, uint8_t *smem, int n_active,
                                                         ColFn src_col)
@@ -58,22 +111,16 @@ __device__ __forceinline__ void stage_units_activations(const GemvParams &p, uin
 #pragma unroll
             for (int i = 0; i < 9; ++i) w[i] = src[i];
         }
-        int S = 0;
+        int S_lo = 0, S_hi = 0;
 #pragma unroll
-        for (int i = 1; i < 9; ++i) S = dp4a_ss(w[i], 0x01010101u, S);
+        for (int i = 1; i < 5; ++i) S_lo = dp4a_ss(w[i], 0x01010101u, S_lo);
+#pragma unroll
+        for (int i = 5; i < 9; ++i) S_hi = dp4a_ss(w[i], 0x01010101u, S_hi);
         const int u = n >> 3, sub = n & 7;
         uint4 *dq = reinterpret_cast<uint4 *>(act_qs + ((size_t)c * U + u) * ACT_QS_STRIDE + 32 * sub);
         dq[0] = make_uint4(w[1], w[2], w[3], w[4]);
         dq[1] = make_uint4(w[5], w[6], w[7], w[8]);
-        float *sc = reinterpret_cast<float *>(act_sc + ((size_t)c * U + u) * ACT_SC_STRIDE);
-        const float d8 = half_bits_to_float(w[0]);
-        if (F == FMT_Q4_K) {
-            sc[4 * (sub >> 1) + (sub & 1)] = d8;
-            sc[4 * (sub >> 1) + 2 + (sub & 1)] = d8 * static_cast<float>(S);
-        } else {
-            sc[2 * sub] = d8;
-            sc[2 * sub + 1] = half_bits_to_float(w[0] >> 16);
-        }
+        store_act_scalars<F>(act_sc + ((size_t)c * U + u) * act_sc_stride<F>(), sub, w[0], S_lo + S_hi, S_lo, S_hi);
     }
 }
 
@@ -148,6 +195,65 @@ __device__ __forceinline__ void unit_dot(const uint32_t (&ub)[NRL], const bool (
                     dbg[r][4 * j + 3] = s1;
                 }
             }
+        }
+    } else if (F == FMT_Q6_K) {
+        // One super-block (210 bytes, 2-byte aligned): ql[128] at 0, qh[64] at
+        // 128, int8 scales[16] at 192, half d at 208.  Element e = 128h + 32g + l
+        // (h < 2, g < 4, l < 32) has low 4 bits in ql[64h + 32(g&1) + l]
+        // (nibble g>>1) and high 2 bits in qh[32h + l] (bits 2g, 2g+1); its
+        // 16-value sub-block is e/16.  Per (h, word w of l), the words of ql_a =
+        // ql[64h..], ql_b = ql[64h+32..] and qh hold 4 elements of each g.
+#pragma unroll
+        for (int r = 0; r < NRL; ++r) {
+            if (!live[r]) continue;
+            uint32_t dw[1], scw[4];
+            lds_run_u2<1>(ub[r] + 208, dw);
+            lds_run_u2<4>(ub[r] + 192, scw);
+            const float d = half_bits_to_float(dw[0]);
+            float acc = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t qa[8], qb[8], qh[8];
+                lds_run_u2<8>(ub[r] + 64 * h, qa);
+                lds_run_u2<8>(ub[r] + 64 * h + 32, qb);
+                lds_run_u2<8>(ub[r] + 128 + 32 * h, qh);
+                const uint4 d8v = lds128(as + 16 * h);          // d8 of q8_1 blocks 4h..4h+3
+                const uint4 s16a = lds128(as + 32 + 32 * h);    // S16 of sub-blocks 8h..8h+3
+                const uint4 s16b = lds128(as + 48 + 32 * h);    // S16 of sub-blocks 8h+4..8h+7
+                const float d8s[4] = {__uint_as_float(d8v.x), __uint_as_float(d8v.y), __uint_as_float(d8v.z),
+                                      __uint_as_float(d8v.w)};
+                const int s16[8] = {static_cast<int>(s16a.x), static_cast<int>(s16a.y), static_cast<int>(s16a.z),
+                                    static_cast<int>(s16a.w), static_cast<int>(s16b.x), static_cast<int>(s16b.y),
+                                    static_cast<int>(s16b.z), static_cast<int>(s16b.w)};
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 a0 = lds128(aq + 128 * h + 32 * g);
+                    const uint4 a1 = lds128(aq + 128 * h + 32 * g + 16);
+                    const uint32_t act[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    int dlo = 0, dhi = 0;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const uint32_t ql = (g & 1) ? qb[w] : qa[w];
+                        const uint32_t lo4 = (g & 2) ? ((ql >> 4) & 0x0F0F0F0Fu) : (ql & 0x0F0F0F0Fu);
+                        const uint32_t hi2 = g == 0 ? (qh[w] << 4) : g == 1 ? (qh[w] << 2) : g == 2 ? qh[w] : (qh[w] >> 2);
+                        const uint32_t q = lo4 | (hi2 & 0x30303030u);  // 6-bit codes 0..63
+                        if (w < 4) dlo = dp4a_us(q, act[w], dlo);
+                        else dhi = dp4a_us(q, act[w], dhi);
+                    }
+                    const int sb0 = 8 * h + 2 * g;
+                    const int t0 = dlo - 32 * s16[2 * g];      // sum (v - 32) * qy, sub-block sb0
+                    const int t1 = dhi - 32 * s16[2 * g + 1];  // sub-block sb0 + 1
+                    const float sc0 = static_cast<float>(static_cast<int8_t>((scw[sb0 >> 2] >> (8 * (sb0 & 3))) & 0xffu));
+                    const float sc1 =
+                        static_cast<float>(static_cast<int8_t>((scw[(sb0 + 1) >> 2] >> (8 * ((sb0 + 1) & 3))) & 0xffu));
+                    acc += d8s[g] * (sc0 * static_cast<float>(t0) + sc1 * static_cast<float>(t1));
+                    if constexpr (DEBUG) {
+                        dbg[r][sb0] = t0;
+                        dbg[r][sb0 + 1] = t1;
+                    }
+                }
+            }
+            v[r] += d * acc;
         }
     } else {
         // 8 Q4_0 blocks: block t occupies bytes [18t, 18t+18) of the unit, i.e.

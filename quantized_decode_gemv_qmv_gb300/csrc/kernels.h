@@ -15,13 +15,10 @@ cudaError_t launch_quantize_weights(int type, const float *w, int64_t M, int64_t
                                     int64_t row_bytes, cudaStream_t st);
 
 // Kernel function pointers of the GEMV instantiations (gemv_<type>.cu).
-// stream: template columns nc_t (PLAIN: 1..8; other modes: 1, 2, 4, 8).
-// Returns nullptr for a combination that is not instantiated.
-const void *gemv_stream_fn(int type, int mode, int nc_t);
+// Tile kernel: template columns nc_t (PLAIN: 1..8; other modes: 1, 2, 4, 8)
+// and rows per tile rw.  Returns nullptr for a combination that is not
+// instantiated.
+const void *gemv_tiles_fn(int type, int mode, int nc_t, int rw);
 const void *gemv_generic_fn(int type, int mode);
-
-// Unit geometry of the streaming kernel for a type.
-int gemv_unit_bytes(int type);
-int gemv_items_per_unit(int type);
 
 }  // namespace qmv

@@ -41,10 +41,11 @@ __device__ __forceinline__ float h2f(uint32_t bits)
 // lane j holding values 8j..8j+7 of the block in v.  Every lane of the warp must
 // call it (the reductions shuffle across the group with the full mask).
 // Returns in w0 / w1 the lane's two code words (codes 8j..8j+3, 8j+4..8j+7,
-// byte i = code i), in ds the block's (half d | half s << 16) word, and in
-// sum the exact integer code sum of the block.
+// byte i = code i), in ds the block's (half d | half s << 16) word, in sum the
+// exact integer code sum of the block and in part the sum of the lane's own 8
+// codes.
 __device__ __forceinline__ void q8_1_block_group4(const float (&v)[8], uint32_t &w0, uint32_t &w1, uint32_t &ds,
-                                                  int &sum)
+                                                  int &sum, int &part)
 {
     float amax = fabsf(v[0]);
 #pragma unroll
@@ -60,6 +61,7 @@ __device__ __forceinline__ void q8_1_block_group4(const float (&v)[8], uint32_t 
         s += q;
         b[i] = static_cast<uint32_t>(q) & 0xffu;
     }
+    part = s;
     s += __shfl_xor_sync(0xffffffffu, s, 1);
     s += __shfl_xor_sync(0xffffffffu, s, 2);
     w0 = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);

@@ -31,8 +31,8 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restr
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (ok) q8_1_load8(x + c * ldx, k, K, vec, v);
     uint32_t w0, w1, ds;
-    int sum;
-    q8_1_block_group4(v, w0, w1, ds, sum);
+    int sum, part;
+    q8_1_block_group4(v, w0, w1, ds, sum, part);
     if (ok) {
         uint32_t *o = reinterpret_cast<uint32_t *>(xq + b * Q8_1_BYTES);
         o[1 + 2 * j] = w0;

@@ -86,8 +86,8 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_quantize_weights(12, p, 4, 100, 100, p, nul) == 3
     assert L.qmv_quantize_weights(9, p, 4, 256, 256, p, nul) == 2
     assert L.qmv_debug_subblock_sums(14, p, 4, 256, p, 0, p, nul) == 4
-    # fused fp32-input calls: Q4_0/Q4_K with K % 256 == 0 and 16-byte aligned W only
-    assert L.qmv_mul_mat_vec_f32(14, p, 16, 4096, p, 4096, 1, p, nul) == 2
+    # fused fp32-input calls: the tile kernel's shapes (Q4_0/Q4_K: K % 256, Q6_K: K % 2048), 16-byte aligned W
+    assert L.qmv_mul_mat_vec_f32(14, p, 16, 2304, p, 2304, 1, p, nul) == 3
     assert L.qmv_mul_mat_vec_f32(2, p, 16, 96, p, 96, 1, p, nul) == 3
     assert L.qmv_mul_mat_vec_f32(12, p, 16, 4096, p, 4000, 1, p, nul) == 3
     assert L.qmv_mul_mat_vec_f32(12, ctypes.c_void_p(0x1008), 16, 4096, p, 4096, 1, p, nul) == 5
@@ -96,10 +96,12 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_mul_mat_vec_gate_up_swiglu_f32(12, nul, p, 16, 4096, p, 4096, 1, p, nul) == 1
     assert L.qmv_mul_mat_vec_gate_up_swiglu_f32(12, ctypes.c_void_p(0x1008), p, 16, 4096, p, 4096, 1, p, nul) == 5
     assert L.qmv_mul_mat_vec_id_f32(12, p, 8, 16, 4096, p, 4096, nul, 4, 2, p, nul, nul) == 1
-    assert L.qmv_mul_mat_vec_id_f32(14, p, 8, 16, 4096, p, 4096, p, 4, 2, p, nul, nul) == 2
+    assert L.qmv_mul_mat_vec_id_f32(14, p, 8, 16, 2304, p, 2304, p, 4, 2, p, nul, nul) == 3
     # tuning knobs validate too
-    assert L.qmv_set_tuning(12, 100, 0, 0, 0, 0) == 3
-    assert L.qmv_set_tuning(12, 544, 0, 0, 0, 0) == 3
-    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 5) == 3
-    assert L.qmv_set_tuning(3, 0, 0, 0, 0, 0) == 2
-    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0) == 0
+    assert L.qmv_set_tuning(12, 100, 0, 0, 0, 0, 0) == 3
+    assert L.qmv_set_tuning(12, 544, 0, 0, 0, 0, 0) == 3
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 5, 0) == 3
+    assert L.qmv_set_tuning(3, 0, 0, 0, 0, 0, 0) == 2
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0, 2) == 3
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0, 1) == 0
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0, 0) == 0

@@ -15,7 +15,7 @@ import synthetic
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-4
-FUSED_TYPES = (oracle.Q4_0, oracle.Q4_K)
+FUSED_TYPES = (oracle.Q4_0, oracle.Q4_K, oracle.Q6_K)
 
 
 @pytest.fixture(scope="module")
@@ -58,8 +58,9 @@ def weights(t, M, K, seed):
     return oracle.quantize_rows(t, synthetic.weights_f32(seed, M, K))
 
 
-@pytest.mark.parametrize("t", FUSED_TYPES)
-@pytest.mark.parametrize("M,K", [(203, 4096), (61, 256), (130, 2304), (37, 11264)])
+@pytest.mark.parametrize("t,M,K", [(oracle.Q4_0, 203, 4096), (oracle.Q4_0, 61, 256), (oracle.Q4_K, 203, 4096),
+                                   (oracle.Q4_K, 130, 2304), (oracle.Q4_K, 37, 11264), (oracle.Q6_K, 203, 4096),
+                                   (oracle.Q6_K, 45, 2048), (oracle.Q6_K, 21, 14336)])
 @pytest.mark.parametrize("ncols", [1, 2, 3, 5, 8])
 def test_fused_plain_equals_two_step(q, t, M, K, ncols):
     W = weights(t, M, K, 1100 + M + ncols)
@@ -76,7 +77,7 @@ def test_fused_plain_equals_two_step(q, t, M, K, ncols):
 def test_fused_strided_and_misaligned_x(q, t):
     import torch
 
-    M, K, nc = 97, 1024, 3
+    M, K, nc = 97, 2048, 3
     W = weights(t, M, K, 1300 + t)
     x = synthetic.activations_f32(1301, nc, K)
     Wd = dev(W)
@@ -107,7 +108,7 @@ def test_fused_gate_up_equals_two_step(q, t, ncols):
 def test_fused_moe_equals_two_step(q, t):
     import torch
 
-    E, M, K = 8, 77, 1024
+    E, M, K = 8, 77, 2048
     W = weights(t, E * M, K, 1500 + t).reshape(E, -1)
     for ids in (synthetic.moe_ids(1501, 4, 2, E), np.array([[1, 9], [-1, 2], [2, 1]], dtype=np.int32)):
         T = ids.shape[0]
@@ -124,11 +125,11 @@ def test_fused_moe_equals_two_step(q, t):
 def test_fused_rejects_what_it_does_not_cover(q):
     import torch
 
-    x = torch.zeros((1, 4096), dtype=torch.float32, device="cuda")
-    W6 = torch.zeros((4, q.row_bytes(q.Q6_K, 4096)), dtype=torch.uint8, device="cuda")
+    x = torch.zeros((1, 2304), dtype=torch.float32, device="cuda")
+    W6 = torch.zeros((4, q.row_bytes(q.Q6_K, 2304)), dtype=torch.uint8, device="cuda")
     with pytest.raises(q.QmvError) as e:
-        q.mul_mat_vec_f32(q.Q6_K, W6, 4, 4096, x)
-    assert e.value.status == 2
+        q.mul_mat_vec_f32(q.Q6_K, W6, 4, 2304, x)
+    assert e.value.status == 3
     x96 = torch.zeros((1, 96), dtype=torch.float32, device="cuda")
     W0 = torch.zeros((4, q.row_bytes(q.Q4_0, 96)), dtype=torch.uint8, device="cuda")
     with pytest.raises(q.QmvError) as e:

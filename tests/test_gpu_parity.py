@@ -188,7 +188,8 @@ def test_tuning_variants_agree(q, t, nc):
     Wd, xd = dev(W), dev(xq)
     try:
         for tune in [(32, 1, 1, 1, 1), (64, 2, 3, 0, 2), (256, 8, 2, 0, 1), (128, 3, 6, 2, 0), (96, 16, 4, 0, 2),
-                     (128, 4, 2, 3, 1), (384, 16, 1, 1, 4), (384, 4, 4, 2, 1)]:
+                     (128, 4, 2, 3, 1), (384, 16, 1, 1, 4), (384, 4, 4, 2, 1), (0, 0, 0, 0, 0, 1),
+                     (256, 16, 3, 0, 0, 1)]:
             q.set_tuning(t, *tune)
             y = host(q.mul_mat_vec(t, Wd, M, K, xd, nc))
             assert_close_l1(y, y_ref, l1, f"type {t} ncols {nc} tuning {tune}")
