@@ -198,16 +198,12 @@ int qmv_device_fault(unsigned int *code);
  *     tiles of 8, 4 or 2 rows; 8 and 2 only for one plain column);
  *     stages = tile buffers per warp (1..4); ctas_per_sm = CTAs per SM;
  *     smem_share = a CTA takes at most 1/smem_share of an SM's shared
- *     memory (1..4, default 2, which leaves room for the next kernel);
- *     flags bit 0 = each warp asks L2 for its whole weight range before the
- *     dependency wait (cp.async.bulk.prefetch.L2), so later tiles hit in L2.
- *   Q6_K (stream kernel): threads per CTA (<= 256); slice_units = 2048-value
- *     units per slice; stages = ring slots per warp; ctas_per_sm; smem_share
- *     and flags unused.
+ *     memory (1..4, default 2, which leaves room for the next kernel).
+ *   Q6_K: the same tile kernel with tiles of 4 rows x 8 super-blocks
+ *     (slice_units is ignored).
  * Returns QMV_ERR_TYPE for a non-weight type, QMV_ERR_SHAPE for values out of
  * range. */
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share,
-                   int flags);
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share);
 
 /* Enables (1, default) or disables (0) programmatic dependent launch for the
  * library's q8_1 and GEMV kernels.  When enabled, a GEMV may start streaming

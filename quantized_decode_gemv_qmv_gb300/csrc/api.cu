@@ -58,7 +58,7 @@ constexpr size_t SMEM_RESERVE = 1024;  // static shared memory and alignment sla
 std::atomic<int> g_pdl{1};
 
 struct Tuning {
-    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0}, flags{0};
+    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0};
 };
 Tuning g_tuning[3];
 
@@ -219,7 +219,6 @@ bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t,
     p.stages = stages;
     p.act_bytes = static_cast<uint32_t>(act);
     p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
-    p.flags = static_cast<uint32_t>(tu.flags.load());
     L.fn = fn;
     L.stream = true;
     L.p = p;
@@ -535,12 +534,11 @@ int qmv_device_fault(unsigned int *code)
     return QMV_OK;
 }
 
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share,
-                   int flags)
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (threads < 0 || threads > TILE_MAX_THREADS || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
-        ctas_per_sm < 0 || smem_share < 0 || smem_share > 4 || flags < 0 || flags > 1)
+        ctas_per_sm < 0 || smem_share < 0 || smem_share > 4)
         return QMV_ERR_SHAPE;
     Tuning &t = g_tuning[tidx(type)];
     t.threads = threads;
@@ -548,7 +546,6 @@ int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_
     t.stages = stages;
     t.ctas_per_sm = ctas_per_sm;
     t.smem_share = smem_share;
-    t.flags = flags;
     return QMV_OK;
 }
 

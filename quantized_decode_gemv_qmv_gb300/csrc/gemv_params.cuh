@@ -30,7 +30,6 @@ struct GemvParams {
     int stages;          // tile kernel: tile buffers per warp
     uint32_t act_bytes;  // tile kernel: shared bytes of the activation area
     uint32_t raw_off;    // tile kernel: offset of the raw q8_1 copy inside the activation area (0: none)
-    uint32_t flags;      // tile kernel: TILE_FLAG_* launch options
 };
 
 // SwiGLU's gate nonlinearity, silu(g) = g / (1 + e^-g) (CUDA expf).

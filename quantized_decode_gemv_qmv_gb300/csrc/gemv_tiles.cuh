@@ -37,7 +37,6 @@ namespace qmv {
 constexpr int TILE_MAX_THREADS = 384;
 constexpr int TILE_MAX_STAGES = 4;
 constexpr int STAGE_BATCH = 4;  // activation loads in flight per thread while staging
-constexpr uint32_t TILE_FLAG_L2_PREFETCH = 1u;  // prefetch each warp's whole weight range into L2 before the wait
 
 // Tile geometry for format F and RW rows per tile: UW = 32/RW units per tile
 // row (one per lane), the row segment SEG 16-byte pieces long, PER_LANE copy
@@ -291,20 +290,6 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     };
 
     while (issued < total && issued < stages) issue_tile();  // weights first
-    if ((p.flags & TILE_FLAG_L2_PREFETCH) && lane == 0 && total > 0) {
-        // this warp's rows are contiguous bytes: ask L2 for them now, so the
-        // refills after the wait hit in L2
-        const int64_t r0 = g_begin * RW;
-        const int64_t r1 = min64((g_begin + my_groups) * RW, p.M);
-        for (int m = 0; m < NM; ++m) {
-            const uint8_t *b = ((NM == 2 && m) ? p.W2 : p.W) + (row_base + r0) * rb;
-            for (int64_t off = 0, len = (r1 - r0) * rb; off < len; off += 32768) {
-                const uint32_t sz = static_cast<uint32_t>(min64(32768, len - off));
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b + off), "r"(sz) : "memory");
-            }
-        }
-    }
-
     if constexpr (MODE != MODE_MOE) pdl_wait();
     if constexpr (MODE == MODE_MOE)
         stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; });

@@ -55,9 +55,29 @@ __device__ __forceinline__ void q8_1_block_group4(const float (&v)[8], uint32_t 
     const float d = __fdiv_rn(amax, 127.0f);
     int s = 0;
     uint32_t b[8];
+    // x/d is needed correctly rounded (the integer code is rounded from the fp32
+    // quotient).  Markstein's final-correction step (Markstein, "Computation of
+    // elementary functions on the IBM RISC System/6000 processor", 1990):
+    // with r = RN(1/d), q0 = RN(x*r) is within an ulp of x/d, the residual
+    // x - d*q0 is exact in one FMA, and RN(q0 + r*(x - d*q0)) = RN(x/d), as long
+    // as nothing overflows or underflows -- guaranteed for d in [2^-40, 2^40]
+    // and |x/d| >= 2^-30 (the residual then stays a normal number; smaller
+    // quotients round to code 0 either way).  Other blocks use the IEEE
+    // division itself.
+    const bool fast = d >= 0x1p-40f && d <= 0x1p40f;  // the same for all 4 lanes of the block
+    const float r = fast ? __frcp_rn(d) : 0.0f;
+    const float tiny = d * 0x1p-30f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int q = (d == 0.0f) ? 0 : clamp_round(__fdiv_rn(v[i], d), -127.0f, 127.0f);
+        float z;
+        if (fast) {
+            const float q0 = __fmul_rn(v[i], r);
+            const float e = __fmaf_rn(-d, q0, v[i]);
+            z = fabsf(v[i]) < tiny ? 0.0f : __fmaf_rn(e, r, q0);
+        } else {
+            z = (d == 0.0f) ? 0.0f : __fdiv_rn(v[i], d);
+        }
+        const int q = clamp_round(z, -127.0f, 127.0f);
         s += q;
         b[i] = static_cast<uint32_t>(q) & 0xffu;
     }
