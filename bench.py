@@ -264,6 +264,92 @@ def run_reference(args):
 
 
 # ---- GPU arm ------------------------------------------------------------------------
+def measure_configs(q, torch, stream, device, reps):
+    """Per-call time of the GEMV at each workload the benchmark is quoted on,
+    each launch chained over distinct weight copies (so consecutive calls do not
+    share L2) and timed with CUDA events as a graph of launches."""
+    import numpy as np
+
+    import synthetic
+
+    def chain_time(calls):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls:
+                c()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+            stream.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            stream.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (reps * len(calls))
+
+    def weights(t, M, K, n, seed):
+        with torch.cuda.stream(stream):
+            ws = [q.quantize_weights(t, synthetic.device_normal_f32(seed + i, (M, K), 0.02, device), stream=stream)
+                  for i in range(n)]
+        stream.synchronize()
+        return ws
+
+    def xq_of(K, nc, seed, outl=0.0):
+        x = torch.from_numpy(synthetic.activations_f32(seed, nc, K, outlier_frac=outl)).to(device)
+        return q.quantize_q8_1(x, stream=stream)
+
+    out = {}
+    y = torch.empty((8, 32000), dtype=torch.float32, device=device)
+
+    def plain(name, t, M, K, n, seed, ncols=1, outl=0.0):
+        ws = weights(t, M, K, n, seed)
+        xq = xq_of(K, ncols, seed + 99, outl)
+        us = chain_time([lambda W=W: q.mul_mat_vec(t, W, M, K, xq, ncols, out=y[:ncols, :M], stream=stream)
+                         for W in ws])
+        wb = ws[0].numel()
+        out[name] = {"us_per_call": round(us, 3), "weight_gbs": round(wb / us / 1e3, 1)}
+        del ws
+        torch.cuda.empty_cache()
+
+    plain("q4_0 4096x4096", q.Q4_0, 4096, 4096, 8, 3_000_000)
+    plain("q6_K 32000x4096", q.Q6_K, 32000, 4096, 4, 3_000_100)
+    plain("q6_K 4096x14336", q.Q6_K, 4096, 14336, 8, 3_000_200)
+    ws = weights(q.Q4_K, 14336, 4096, 8, 3_000_300)
+    sweep = {}
+    for nc in range(1, 9):
+        xq = xq_of(4096, nc, 3_000_400 + nc)
+        us = chain_time([lambda W=W: q.mul_mat_vec(q.Q4_K, W, 14336, 4096, xq, nc, out=y[:nc, :14336], stream=stream)
+                         for W in ws])
+        sweep[str(nc)] = {"us_per_call": round(us, 3), "weight_gbs": round(ws[0].numel() / us / 1e3, 1)}
+    out["q4_K 14336x4096 ncols 1..8"] = sweep
+    # fused gate/up, two 14336x4096 matrices per call
+    xq = xq_of(4096, 1, 3_000_500)
+    pairs = [(ws[2 * i], ws[2 * i + 1]) for i in range(4)]
+    us = chain_time([lambda g=g, u=u: q.mul_mat_vec_gate_up_swiglu(q.Q4_K, g, u, 14336, 4096, xq, 1,
+                                                                    out=y[:1, :14336], stream=stream) for g, u in pairs])
+    out["q4_K gate+up 2x14336x4096 swiglu"] = {"us_per_call": round(us, 3),
+                                               "weight_gbs": round(2 * ws[0].numel() / us / 1e3, 1)}
+    # MoE: 8 experts of 14336x4096, 4 tokens, top-2 drawn without replacement
+    E = torch.stack(ws).view(8, -1)
+    ids = synthetic.moe_ids(3_000_600, 4, 2, 8)
+    n_touched = len(set(ids.reshape(-1).tolist()))
+    idd = torch.from_numpy(ids).to(device)
+    xq4 = xq_of(4096, 4, 3_000_700)
+    ym = torch.empty((4, 2, 14336), dtype=torch.float32, device=device)
+    us = chain_time([lambda: q.mul_mat_vec_id(q.Q4_K, E, 8, 14336, 4096, xq4, idd, out=ym, stream=stream)] * 4)
+    out["q4_K moe 8x14336x4096 4 tokens top-2"] = {
+        "us_per_call": round(us, 3), "experts_touched": n_touched,
+        "weight_gbs": round(n_touched * ws[0].numel() / us / 1e3, 1),
+        "note": "the same call repeated; the touched experts (%d x 33 MB) exceed L2" % n_touched}
+    del ws, E
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -423,6 +509,8 @@ def run_gpu(args):
     achieved = tot_bytes / tot_time / 1e3  # GB/s
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["csrc_sha"] == csrc_sha() else None
 
+    configs = measure_configs(q, torch, stream, device, reps) if not args.no_configs else None
+
     # ---- end to end: host buffers, copies inside the timed region ---------------------
     h2d = x_flat_host.numel() * 4
     d2h = y_flat_host.numel() * 4
@@ -473,6 +561,7 @@ def run_gpu(args):
                      "peak_kind": f"{peak_kind} HBM copy bandwidth"},
         "step_kernels": kinds,
         "per_shape": per_shape,
+        "configs": configs,
         "hbm_frac_of_measured": round(value / peak, 4),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
@@ -533,6 +622,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=6.0, help="CPU-baseline timing budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config timing section")
     ap.add_argument("--kernel-only", default=None, help="profiling aid: only GEMV launches of one shape or step kind")
     ap.add_argument("--launches", type=int, default=8)
     args = ap.parse_args()

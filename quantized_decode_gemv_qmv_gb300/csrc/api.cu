@@ -53,7 +53,7 @@ __device__ unsigned int g_fault_word;
 namespace {
 
 constexpr int MAX_DEVICES = 64;
-constexpr size_t SMEM_RESERVE = 1024;  // static shared memory and alignment slack per CTA
+constexpr size_t SMEM_RESERVE = 2048;  // static shared memory (MoE token lists) and alignment slack per CTA
 
 std::atomic<int> g_pdl{1};
 
@@ -70,6 +70,8 @@ std::map<std::pair<int, const void *>, bool> g_smem_attr;
 int g_num_sms[MAX_DEVICES];
 int g_smem_optin[MAX_DEVICES];
 int g_smem_sm[MAX_DEVICES];
+int g_smem_resv[MAX_DEVICES];
+std::map<const void *, size_t> g_static_smem;  // kernel -> static shared bytes
 unsigned int *g_fault_ptr[MAX_DEVICES];
 
 qmv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ERR_CUDA; }
@@ -79,6 +81,7 @@ struct DevInfo {
     int num_sms;
     size_t smem_limit;  // dynamic shared memory a CTA may use
     size_t smem_per_sm; // shared memory of one SM
+    size_t smem_resv;   // shared memory the hardware reserves per CTA
     unsigned int *fault;
 };
 
@@ -97,6 +100,9 @@ qmv_status device_info(DevInfo &d)
         if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d.dev) != cudaSuccess)
             return QMV_ERR_CUDA;
         g_smem_sm[d.dev] = per_sm;
+        int resv = 0;
+        if (cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, d.dev) != cudaSuccess) resv = 1024;
+        g_smem_resv[d.dev] = resv;
         void *f = nullptr;
         if (cudaGetSymbolAddress(&f, g_fault_word) != cudaSuccess) return QMV_ERR_CUDA;
         g_fault_ptr[d.dev] = static_cast<unsigned int *>(f);
@@ -105,6 +111,7 @@ qmv_status device_info(DevInfo &d)
     d.num_sms = g_num_sms[d.dev];
     d.smem_limit = static_cast<size_t>(g_smem_optin[d.dev]) - SMEM_RESERVE;
     d.smem_per_sm = static_cast<size_t>(g_smem_sm[d.dev]);
+    d.smem_resv = static_cast<size_t>(g_smem_resv[d.dev]);
     d.fault = g_fault_ptr[d.dev];
     return QMV_OK;
 }
@@ -119,6 +126,17 @@ qmv_status ensure_smem_attr(const DevInfo &d, const void *fn)
         return QMV_ERR_CUDA;
     g_smem_attr[key] = true;
     return QMV_OK;
+}
+
+size_t static_smem(const void *fn)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_static_smem.find(fn);
+    if (it != g_static_smem.end()) return it->second;
+    cudaFuncAttributes a{};
+    const size_t v = cudaFuncGetAttributes(&a, fn) == cudaSuccess ? a.sharedSizeBytes : 2048;
+    g_static_smem[fn] = v;
+    return v;
 }
 
 int occupancy(int dev, const void *fn, int threads, size_t smem)
@@ -163,10 +181,13 @@ bool tile_shape_ok(int type, int64_t K, int64_t row_bytes)
 // Geometry of the tile kernel: warp tiles of RW rows x 32/RW units, a ring of
 // `stages` tile buffers per warp; the grid covers every SM (one CTA per SM
 // unless tuned) with up to 12 warps per CTA, every warp owning a balanced
-// contiguous range of RW-row groups.  Returns false if the
-// activations do not fit in shared memory.
-bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t, int n_potential_experts,
-                Launch &L)
+// contiguous range of RW-row groups.  NoFit: the activations do not fit in
+// shared memory (the caller may fall back to the generic kernel); Error: a
+// CUDA call failed or the kernel is missing (never a silent fallback).
+enum class TilePlan { Ok, NoFit, Error };
+
+TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t, int n_potential_experts,
+                    Launch &L)
 {
     const Tuning &tu = g_tuning[tidx(type)];
     const int U = static_cast<int>(p.K / 256);
@@ -177,7 +198,7 @@ bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t,
         rw = 4;
         fn = gemv_tiles_fn(type, mode, nc_t, rw);
     }
-    if (!fn) return false;
+    if (!fn) return TilePlan::Error;
     const int sc_stride = type == FMT_Q6_K ? act_sc_stride<FMT_Q6_K>() : act_sc_stride<FMT_Q4_K>();
     const size_t packed = align_up(static_cast<size_t>(nc_t) * U * (ACT_QS_STRIDE + sc_stride), 128);
     const size_t raw = align_up(static_cast<size_t>(nc_t) * U * 8 * Q8_1_BYTES, 128);
@@ -190,30 +211,62 @@ bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t,
     // grid: every SM first (MoE: the SMs shared among the experts that may be
     // picked), then more warps per CTA; warps own whole row groups
     const int cps = tu.ctas_per_sm.load() > 0 ? tu.ctas_per_sm.load() : 1;
-    int64_t max_ctas = static_cast<int64_t>(cps) * dev.num_sms;
-    if (mode == MODE_MOE) max_ctas = std::max<int64_t>(1, (max_ctas + n_potential_experts - 1) / n_potential_experts);
+    const int64_t max_ctas = static_cast<int64_t>(cps) * dev.num_sms;
     const int64_t G = (p.M + rw - 1) / rw;
-    const int64_t gx = std::min(max_ctas, G);
-    max_wpc = static_cast<int>(std::min<int64_t>(max_wpc, (G + gx - 1) / gx));
+    int64_t gx = std::min(max_ctas, G);
+    int64_t groups_per_cta = (G + gx - 1) / gx;
+    if (mode == MODE_MOE) {
+        // the kernel shares the grid among the experts the ids pick (at most
+        // n_potential_experts); at least one CTA per possible expert
+        gx = std::max<int64_t>(max_ctas, static_cast<int64_t>(p.n_tokens) * p.top_k);
+        groups_per_cta = (G * n_potential_experts + gx - 1) / gx;
+    }
+    max_wpc = static_cast<int>(std::min<int64_t>(max_wpc, std::max<int64_t>(1, groups_per_cta)));
     // Budget: by default half of an SM's shared memory, so that the next
-    // kernel's CTA fits beside this one and streams its first tiles early.
-    // Warps and stages are fixed from the packed activations alone, so the
-    // fp32-input and q8_1-input launches of a shape share one geometry (and
-    // produce bit-identical results).
-    const int share = tu.smem_share.load() > 0 ? tu.smem_share.load() : 2;
-    const size_t budget = std::min(dev.smem_limit, dev.smem_per_sm / share - SMEM_RESERVE);
+    // kernel's CTA fits beside this one and streams its first tiles early --
+    // unless that would give some warp more row groups than the whole SM's
+    // budget would (more serial work outweighs the overlap).  Warps and stages
+    // are fixed from the packed activations alone, so the fp32-input and
+    // q8_1-input launches of a shape share one geometry (and produce
+    // bit-identical results).
+    const size_t st_smem = static_smem(fn);
+    const size_t fn_limit = std::min(dev.smem_limit, dev.smem_limit + SMEM_RESERVE - st_smem);
     auto need = [&](int w, int st, size_t act) { return act + static_cast<size_t>(w) * st * tb + 128; };
-    while (max_wpc > 1 && need(max_wpc, stages, packed) > budget) --max_wpc;
-    while (stages > 1 && need(max_wpc, stages, packed) > budget) --stages;
-    if (need(max_wpc, stages, packed) > dev.smem_limit) return false;
+    auto fit = [&](size_t budget, int &w, int &st) {
+        w = max_wpc;
+        st = stages;
+        while (w > 1 && need(w, st, packed) > budget) --w;
+        while (st > 1 && need(w, st, packed) > budget) --st;
+        return need(w, st, packed) <= budget;
+    };
+    auto share_budget = [&](int share) {
+        return std::min(fn_limit, dev.smem_per_sm / share - dev.smem_resv - st_smem);
+    };
+    int wpc_f = 0, st_f = 0;
+    const bool tuned_share = tu.smem_share.load() > 0;
+    size_t budget = share_budget(tuned_share ? tu.smem_share.load() : 2);
+    if (!fit(budget, wpc_f, st_f)) {
+        budget = fn_limit;
+        if (!fit(budget, wpc_f, st_f)) return TilePlan::NoFit;
+    } else if (!tuned_share && mode != MODE_MOE) {
+        int wpc_1 = 0, st_1 = 0;
+        const int64_t gpc = (G + gx - 1) / gx;  // most row groups a CTA owns
+        if (fit(fn_limit, wpc_1, st_1) && (gpc + wpc_1 - 1) / wpc_1 < (gpc + wpc_f - 1) / wpc_f) {
+            budget = fn_limit;
+            wpc_f = wpc_1;
+            st_f = st_1;
+        }
+    }
+    max_wpc = wpc_f;
+    stages = st_f;
     // the raw copy of the q8_1 blocks (coalesced staging) only if it still fits;
     // fp32 input is quantized straight into the packed layout
     size_t act = packed;
     if (p.xf == nullptr && need(max_wpc, stages, packed + raw) <= budget) act = packed + raw;
     const int wpc = max_wpc;
     const size_t smem = need(wpc, stages, act);
-    if (ensure_smem_attr(dev, fn) != QMV_OK) return false;
-    if (occupancy(dev.dev, fn, wpc * 32, smem) <= 0) return false;
+    if (ensure_smem_attr(dev, fn) != QMV_OK) return TilePlan::Error;
+    if (occupancy(dev.dev, fn, wpc * 32, smem) <= 0) return TilePlan::Error;
     p.units_per_row = U;
     p.n_groups = G;
     p.stages = stages;
@@ -223,9 +276,9 @@ bool plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t,
     L.stream = true;
     L.p = p;
     L.block = dim3(static_cast<unsigned>(wpc * 32));
-    L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)), mode == MODE_MOE ? p.n_expert + 1 : 1);
+    L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)));
     L.smem = smem;
-    return true;
+    return TilePlan::Ok;
 }
 
 // Host checks of the fused fp32-input path (before any CUDA call): the tile
@@ -247,8 +300,11 @@ qmv_status plan_f32(int type, int mode, const DevInfo &dev, GemvParams p, int nc
     if (reinterpret_cast<uintptr_t>(p.W) % 16 != 0 ||
         (mode == MODE_GATE && reinterpret_cast<uintptr_t>(p.W2) % 16 != 0))
         return QMV_ERR_ALIGN;
-    if (!plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L)) return QMV_ERR_SHAPE;
-    return QMV_OK;
+    switch (plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L)) {
+    case TilePlan::Ok: return QMV_OK;
+    case TilePlan::NoFit: return QMV_ERR_SHAPE;
+    default: return QMV_ERR_CUDA;
+    }
 }
 
 qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_active, int n_potential_experts,
@@ -257,7 +313,9 @@ qmv_status plan(int type, int mode, const DevInfo &dev, GemvParams p, int nc_act
     const int nc_t = (mode == MODE_PLAIN) ? nc_active : round_nc(nc_active);
     if (tile_shape_ok(type, p.K, p.row_bytes) && reinterpret_cast<uintptr_t>(p.W) % 16 == 0 &&
         (mode != MODE_GATE || reinterpret_cast<uintptr_t>(p.W2) % 16 == 0)) {
-        if (plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L)) return QMV_OK;
+        const TilePlan tp = plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L);
+        if (tp == TilePlan::Ok) return QMV_OK;
+        if (tp == TilePlan::Error) return QMV_ERR_CUDA;
     }
     L.fn = gemv_generic_fn(type, mode);
     if (!L.fn) return QMV_ERR_TYPE;

@@ -238,6 +238,13 @@ __device__ __forceinline__ float ld_cg_f32(const float *p)
     return v;
 }
 
+__device__ __forceinline__ int ld_cg_s32(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 // ---- per-thread asynchronous copies (cp.async, 16 bytes) --------------------
 
 // 16-byte global -> shared copy that bypasses registers and L1 (.cg); both

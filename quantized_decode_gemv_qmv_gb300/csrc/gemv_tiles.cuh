@@ -37,6 +37,7 @@ namespace qmv {
 constexpr int TILE_MAX_THREADS = 384;
 constexpr int TILE_MAX_STAGES = 4;
 constexpr int STAGE_BATCH = 4;  // activation loads in flight per thread while staging
+constexpr int MOE_MAX_SLOTS = 256;  // n_tokens * top_k <= 8 * 32
 
 // Tile geometry for format F and RW rows per tile: UW = 32/RW units per tile
 // row (one per lane), the row segment SEG 16-byte pieces long, PER_LANE copy
@@ -218,43 +219,73 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 
     int n_active = p.ncols;
     int64_t row_base = 0;  // MoE: first row of this CTA's expert
+    int64_t cta_index = blockIdx.x, cta_count = gridDim.x;
     if constexpr (MODE == MODE_MOE) {
-        pdl_wait();  // the expert ids come from the previous grid
-        if (blockIdx.y == static_cast<unsigned>(p.n_expert)) {
+        // Routing is known only here (ids come from the previous grid).  The
+        // experts some token picks are listed in ascending order and the grid
+        // is shared among them -- CTA b serves expert floor(b*T/grid) -- so
+        // every SM works whatever the routing.  CTA 0 also zero-fills the
+        // outputs of invalid ids and counts them.
+        __shared__ int s_exp[MOE_MAX_SLOTS];
+        __shared__ int s_ne;
+        pdl_wait();
+        const int n_slots = p.n_tokens * p.top_k;
+        if (threadIdx.x == 0) {
+            int ne = 0;
+            for (int s = 0; s < n_slots; ++s) {
+                const int e = ld_cg_s32(p.ids + s);
+                if (e < 0 || e >= p.n_expert) continue;
+                int j = ne;
+                while (j > 0 && s_exp[j - 1] > e) --j;
+                if (j > 0 && s_exp[j - 1] == e) continue;
+                for (int k = ne; k > j; --k) s_exp[k] = s_exp[k - 1];
+                s_exp[j] = e;
+                ++ne;
+            }
+            s_ne = ne;
+        }
+        __syncthreads();
+        const int ne = s_ne;
+        if (blockIdx.x == 0) {
             int bad = 0;
-            for (int s = 0; s < p.n_tokens * p.top_k; ++s) {
-                const int e = p.ids[s];
+            for (int s = 0; s < n_slots; ++s) {
+                const int e = ld_cg_s32(p.ids + s);
                 if (e < 0 || e >= p.n_expert) {
                     ++bad;
                     float *ys = p.y + (size_t)s * p.M;
-                    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < p.M;
-                         r += (int64_t)gridDim.x * blockDim.x)
-                        ys[r] = 0.f;
+                    for (int64_t r = threadIdx.x; r < p.M; r += blockDim.x) ys[r] = 0.f;
                 }
             }
-            if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) *p.status = bad;
-            return;
+            if (threadIdx.x == 0 && p.status) *p.status = bad;
         }
+        if (ne == 0) return;
+        const int G = static_cast<int>(gridDim.x);
+        const int e_idx = static_cast<int>(static_cast<int64_t>(blockIdx.x) * ne / G);
+        const int64_t first = (static_cast<int64_t>(e_idx) * G + ne - 1) / ne;
+        const int64_t next = (static_cast<int64_t>(e_idx + 1) * G + ne - 1) / ne;
+        const int expert = s_exp[e_idx];
+        cta_index = blockIdx.x - first;
+        cta_count = next - first;
         if (threadIdx.x == 0) {
             int cnt = 0;
             for (int t = 0; t < p.n_tokens; ++t) {
                 uint32_t mask = 0;
                 for (int k = 0; k < p.top_k; ++k)
-                    if (p.ids[t * p.top_k + k] == static_cast<int>(blockIdx.y)) mask |= 1u << k;
+                    if (ld_cg_s32(p.ids + t * p.top_k + k) == expert) mask |= 1u << k;
                 if (mask) { s_tok[cnt] = t; s_slots[cnt] = mask; ++cnt; }
             }
             s_cnt = cnt;
         }
         __syncthreads();
         n_active = s_cnt;
-        if (n_active == 0) return;
-        row_base = static_cast<int64_t>(blockIdx.y) * p.M;
+        row_base = static_cast<int64_t>(expert) * p.M;
     }
 
-    // every warp of the grid owns a contiguous, balanced range of row groups
-    // (whole groups: a row's partial sums never leave the warp)
-    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
-    const int64_t wtot = static_cast<int64_t>(gridDim.x) * nwarps;
+    // every warp (of the grid; MoE: of the expert's CTAs) owns a contiguous,
+    // balanced range of row groups (whole groups: a row's partial sums never
+    // leave the warp)
+    const int64_t gwarp = cta_index * nwarps + warp;
+    const int64_t wtot = cta_count * nwarps;
     const int64_t g_begin = (gwarp * p.n_groups) / wtot;
     const int64_t my_groups = ((gwarp + 1) * p.n_groups) / wtot - g_begin;
     const int64_t total = my_groups * n_kt * NM;
