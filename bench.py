@@ -53,8 +53,8 @@ SHAPES = {"4096x4096": (D_MODEL, D_MODEL), "11008x4096": (D_FF, D_MODEL), "4096x
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "5f1ec1dc6ea38e04", "bytes_per_launch": 16290688,
-           "shape": "step mix 4x 4096x4096 : 2x 11008x4096 : 1x 4096x11008 (profiles/gemv_tiles_q4_K_4096x11008.md)"}
+TRAFFIC = {"csrc_sha": "dbd12f8e1c2a9fac", "bytes_per_launch": 28543680,
+           "shape": "mean of the step's launch kinds qkv, o, gate+up, down (profiles/gemv_tiles_q4_K_down_fused.md)"}
 
 
 def row_bytes(M, K):
