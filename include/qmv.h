@@ -158,9 +158,10 @@ int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int
  * here the quantize pass is not a separate kernel at all), so y is
  * bit-identical to qmv_quantize_q8_1 followed by the q8_1-input call, with one
  * kernel launch instead of two.  Available for Q4_0 and Q4_K with K a
- * multiple of 256 and W (and W_gate) 16-byte aligned; otherwise returns
- * QMV_ERR_TYPE (Q6_K), QMV_ERR_SHAPE or QMV_ERR_ALIGN before launching, and
- * the q8_1-input calls apply.  Arguments, limits, outputs and error behaviour
+ * multiple of 256 and for Q6_K with K a multiple of 2048, W (and W_gate)
+ * 16-byte aligned; otherwise returns QMV_ERR_SHAPE or QMV_ERR_ALIGN before
+ * launching (QMV_ERR_TYPE for a type that is not a weight type), and the
+ * q8_1-input calls apply.  Arguments, limits, outputs and error behaviour
  * are otherwise those of the calls above. */
 int qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const float *x, int64_t ldx,
                         int ncols, float *y, void *stream);
