@@ -194,17 +194,22 @@ int qmv_device_fault(unsigned int *code);
  * Overrides the launch geometry the library picks for the streaming GEMV of
  * `type` (0 = keep the built-in choice for that field).  Meant for tuning
  * sweeps; results are identical for every setting.
- *   Q4_0 / Q4_K (tile kernel): threads = most threads per CTA (multiple of 32,
- *     <= 384); slice_units = units of 144 bytes per tile row (4, 8 or 16:
+ *   Q4_0 / Q4_K (tile kernel): threads = threads per CTA (multiple of 32,
+ *     <= 384; all of them stage the activations, as many warps as the row
+ *     groups and shared memory allow also stream weights); slice_units = units of 144 bytes per tile row (4, 8 or 16:
  *     tiles of 8, 4 or 2 rows; 8 and 2 only for one plain column);
  *     stages = tile buffers per warp (1..4); ctas_per_sm = CTAs per SM;
  *     smem_share = a CTA takes at most 1/smem_share of an SM's shared
  *     memory (1..4, default 2, which leaves room for the next kernel).
  *   Q6_K: the same tile kernel with tiles of 4 rows x 8 super-blocks
  *     (slice_units is ignored).
+ *   cluster: CTAs per thread-block cluster for the fp32-input plain and
+ *     gate/up calls (1..8; 1 = no cluster), which share the quantization of
+ *     the activations among the cluster's CTAs (default 2).
  * Returns QMV_ERR_TYPE for a non-weight type, QMV_ERR_SHAPE for values out of
  * range. */
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share);
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share,
+                   int cluster);
 
 /* Enables (1, default) or disables (0) programmatic dependent launch for the
  * library's q8_1 and GEMV kernels.  When enabled, a GEMV may start streaming

@@ -76,7 +76,7 @@ def lib():
                                              _vp]
         L.qmv_debug_subblock_sums.argtypes = [_int, _vp, _i64, _i64, _vp, _int, _vp, _vp]
         L.qmv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
-        L.qmv_set_tuning.argtypes = [_int, _int, _int, _int, _int, _int]
+        L.qmv_set_tuning.argtypes = [_int, _int, _int, _int, _int, _int, _int]
         L.qmv_set_pdl.argtypes = [_int]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
@@ -266,9 +266,10 @@ def device_fault() -> int:
 
 
 def set_tuning(qtype: int, threads: int = 0, slice_units: int = 0, stages: int = 0, ctas_per_sm: int = 0,
-               smem_share: int = 0):
+               smem_share: int = 0, cluster: int = 0):
     """Launch-geometry override for sweeps (0 keeps the default; see include/qmv.h)."""
-    _check("qmv_set_tuning", lib().qmv_set_tuning(qtype, threads, slice_units, stages, ctas_per_sm, smem_share))
+    _check("qmv_set_tuning",
+           lib().qmv_set_tuning(qtype, threads, slice_units, stages, ctas_per_sm, smem_share, cluster))
 
 
 def set_pdl(enable: bool):

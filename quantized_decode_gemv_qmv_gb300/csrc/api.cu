@@ -54,11 +54,13 @@ namespace {
 
 constexpr int MAX_DEVICES = 64;
 constexpr size_t SMEM_RESERVE = 2048;  // static shared memory (MoE token lists) and alignment slack per CTA
+constexpr int F32_CLUSTER = 2;         // CTAs that share the quantization of fp32 activations (a TPC pair)
+constexpr int MAX_CLUSTER = 8;         // portable cluster size limit
 
 std::atomic<int> g_pdl{1};
 
 struct Tuning {
-    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0};
+    std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0}, cluster{0};
 };
 Tuning g_tuning[3];
 
@@ -66,6 +68,7 @@ int tidx(int type) { return type == FMT_Q4_0 ? 0 : type == FMT_Q4_K ? 1 : 2; }
 
 std::mutex g_mu;
 std::map<std::tuple<int, const void *, int, size_t>, int> g_occupancy;  // (dev, fn, threads, smem) -> CTAs/SM
+std::map<std::tuple<int, const void *, int, size_t, int>, int> g_clusters;  // (..., cluster size) -> resident clusters
 std::map<std::pair<int, const void *>, bool> g_smem_attr;
 int g_num_sms[MAX_DEVICES];
 int g_smem_optin[MAX_DEVICES];
@@ -151,6 +154,33 @@ int occupancy(int dev, const void *fn, int threads, size_t smem)
     return n;
 }
 
+// Clusters of `cl` CTAs of fn that can be resident at once (0: none fits).
+int cluster_occupancy(int dev, const void *fn, int threads, size_t smem, int cl)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(dev, fn, threads, smem, cl);
+    auto it = g_clusters.find(key);
+    if (it != g_clusters.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cl));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    g_clusters[key] = n;
+    return n;
+}
+
 int round_nc(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -158,6 +188,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Launch {
     const void *fn = nullptr;
     bool stream = false;
+    int cluster = 1;  // CTAs per cluster (1: no cluster dimension)
     GemvParams p{};
     dim3 grid, block;
     size_t smem = 0;
@@ -207,6 +238,10 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     stages = std::max(1, std::min(TILE_MAX_STAGES, stages));
     int max_wpc = tu.threads.load() ? tu.threads.load() / 32 : TILE_MAX_THREADS / 32;
     max_wpc = std::max(1, std::min(TILE_MAX_THREADS / 32, max_wpc));
+    // every CTA has this many warps: all of them stage the activations (a
+    // latency-bound phase that wants many warps), the first wpc of them also
+    // stream and decode weight tiles
+    const int cta_warps = max_wpc;
 
     // grid: every SM first (MoE: the SMs shared among the experts that may be
     // picked), then more warps per CTA; warps own whole row groups
@@ -266,16 +301,31 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     const int wpc = max_wpc;
     const size_t smem = need(wpc, stages, act);
     if (ensure_smem_attr(dev, fn) != QMV_OK) return TilePlan::Error;
-    if (occupancy(dev.dev, fn, wpc * 32, smem) <= 0) return TilePlan::Error;
+    if (occupancy(dev.dev, fn, cta_warps * 32, smem) <= 0) return TilePlan::Error;
+    // fp32 input: clusters of CTAs share the quantization of the activations
+    // (the grid becomes a whole number of clusters; CTAs without row groups
+    // still take their share); one CTA per cluster if no such cluster fits
+    int cl = 1;
+    if (p.xf != nullptr && (mode == MODE_PLAIN || mode == MODE_GATE)) {
+        cl = tu.cluster.load() ? tu.cluster.load() : F32_CLUSTER;
+        cl = std::max(1, std::min(MAX_CLUSTER, cl));
+        if (cl > 1) {
+            const int64_t gx_cl = (gx + cl - 1) / cl * cl;
+            if (cluster_occupancy(dev.dev, fn, cta_warps * 32, smem, cl) > 0) gx = gx_cl;
+            else cl = 1;
+        }
+    }
     p.units_per_row = U;
     p.n_groups = G;
     p.stages = stages;
+    p.dec_warps = wpc;
     p.act_bytes = static_cast<uint32_t>(act);
     p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
     L.fn = fn;
     L.stream = true;
+    L.cluster = cl;
     L.p = p;
-    L.block = dim3(static_cast<unsigned>(wpc * 32));
+    L.block = dim3(static_cast<unsigned>(cta_warps * 32));
     L.grid = dim3(static_cast<unsigned>(std::max<int64_t>(1, gx)));
     L.smem = smem;
     return TilePlan::Ok;
@@ -338,11 +388,22 @@ qmv_status launch(const Launch &L, cudaStream_t st)
     cfg.blockDim = L.block;
     cfg.dynamicSmemBytes = L.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 0;
+    if (g_pdl.load()) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
+    if (L.cluster > 1) {
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = static_cast<unsigned>(L.cluster);
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = g_pdl.load() ? 1 : 0;
+    cfg.numAttrs = n_attr;
     GemvParams p = L.p;
     void *args[1] = {&p};
     cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, args);
@@ -592,11 +653,11 @@ int qmv_device_fault(unsigned int *code)
     return QMV_OK;
 }
 
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share)
+int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share, int cluster)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (threads < 0 || threads > TILE_MAX_THREADS || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
-        ctas_per_sm < 0 || smem_share < 0 || smem_share > 4)
+        ctas_per_sm < 0 || smem_share < 0 || smem_share > 4 || cluster < 0 || cluster > MAX_CLUSTER)
         return QMV_ERR_SHAPE;
     Tuning &t = g_tuning[tidx(type)];
     t.threads = threads;
@@ -604,6 +665,7 @@ int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_
     t.stages = stages;
     t.ctas_per_sm = ctas_per_sm;
     t.smem_share = smem_share;
+    t.cluster = cluster;
     return QMV_OK;
 }
 

@@ -36,7 +36,7 @@ namespace qmv {
 
 constexpr int TILE_MAX_THREADS = 384;
 constexpr int TILE_MAX_STAGES = 4;
-constexpr int STAGE_BATCH = 4;  // activation loads in flight per thread while staging
+constexpr int STAGE_BATCH = 4;  // q8_1 staging: 16-byte loads in flight per thread
 constexpr int MOE_MAX_SLOTS = 256;  // n_tokens * top_k <= 8 * 32
 
 // Tile geometry for format F and RW rows per tile: UW = 32/RW units per tile
@@ -85,55 +85,86 @@ inline int tile_bytes_rt(int type, int rw)
 // With fp32 input (p.xf) the activations are quantized here, straight into the
 // repacked layout, with the q8_1 block arithmetic of the standalone quantizer
 // (q8_1.cuh): the staged values, and so y, are bit-identical to quantizing
-// first and passing the q8_1 blocks.
+// first and passing the q8_1 blocks.  In a cluster of ncta CTAs, CTA crank
+// quantizes only its share of the blocks (a contiguous 1/ncta of them) and
+// stores each result into the shared memory of every CTA of the cluster
+// (distributed shared memory), so the work is not repeated in every CTA; the
+// caller has made sure every CTA of the cluster is running, and completes the
+// exchange with a cluster barrier.
 template <int F, int NC, typename ColFn>
-__device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint8_t *smem, int n_active, ColFn src_col)
+__device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint8_t *smem, int n_active, ColFn src_col,
+                                                       uint32_t crank, uint32_t ncta)
 {
     if (p.xf != nullptr) {
         const int U = p.units_per_row;
         const int nblk = U * 8;                 // q8_1 blocks per column (K = 256 U)
-        const int tasks = n_active * nblk * 4;  // 4 lanes per block
+        const int n_all = n_active * nblk;      // blocks of all columns
+        const int blk0 = static_cast<int>(static_cast<int64_t>(crank) * n_all / ncta);
+        const int blk1 = static_cast<int>(static_cast<int64_t>(crank + 1) * n_all / ncta);
+        const int tasks = (blk1 - blk0) * 4;    // 4 lanes per block
         const bool vec = ((reinterpret_cast<uintptr_t>(p.xf) | static_cast<uintptr_t>(p.ldx * 4)) & 15u) == 0;
-        uint8_t *act_qs = smem;
-        uint8_t *act_sc = smem + (size_t)NC * U * ACT_QS_STRIDE;
+        const uint32_t act_qs = smem_u32(smem);
+        const uint32_t act_sc = act_qs + static_cast<uint32_t>(NC * U * ACT_QS_STRIDE);
         const int rounds = (tasks + blockDim.x - 1) / blockDim.x;  // the same for every thread
-        // STAGE_BATCH rounds of loads in flight before any is consumed: one
-        // L2 round trip per batch, not per round
-        for (int r0 = 0; r0 < rounds; r0 += STAGE_BATCH) {
-            float v[STAGE_BATCH][8];
+        // One round (blockDim.x tasks) at a time, the next round's loads issued
+        // before this round's arithmetic: the load latency overlaps the
+        // quantization while the code holds a single copy of it (the staging
+        // runs once per CTA, from a cold instruction cache when kernels of
+        // another instance share the SM).
+        auto load = [&](int r, float (&v)[8]) {
+            const int t = r * blockDim.x + threadIdx.x;
 #pragma unroll
-            for (int r = 0; r < STAGE_BATCH; ++r) {
-                const int t = (r0 + r) * blockDim.x + threadIdx.x;
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+            if (t < tasks) {
+                const int g = blk0 * 4 + t;
+                const int c = NC == 1 ? 0 : g / (nblk * 4);
+                const int rem = g - c * nblk * 4;
+                q8_1_load8(p.xf + (size_t)src_col(c) * p.ldx, (int64_t)(rem >> 2) * QK8_1 + 8 * (rem & 3), p.K, vec, v);
+            }
+        };
+        float v[8];
+        if (rounds > 0) load(0, v);
+        for (int r = 0; r < rounds; ++r) {
+            float vn[8];
+            load(r + 1, vn);  // zeros past the last round
+            const int t = r * blockDim.x + threadIdx.x;
+            uint32_t w0, w1, ds;
+            int S, part;
+            q8_1_block_group4(v, w0, w1, ds, S, part);
+            // half sums: codes 0..15 (lanes 0, 1 of the group), 16..31 (lanes 2, 3)
+            const int half = part + __shfl_xor_sync(0xffffffffu, part, 1);
+            const int other = __shfl_xor_sync(0xffffffffu, half, 2);
+            if (t < tasks) {
+                const int g = blk0 * 4 + t;
+                const int c = NC == 1 ? 0 : g / (nblk * 4);
+                const int rem = g - c * nblk * 4;
+                const int n = rem >> 2, j = rem & 3;
+                const int u = n >> 3, sub = n & 7;
+                const uint32_t dq = act_qs + static_cast<uint32_t>((c * U + u) * ACT_QS_STRIDE + 32 * sub + 8 * j);
+                const uint32_t sc = act_sc + static_cast<uint32_t>((c * U + u) * act_sc_stride<F>());
+                uint32_t off[3], val[3];
+                const int nw = act_scalar_words<F>(sub, ds, S, half, other, off, val);
+                if (ncta == 1) {
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dq), "r"(w0), "r"(w1) : "memory");
+                    if (j == 0) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[r][i] = 0.f;
-                if (r0 + r < rounds && t < tasks) {
-                    const int c = t / (nblk * 4);
-                    const int rem = t - c * nblk * 4;
-                    q8_1_load8(p.xf + (size_t)src_col(c) * p.ldx, (int64_t)(rem >> 2) * QK8_1 + 8 * (rem & 3), p.K,
-                               vec, v[r]);
+                        for (int i = 0; i < 3; ++i)
+                            if (i < nw) asm volatile("st.shared.u32 [%0], %1;" ::"r"(sc + off[i]), "r"(val[i]) : "memory");
+                    }
+                } else {
+                    for (uint32_t q = 0; q < ncta; ++q) {
+                        st_cluster_v2(mapa_shared(dq, q), w0, w1);
+                        if (j == 0) {
+                            const uint32_t scq = mapa_shared(sc, q);
+#pragma unroll
+                            for (int i = 0; i < 3; ++i)
+                                if (i < nw) st_cluster_u32(scq + off[i], val[i]);
+                        }
+                    }
                 }
             }
 #pragma unroll
-            for (int r = 0; r < STAGE_BATCH; ++r) {
-                if (r0 + r >= rounds) break;  // uniform: every lane reaches the group reductions
-                const int t = (r0 + r) * blockDim.x + threadIdx.x;
-                uint32_t w0, w1, ds;
-                int S, part;
-                q8_1_block_group4(v[r], w0, w1, ds, S, part);
-                // half sums: codes 0..15 (lanes 0, 1 of the group), 16..31 (lanes 2, 3)
-                const int half = part + __shfl_xor_sync(0xffffffffu, part, 1);
-                const int other = __shfl_xor_sync(0xffffffffu, half, 2);
-                if (t < tasks) {
-                    const int c = t / (nblk * 4);
-                    const int rem = t - c * nblk * 4;
-                    const int n = rem >> 2, j = rem & 3;
-                    const int u = n >> 3, sub = n & 7;
-                    uint2 *dq = reinterpret_cast<uint2 *>(act_qs + ((size_t)c * U + u) * ACT_QS_STRIDE + 32 * sub + 8 * j);
-                    *dq = make_uint2(w0, w1);
-                    if (j == 0)
-                        store_act_scalars<F>(act_sc + ((size_t)c * U + u) * act_sc_stride<F>(), sub, ds, S, half, other);
-                }
-            }
+            for (int i = 0; i < 8; ++i) v[i] = vn[i];
         }
         return;
     }
@@ -207,7 +238,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     constexpr int NM = (MODE == MODE_GATE) ? 2 : 1;  // matrices (GATE: up, gate)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
+    const int nwarps = p.dec_warps;  // warps that stream and decode; the others only help staging
     const int U = p.units_per_row;
     const int r_l = lane % RW;  // this lane's row inside a tile
     const int u_l = lane / RW;  // this lane's unit inside a tile
@@ -216,6 +247,16 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     const int stages = p.stages;
 
     pdl_launch_dependents();
+    // fp32 input in a cluster: the CTAs share the quantization (see
+    // stage_tile_activations); this arrive lets the others know this CTA runs
+    uint32_t crank = 0, ncta = 1;
+    if constexpr (MODE == MODE_PLAIN || MODE == MODE_GATE) {
+        ncta = cluster_nctarank();
+        if (ncta > 1) {
+            crank = cluster_ctarank();
+            cluster_arrive_relaxed();
+        }
+    }
 
     int n_active = p.ncols;
     int64_t row_base = 0;  // MoE: first row of this CTA's expert
@@ -286,11 +327,11 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     // leave the warp)
     const int64_t gwarp = cta_index * nwarps + warp;
     const int64_t wtot = cta_count * nwarps;
-    const int64_t g_begin = (gwarp * p.n_groups) / wtot;
-    const int64_t my_groups = ((gwarp + 1) * p.n_groups) / wtot - g_begin;
+    const int64_t g_begin = warp < nwarps ? (gwarp * p.n_groups) / wtot : 0;
+    const int64_t my_groups = warp < nwarps ? ((gwarp + 1) * p.n_groups) / wtot - g_begin : 0;
     const int64_t total = my_groups * n_kt * NM;
 
-    const uint32_t ring = smem_u32(smem + p.act_bytes) + static_cast<uint32_t>(warp * stages * TB);
+    const uint32_t ring = smem_u32(smem + p.act_bytes) + static_cast<uint32_t>(min(warp, nwarps - 1) * stages * TB);
 
     // ---- copies: tile (group, k-tile, matrix) -> ring buffer, one group per tile ----
     int64_t ld_g = g_begin;
@@ -322,11 +363,17 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 
     while (issued < total && issued < stages) issue_tile();  // weights first
     if constexpr (MODE != MODE_MOE) pdl_wait();
+    if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
     if constexpr (MODE == MODE_MOE)
-        stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; });
+        stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; }, 0u, 1u);
     else
-        stage_tile_activations<F, NC>(p, smem, n_active, [](int c) { return c; });
-    __syncthreads();
+        stage_tile_activations<F, NC>(p, smem, n_active, [](int c) { return c; }, crank, ncta);
+    if (ncta > 1) {
+        cluster_arrive();  // this CTA's share is stored everywhere ...
+        cluster_wait();    // ... and every share is here; no remote access after this point
+    } else {
+        __syncthreads();
+    }
 
     const uint32_t act_qs = smem_u32(smem);
     const uint32_t act_sc = act_qs + NC * U * ACT_QS_STRIDE;

@@ -38,26 +38,48 @@ __host__ __device__ constexpr int act_sc_stride()
     return F == FMT_Q6_K ? 96 : ACT_SC_STRIDE;
 }
 
-// Writes the scalars of q8_1 block `sub` (0..7) of a unit: ds = (half d | half
-// s << 16) as stored, S = the block's code sum, S_lo / S_hi = the sums of its
-// codes 0..15 / 16..31.
+// The scalars of q8_1 block `sub` (0..7) of a unit as 32-bit words of the
+// unit's scalar area: n words, word i at byte offset off[i] holding val[i].
+// ds = (half d | half s << 16) as stored, S = the block's code sum, S_lo / S_hi
+// = the sums of its codes 0..15 / 16..31.
+template <int F>
+__device__ __forceinline__ int act_scalar_words(int sub, uint32_t ds, int S, int S_lo, int S_hi, uint32_t (&off)[3],
+                                                uint32_t (&val)[3])
+{
+    const float d8 = half_bits_to_float(ds);
+    if constexpr (F == FMT_Q4_K) {
+        off[0] = 4u * (4 * (sub >> 1) + (sub & 1));
+        val[0] = __float_as_uint(d8);
+        off[1] = 4u * (4 * (sub >> 1) + 2 + (sub & 1));
+        val[1] = __float_as_uint(d8 * static_cast<float>(S));
+        return 2;
+    } else if constexpr (F == FMT_Q4_0) {
+        off[0] = 8u * sub;
+        val[0] = __float_as_uint(d8);
+        off[1] = 8u * sub + 4u;
+        val[1] = __float_as_uint(half_bits_to_float(ds >> 16));
+        return 2;
+    } else {
+        off[0] = 4u * sub;
+        val[0] = __float_as_uint(d8);
+        off[1] = 32u + 8u * sub;
+        val[1] = static_cast<uint32_t>(S_lo);
+        off[2] = 36u + 8u * sub;
+        val[2] = static_cast<uint32_t>(S_hi);
+        return 3;
+    }
+}
+
+// Writes the scalars of q8_1 block `sub` of a unit (act_scalar_words) into this
+// CTA's shared memory at sc_unit.
 template <int F>
 __device__ __forceinline__ void store_act_scalars(uint8_t *sc_unit, int sub, uint32_t ds, int S, int S_lo, int S_hi)
 {
-    float *sc = reinterpret_cast<float *>(sc_unit);
-    const float d8 = half_bits_to_float(ds);
-    if constexpr (F == FMT_Q4_K) {
-        sc[4 * (sub >> 1) + (sub & 1)] = d8;
-        sc[4 * (sub >> 1) + 2 + (sub & 1)] = d8 * static_cast<float>(S);
-    } else if constexpr (F == FMT_Q4_0) {
-        sc[2 * sub] = d8;
-        sc[2 * sub + 1] = half_bits_to_float(ds >> 16);
-    } else {
-        sc[sub] = d8;
-        int *s16 = reinterpret_cast<int *>(sc + 8);
-        s16[2 * sub] = S_lo;
-        s16[2 * sub + 1] = S_hi;
-    }
+    uint32_t off[3], val[3];
+    const int n = act_scalar_words<F>(sub, ds, S, S_lo, S_hi, off, val);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        if (i < n) *reinterpret_cast<uint32_t *>(sc_unit + off[i]) = val[i];
 }
 
 // NW consecutive 32-bit words starting at a 2-byte aligned shared address: the

@@ -55,29 +55,32 @@ __device__ __forceinline__ void q8_1_block_group4(const float (&v)[8], uint32_t 
     const float d = __fdiv_rn(amax, 127.0f);
     int s = 0;
     uint32_t b[8];
-    // x/d is needed correctly rounded (the integer code is rounded from the fp32
-    // quotient).  Markstein's final-correction step (Markstein, "Computation of
-    // elementary functions on the IBM RISC System/6000 processor", 1990):
-    // with r = RN(1/d), q0 = RN(x*r) is within an ulp of x/d, the residual
-    // x - d*q0 is exact in one FMA, and RN(q0 + r*(x - d*q0)) = RN(x/d), as long
-    // as nothing overflows or underflows -- guaranteed for d in [2^-40, 2^40]
-    // and |x/d| >= 2^-30 (the residual then stays a normal number; smaller
-    // quotients round to code 0 either way).  Other blocks use the IEEE
-    // division itself.
+    // x/d is needed correctly rounded (the integer code is rounded from the
+    // fp32 quotient).  With y = RN(1/d), Markstein's correction (Markstein,
+    // "Computation of elementary functions on the IBM RISC System/6000
+    // processor", IBM J. Res. Dev. 34(1), 1990) q' = RN(q + y*(x - d*q)), the
+    // residual x - d*q formed exactly by one FMA, returns RN(x/d) when q is
+    // within one ulp of x/d.  q0 = RN(x*y) can be up to 1.5 ulp off, so the
+    // correction is applied twice: q0 + y*(x - d*q0) = x/d + (q0 - x/d)(1 - d*y)
+    // with |1 - d*y| <= 2^-24, so even with the residual rounded the first step
+    // leaves q1 within 1/2 ulp + 3*2^-24 ulp < 1 ulp of x/d, and the second
+    // step is the theorem's case.  No intermediate over- or underflows for d in
+    // [2^-40, 2^40] and |x/d| >= 2^-30; smaller quotients give code 0 from
+    // either quotient.  Since d = RN(amax/127), |x/d| <= 127 (1 + 2^-23) and the
+    // codes need no clamp.  Other scales use the IEEE division itself.
     const bool fast = d >= 0x1p-40f && d <= 0x1p40f;  // the same for all 4 lanes of the block
-    const float r = fast ? __frcp_rn(d) : 0.0f;
-    const float tiny = d * 0x1p-30f;
+    const float y = fast ? __frcp_rn(d) : 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        float z;
+        int q;
         if (fast) {
-            const float q0 = __fmul_rn(v[i], r);
-            const float e = __fmaf_rn(-d, q0, v[i]);
-            z = fabsf(v[i]) < tiny ? 0.0f : __fmaf_rn(e, r, q0);
+            const float q0 = __fmul_rn(v[i], y);
+            const float q1 = __fmaf_rn(__fmaf_rn(-d, q0, v[i]), y, q0);
+            const float q2 = __fmaf_rn(__fmaf_rn(-d, q1, v[i]), y, q1);
+            q = static_cast<int>(roundf(q2));
         } else {
-            z = (d == 0.0f) ? 0.0f : __fdiv_rn(v[i], d);
+            q = clamp_round((d == 0.0f) ? 0.0f : __fdiv_rn(v[i], d), -127.0f, 127.0f);
         }
-        const int q = clamp_round(z, -127.0f, 127.0f);
         s += q;
         b[i] = static_cast<uint32_t>(q) & 0xffu;
     }

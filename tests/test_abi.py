@@ -98,8 +98,10 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_mul_mat_vec_id_f32(12, p, 8, 16, 4096, p, 4096, nul, 4, 2, p, nul, nul) == 1
     assert L.qmv_mul_mat_vec_id_f32(14, p, 8, 16, 2304, p, 2304, p, 4, 2, p, nul, nul) == 3
     # tuning knobs validate too
-    assert L.qmv_set_tuning(12, 100, 0, 0, 0, 0) == 3
-    assert L.qmv_set_tuning(12, 544, 0, 0, 0, 0) == 3
-    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 5) == 3
-    assert L.qmv_set_tuning(3, 0, 0, 0, 0, 0) == 2
-    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0) == 0
+    assert L.qmv_set_tuning(12, 100, 0, 0, 0, 0, 0) == 3
+    assert L.qmv_set_tuning(12, 544, 0, 0, 0, 0, 0) == 3
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 5, 0) == 3
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0, 9) == 3
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0, -1) == 3
+    assert L.qmv_set_tuning(3, 0, 0, 0, 0, 0, 0) == 2
+    assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0, 0) == 0

@@ -168,3 +168,24 @@ def test_fused_chain_reads_the_previous_kernels_output(q):
     y.zero_()
     g.replay()
     assert np.array_equal(host(y), y_ref)
+
+
+@pytest.mark.parametrize("cl", [1, 2, 8])
+@pytest.mark.parametrize("t,M,K,ncols", [(oracle.Q4_0, 5, 256, 3), (oracle.Q4_K, 203, 2304, 1),
+                                         (oracle.Q4_K, 3, 256, 8), (oracle.Q6_K, 77, 2048, 2)])
+def test_fused_cluster_sizes_bitwise(q, cl, t, M, K, ncols):
+    """The CTAs of a cluster share the quantization (each stores its blocks in
+    every CTA's shared memory): any cluster size, including more CTAs than row
+    groups and one q8_1 block per CTA, gives the two-step result bit for bit."""
+    W = weights(t, M, K, 1700 + M)
+    Wg = weights(t, M, K, 1701 + M)
+    x = synthetic.activations_f32(1702 + K, ncols, K, outlier_frac=0.01)
+    Wd, Wgd, xd = dev(W), dev(Wg), dev(x)
+    y_two = host(q.mul_mat_vec(t, Wd, M, K, q.quantize_q8_1(xd), ncols))
+    g_two = host(q.mul_mat_vec_gate_up_swiglu(t, Wgd, Wd, M, K, q.quantize_q8_1(xd), ncols))
+    q.set_tuning(t, cluster=cl)
+    try:
+        assert np.array_equal(host(q.mul_mat_vec_f32(t, Wd, M, K, xd)), y_two)
+        assert np.array_equal(host(q.mul_mat_vec_gate_up_swiglu_f32(t, Wgd, Wd, M, K, xd)), g_two)
+    finally:
+        q.set_tuning(t)
