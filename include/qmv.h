@@ -211,6 +211,15 @@ int qmv_device_fault(unsigned int *code);
 int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share,
                    int cluster);
 
+/* Two more launch-geometry overrides of the streaming GEMV of `type`, for
+ * sweeps (0 keeps the built-in choice; results are identical for every
+ * setting): dec_warps = most warps per CTA that stream and decode weight tiles
+ * (1..12); pre_tiles = tiles each of those warps requests before waiting for
+ * the previous kernel on the stream (1..4, at most the ring's stages; the
+ * rest of the ring is requested once the activations are staged).  Returns
+ * QMV_ERR_TYPE for a non-weight type, QMV_ERR_SHAPE for values out of range. */
+int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
+
 /* Enables (1, default) or disables (0) programmatic dependent launch for the
  * library's q8_1 and GEMV kernels.  When enabled, a GEMV may start streaming
  * its weights while the kernel before it on the stream is still finishing,

@@ -28,7 +28,7 @@ EXPORTS = (
     "qmv_status_str", "qmv_version", "qmv_row_bytes", "qmv_q8_1_padded_k", "qmv_q8_1_bytes",
     "qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec", "qmv_mul_mat_vec_gate_up_swiglu",
     "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32", "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32",
-    "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_pdl",
+    "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
 )
 
 
@@ -77,11 +77,12 @@ def lib():
         L.qmv_debug_subblock_sums.argtypes = [_int, _vp, _i64, _i64, _vp, _int, _vp, _vp]
         L.qmv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.qmv_set_tuning.argtypes = [_int, _int, _int, _int, _int, _int, _int]
+        L.qmv_set_stream_tuning.argtypes = [_int, _int, _int]
         L.qmv_set_pdl.argtypes = [_int]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
                      "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_debug_subblock_sums",
-                     "qmv_device_fault", "qmv_set_tuning", "qmv_set_pdl"):
+                     "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -270,6 +271,11 @@ def set_tuning(qtype: int, threads: int = 0, slice_units: int = 0, stages: int =
     """Launch-geometry override for sweeps (0 keeps the default; see include/qmv.h)."""
     _check("qmv_set_tuning",
            lib().qmv_set_tuning(qtype, threads, slice_units, stages, ctas_per_sm, smem_share, cluster))
+
+
+def set_stream_tuning(qtype: int, dec_warps: int = 0, pre_tiles: int = 0):
+    """Decoding warps per CTA and tiles per warp requested before the dependency wait (0: default)."""
+    _check("qmv_set_stream_tuning", lib().qmv_set_stream_tuning(qtype, dec_warps, pre_tiles))
 
 
 def set_pdl(enable: bool):

@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         ++issued;
     };
 
-    while (issued < total && issued < stages) issue_tile();  // weights first
+    while (issued < total && issued < p.pre_tiles) issue_tile();  // weights first
     if constexpr (MODE != MODE_MOE) pdl_wait();
     if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
     if constexpr (MODE == MODE_MOE)
@@ -374,6 +374,8 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     } else {
         __syncthreads();
     }
+
+    while (issued < total && issued < stages) issue_tile();  // the rest of the ring
 
     const uint32_t act_qs = smem_u32(smem);
     const uint32_t act_sc = act_qs + NC * U * ACT_QS_STRIDE;

@@ -105,3 +105,8 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0, -1) == 3
     assert L.qmv_set_tuning(3, 0, 0, 0, 0, 0, 0) == 2
     assert L.qmv_set_tuning(12, 0, 0, 0, 0, 0, 0) == 0
+    assert L.qmv_set_stream_tuning(12, 13, 0) == 3
+    assert L.qmv_set_stream_tuning(12, 0, 5) == 3
+    assert L.qmv_set_stream_tuning(12, -1, 0) == 3
+    assert L.qmv_set_stream_tuning(9, 0, 0) == 2
+    assert L.qmv_set_stream_tuning(12, 0, 0) == 0

@@ -221,6 +221,28 @@ def test_tuning_variants_agree(q, t, nc):
         q.set_tuning(t)
 
 
+@pytest.mark.parametrize("t", oracle.WEIGHT_TYPES)
+def test_stream_tuning_variants_agree(q, t):
+    # decoding warps and tiles requested before the dependency wait change the
+    # launch, never the result (bitwise: rows never change warps' arithmetic order)
+    M, K, nc = 517, 4096, 2
+    W = weights(t, M, K, 710 + t)
+    xq = oracle.quantize_q8_1(synthetic.activations_f32(711, nc, K))
+    y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq, nc)
+    Wd, xd = dev(W), dev(xq)
+    y0 = host(q.mul_mat_vec(t, Wd, M, K, xd, nc))
+    assert_close_l1(y0, y_ref, l1, f"type {t} default")
+    try:
+        for dw, pre, st in [(1, 1, 2), (3, 1, 1), (5, 2, 2), (12, 1, 4), (7, 3, 3), (2, 4, 4)]:
+            q.set_tuning(t, stages=st)
+            q.set_stream_tuning(t, dec_warps=dw, pre_tiles=pre)
+            y = host(q.mul_mat_vec(t, Wd, M, K, xd, nc))
+            assert_close_l1(y, y_ref, l1, f"type {t} dec_warps {dw} pre {pre} stages {st}")
+    finally:
+        q.set_tuning(t)
+        q.set_stream_tuning(t)
+
+
 # ---- fused gate/up + SwiGLU ------------------------------------------------------
 def _swiglu_tol(g, u, l1g, l1u):
     sig = 1.0 / (1.0 + np.exp(-g))
