@@ -333,6 +333,14 @@ def measure_configs(q, torch, stream, device, reps):
                                                                     out=y[:1, :14336], stream=stream) for g, u in pairs])
     out["q4_K gate+up 2x14336x4096 swiglu"] = {"us_per_call": round(us, 3),
                                                "weight_gbs": round(2 * ws[0].numel() / us / 1e3, 1)}
+    # the same with the fused epilogue's up and gate biases
+    bu = torch.from_numpy(synthetic.activations_f32(3_000_510, 1, 14336)[0]).to(device)
+    bg = torch.from_numpy(synthetic.activations_f32(3_000_511, 1, 14336)[0]).to(device)
+    us = chain_time([lambda g=g, u=u: q.mul_mat_vec_fused(q.Q4_K, u, 14336, 4096, xq=xq, W_gate=g, bias=bu,
+                                                          gate_bias=bg, out=y[:1, :14336], stream=stream)
+                     for g, u in pairs])
+    out["q4_K gate+up 2x14336x4096 swiglu + up/gate biases"] = {
+        "us_per_call": round(us, 3), "weight_gbs": round(2 * ws[0].numel() / us / 1e3, 1)}
     # MoE: 8 experts of 14336x4096, 4 tokens, top-2 drawn without replacement
     E = torch.stack(ws).view(8, -1)
     ids = synthetic.moe_ids(3_000_600, 4, 2, 8)
@@ -345,7 +353,15 @@ def measure_configs(q, torch, stream, device, reps):
         "us_per_call": round(us, 3), "experts_touched": n_touched,
         "weight_gbs": round(n_touched * ws[0].numel() / us / 1e3, 1),
         "note": "the same call repeated; the touched experts (%d x 33 MB) exceed L2" % n_touched}
-    del ws, E
+    # the same routing plus a shared expert (every token), one launch
+    w_sh = weights(q.Q4_K, 14336, 4096, 1, 3_000_800)[0]
+    ysh = torch.empty((4, 14336), dtype=torch.float32, device=device)
+    us = chain_time([lambda: q.mul_mat_vec_id_fused(q.Q4_K, E, 8, 14336, 4096, idd, xq=xq4, W_shared=w_sh, out=ym,
+                                                    out_shared=ysh, stream=stream)] * 4)
+    out["q4_K moe 8x14336x4096 4 tokens top-2 + shared expert 14336x4096"] = {
+        "us_per_call": round(us, 3), "experts_touched": n_touched + 1,
+        "weight_gbs": round((n_touched + 1) * ws[0].numel() / us / 1e3, 1)}
+    del ws, E, w_sh
     torch.cuda.empty_cache()
     return out
 

@@ -174,6 +174,45 @@ int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M,
                            const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k,
                            float *y, int32_t *dev_status, void *stream);
 
+/* ---- fused epilogue extras -----------------------------------------------------
+ * The mul_mat_vec_q page, section "融合:把 gate、bias 和 SwiGLU 塞进同一个 kernel",
+ * lists what its fused launch can carry besides the gate matrix: a bias on
+ * the up (x) output and one on the gate output, added before the GLU, and a
+ * MoE shared expert served as one more slice of the same grid.
+ *
+ * qmv_mul_mat_vec_fused: y = W_up . x (+ bias) when W_gate is NULL, else
+ *   y = (W_up . x + bias) * silu(W_gate . x + gate_bias), per column.
+ *   Exactly one of xq (q8_1 activations, as for qmv_mul_mat_vec) and x
+ *   (fp32 activations, column c at x + c*ldx, as for qmv_mul_mat_vec_f32;
+ *   ldx is ignored for xq) is non-NULL.  bias and gate_bias are NULL or
+ *   fp32 [M] (4-byte aligned), the same for every column; gate_bias needs
+ *   W_gate.  The biases are read like the weights, before the kernel waits
+ *   for the previous kernel on the stream: no kernel may be writing them.
+ *   With both biases NULL the result equals qmv_mul_mat_vec(_f32) or
+ *   qmv_mul_mat_vec_gate_up_swiglu(_f32) bit for bit.  Shapes and alignment
+ *   as for the _f32 calls (the streaming kernel only: Q4_0 / Q4_K with K a
+ *   multiple of 256, Q6_K with K a multiple of 2048, W_up and W_gate 16-byte
+ *   aligned).  Errors: QMV_ERR_NULL (no activations, y NULL), QMV_ERR_SHAPE
+ *   (both activations given, gate_bias without W_gate, shape), QMV_ERR_ALIGN,
+ *   QMV_ERR_NCOLS (ncols outside 1..8), QMV_ERR_TYPE; all before launching.
+ *
+ * qmv_mul_mat_vec_id_fused: qmv_mul_mat_vec_id(_f32) (one of xq / x, as
+ *   above) plus, when W_shared is not NULL, a shared expert applied to every
+ *   token: y_shared[t*M + r] = (W_shared . x_t)[r] for t < n_tokens, with
+ *   W_shared one [M][row bytes] matrix (16-byte aligned) and y_shared fp32
+ *   [n_tokens][M].  W_shared and y_shared are both NULL or both set
+ *   (QMV_ERR_NULL otherwise).  The routed outputs, invalid-id handling and
+ *   dev_status are those of qmv_mul_mat_vec_id; one launch serves the routed
+ *   and the shared experts. */
+int qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K,
+                          const void *xq, const float *x, int64_t ldx, int ncols, const float *bias,
+                          const float *gate_bias, float *y, void *stream);
+
+int qmv_mul_mat_vec_id_fused(int type, const void *W, int64_t n_expert, int64_t M, int64_t K,
+                             const void *xq, const float *x, int64_t ldx, const int32_t *ids,
+                             int n_tokens, int top_k, float *y, const void *W_shared, float *y_shared,
+                             int32_t *dev_status, void *stream);
+
 /* ---- verification --------------------------------------------------------------
  * The exact int32 intermediates of the block formulas, computed by the same
  * device code as qmv_mul_mat_vec (for bit-exact parity tests).  out is

@@ -231,6 +231,31 @@ def swiglu(gate, up):
     return np.asarray(up, dtype=np.float64) * silu(gate)
 
 
+def fused_epilogue(up, gate=None, bias=None, gate_bias=None):
+    """The fused epilogue of the mul_mat_vec_q page, section "融合" (its
+    SwiGLU case), in fp64: result = up + x_bias; with a gate, gate_value =
+    gate + gate_bias and result *= silu(gate_value).  up and gate are
+    [ncols][M]; bias and gate_bias are [M] vectors, the same for every column
+    (the reading this build takes: the page's epilogue adds the bias of the
+    output row, and a layer's bias does not depend on the token)."""
+    r = np.asarray(up, dtype=np.float64)
+    if bias is not None:
+        r = r + np.asarray(bias, dtype=np.float64)[None, :]
+    if gate is None:
+        return r
+    g = np.asarray(gate, dtype=np.float64)
+    if gate_bias is not None:
+        g = g + np.asarray(gate_bias, dtype=np.float64)[None, :]
+    return r * silu(g)
+
+
+def shared_expert_gemv(t: int, W_shared: np.ndarray, M: int, K: int, xq: np.ndarray, n_tokens: int, rows=None):
+    """MoE shared expert (mul_mat_vec_q page, section "融合", the extra grid
+    slice after the routed experts): every token uses the same matrix, so
+    y_shared[t] = W_shared . x[t]; returns (y, l1), each [n_tokens][nrows]."""
+    return gemv_formula(t, W_shared, M, K, xq, n_tokens, rows)
+
+
 def moe_gemv(t: int, W: np.ndarray, n_expert: int, M: int, K: int, xq: np.ndarray, ids: np.ndarray,
              rows=None):
     """Expert-indexed GEMV (mul_mat_vec_q page, "MoE" section): for token t and

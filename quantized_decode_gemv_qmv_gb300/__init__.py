@@ -28,6 +28,7 @@ EXPORTS = (
     "qmv_status_str", "qmv_version", "qmv_row_bytes", "qmv_q8_1_padded_k", "qmv_q8_1_bytes",
     "qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec", "qmv_mul_mat_vec_gate_up_swiglu",
     "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32", "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32",
+    "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
 )
 
@@ -74,6 +75,9 @@ def lib():
         L.qmv_mul_mat_vec_gate_up_swiglu_f32.argtypes = [_int, _vp, _vp, _i64, _i64, _vp, _i64, _int, _vp, _vp]
         L.qmv_mul_mat_vec_id_f32.argtypes = [_int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _int, _vp, _vp,
                                              _vp]
+        L.qmv_mul_mat_vec_fused.argtypes = [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _vp]
+        L.qmv_mul_mat_vec_id_fused.argtypes = [_int, _vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int, _vp,
+                                               _vp, _vp, _vp, _vp]
         L.qmv_debug_subblock_sums.argtypes = [_int, _vp, _i64, _i64, _vp, _int, _vp, _vp]
         L.qmv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.qmv_set_tuning.argtypes = [_int, _int, _int, _int, _int, _int, _int]
@@ -81,7 +85,8 @@ def lib():
         L.qmv_set_pdl.argtypes = [_int]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
-                     "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_debug_subblock_sums",
+                     "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_mul_mat_vec_fused",
+                     "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl"):
             getattr(L, name).restype = _int
         _lib = L
@@ -247,6 +252,59 @@ def mul_mat_vec_id_f32(qtype: int, W, n_expert: int, M: int, K: int, x, ids, out
            lib().qmv_mul_mat_vec_id_f32(qtype, _ptr(W), n_expert, M, K, _ptr(x2), x2.stride(0), _ptr(ids), n_tokens,
                                         top_k, _ptr(out), _ptr(status), _stream_handle(stream)))
     return out
+
+
+def _activations(xq, x):
+    """(xq pointer, x pointer, ldx, ncols) for exactly one of q8_1 rows xq [ncols][bytes] or fp32 x [ncols][K]."""
+    import torch
+
+    if (xq is None) == (x is None):
+        raise ValueError("pass exactly one of xq (q8_1) and x (fp32)")
+    if x is not None:
+        x2 = _x2d(x)
+        return _vp(0), _ptr(x2), x2.stride(0), x2.shape[0]
+    xq2 = xq.unsqueeze(0) if xq.dim() == 1 else xq
+    _need_cuda(xq2, "xq", torch.uint8)
+    return _ptr(xq2), _vp(0), 0, xq2.shape[0]
+
+
+def mul_mat_vec_fused(qtype: int, W_up, M: int, K: int, xq=None, x=None, W_gate=None, bias=None, gate_bias=None,
+                      out=None, stream=None):
+    """y = W_up.x (+ bias), or (W_up.x + bias) * silu(W_gate.x + gate_bias) with W_gate; q8_1 xq or fp32 x."""
+    import torch
+
+    pq, px, ldx, ncols = _activations(xq, x)
+    for name, b in (("bias", bias), ("gate_bias", gate_bias)):
+        if b is not None:
+            _need_cuda(b, name, torch.float32)
+    if out is None:
+        out = torch.empty((ncols, M), dtype=torch.float32, device=W_up.device)
+    _check("qmv_mul_mat_vec_fused",
+           lib().qmv_mul_mat_vec_fused(qtype, _ptr(W_up), _ptr(W_gate), M, K, pq, px, ldx, ncols, _ptr(bias),
+                                       _ptr(gate_bias), _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def mul_mat_vec_id_fused(qtype: int, W, n_expert: int, M: int, K: int, ids, xq=None, x=None, W_shared=None,
+                         out=None, out_shared=None, status=None, stream=None):
+    """Expert-indexed GEMV (q8_1 xq or fp32 x, one row per token) plus an optional shared expert:
+    returns (y [n_tokens][top_k][M], y_shared [n_tokens][M] or None)."""
+    import torch
+
+    pq, px, ldx, n_tok = _activations(xq, x)
+    _need_cuda(ids, "ids", torch.int32)
+    n_tokens, top_k = ids.shape
+    if n_tok < n_tokens:
+        raise ValueError("fewer activation rows than tokens")
+    if out is None:
+        out = torch.empty((n_tokens, top_k, M), dtype=torch.float32, device=W.device)
+    if W_shared is not None and out_shared is None:
+        out_shared = torch.empty((n_tokens, M), dtype=torch.float32, device=W.device)
+    _check("qmv_mul_mat_vec_id_fused",
+           lib().qmv_mul_mat_vec_id_fused(qtype, _ptr(W), n_expert, M, K, pq, px, ldx, _ptr(ids), n_tokens, top_k,
+                                          _ptr(out), _ptr(W_shared), _ptr(out_shared if W_shared is not None else None),
+                                          _ptr(status), _stream_handle(stream)))
+    return out, (out_shared if W_shared is not None else None)
 
 
 def debug_subblock_sums(qtype: int, W, M: int, K: int, xq, ncols: int, stream=None):

@@ -120,13 +120,19 @@ qmv_status device_info(DevInfo &d)
     return QMV_OK;
 }
 
+size_t static_smem(const void *fn);
+
+// Lets fn use as much dynamic shared memory as the opt-in limit leaves beside
+// its static shared memory (at most d.smem_limit).
 qmv_status ensure_smem_attr(const DevInfo &d, const void *fn)
 {
+    const size_t st = static_smem(fn);
     std::lock_guard<std::mutex> lk(g_mu);
     auto key = std::make_pair(d.dev, fn);
     if (g_smem_attr.count(key)) return QMV_OK;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(d.smem_limit)) !=
-        cudaSuccess)
+    const size_t optin = static_cast<size_t>(g_smem_optin[d.dev]);
+    const size_t lim = std::min(d.smem_limit, optin > st ? optin - st : size_t(0));
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(lim)) != cudaSuccess)
         return QMV_ERR_CUDA;
     g_smem_attr[key] = true;
     return QMV_OK;
@@ -254,7 +260,7 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     if (mode == MODE_MOE) {
         // the kernel shares the grid among the experts the ids pick (at most
         // n_potential_experts); at least one CTA per possible expert
-        gx = std::max<int64_t>(max_ctas, static_cast<int64_t>(p.n_tokens) * p.top_k);
+        gx = std::max<int64_t>(max_ctas, static_cast<int64_t>(p.n_tokens) * p.top_k + (p.W2 ? 1 : 0));
         groups_per_cta = (G * n_potential_experts + gx - 1) / gx;
     }
     max_wpc = static_cast<int>(std::min<int64_t>(max_wpc, std::max<int64_t>(1, groups_per_cta)));
@@ -281,7 +287,10 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     };
     int wpc_f = 0, st_f = 0;
     const bool tuned_share = tu.smem_share.load() > 0;
-    size_t budget = share_budget(tuned_share ? tu.smem_share.load() : 2);
+    // The half-SM share only helps if a second CTA fits the SM at all: kernels
+    // whose registers allow one CTA per SM (more than one column) take it whole
+    const bool one_cta = occupancy(dev.dev, fn, cta_warps * 32, 0) < 2;
+    size_t budget = share_budget(tuned_share ? tu.smem_share.load() : (one_cta ? 1 : 2));
     if (!fit(budget, wpc_f, st_f)) {
         budget = fn_limit;
         if (!fit(budget, wpc_f, st_f)) return TilePlan::NoFit;
@@ -629,6 +638,73 @@ int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M,
     p.n_expert = static_cast<int>(n_expert);
     p.expert_bytes = M * p.row_bytes;
     const int potential = static_cast<int>(std::min<int64_t>(n_expert, static_cast<int64_t>(n_tokens) * top_k));
+    Launch L;
+    if ((s = plan_f32(type, MODE_MOE, dev, p, n_tokens, potential, L)) != QMV_OK) return s;
+    return launch(L, static_cast<cudaStream_t>(stream));
+}
+
+int qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K, const void *xq,
+                          const float *x, int64_t ldx, int ncols, const float *bias, const float *gate_bias, float *y,
+                          void *stream)
+{
+    if (!xq && !x) return QMV_ERR_NULL;
+    if (xq && x) return QMV_ERR_SHAPE;
+    qmv_status s = check_common(type, W_up, M, K, xq ? xq : static_cast<const void *>(x), y);
+    if (s != QMV_OK) return s;
+    if (gate_bias && !W_gate) return QMV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(bias) % 4 || reinterpret_cast<uintptr_t>(gate_bias) % 4) return QMV_ERR_ALIGN;
+    if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    if ((s = check_f32(type, W_up, W_gate, K, x ? ldx : K)) != QMV_OK) return s;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W_up, M, K, xq, ncols);
+    if (x) {
+        p.xf = x;
+        p.ldx = ldx;
+    }
+    p.W2 = static_cast<const uint8_t *>(W_gate);
+    p.bias = bias;
+    p.gate_bias = gate_bias;
+    p.y = y;
+    Launch L;
+    if ((s = plan_f32(type, W_gate ? MODE_GATE : MODE_PLAIN, dev, p, ncols, 1, L)) != QMV_OK) return s;
+    return launch(L, static_cast<cudaStream_t>(stream));
+}
+
+int qmv_mul_mat_vec_id_fused(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const void *xq,
+                             const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k, float *y,
+                             const void *W_shared, float *y_shared, int32_t *dev_status, void *stream)
+{
+    if (!xq && !x) return QMV_ERR_NULL;
+    if (xq && x) return QMV_ERR_SHAPE;
+    qmv_status s = check_common(type, W, M, K, xq ? xq : static_cast<const void *>(x), y);
+    if (s != QMV_OK) return s;
+    if (!ids) return QMV_ERR_NULL;
+    if (!W_shared != !y_shared) return QMV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(ids) % 4 || reinterpret_cast<uintptr_t>(dev_status) % 4 ||
+        reinterpret_cast<uintptr_t>(y_shared) % 4)
+        return QMV_ERR_ALIGN;
+    if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
+    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
+    if ((s = check_f32(type, W, W_shared, K, x ? ldx : K)) != QMV_OK) return s;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W, M, K, xq, n_tokens);
+    if (x) {
+        p.xf = x;
+        p.ldx = ldx;
+    }
+    p.W2 = static_cast<const uint8_t *>(W_shared);
+    p.y_shared = y_shared;
+    p.y = y;
+    p.ids = ids;
+    p.status = dev_status;
+    p.n_tokens = n_tokens;
+    p.top_k = top_k;
+    p.n_expert = static_cast<int>(n_expert);
+    p.expert_bytes = M * p.row_bytes;
+    const int potential = static_cast<int>(std::min<int64_t>(n_expert, static_cast<int64_t>(n_tokens) * top_k)) +
+                          (W_shared ? 1 : 0);
     Launch L;
     if ((s = plan_f32(type, MODE_MOE, dev, p, n_tokens, potential, L)) != QMV_OK) return s;
     return launch(L, static_cast<cudaStream_t>(stream));

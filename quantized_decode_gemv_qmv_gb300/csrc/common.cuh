@@ -238,6 +238,15 @@ __device__ __forceinline__ float ld_cg_f32(const float *p)
     return v;
 }
 
+// Read-only (non-coherent) load of a value that no kernel writes while this
+// one runs (weights, biases).
+__device__ __forceinline__ float ld_nc_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ int ld_cg_s32(const int32_t *p)
 {
     int v;

@@ -9,7 +9,7 @@ enum Mode { MODE_PLAIN = 0, MODE_GATE = 1, MODE_MOE = 2, MODE_DEBUG = 3 };
 
 struct GemvParams {
     const uint8_t *W;    // weights (MoE: expert 0); GATE: the up matrix
-    const uint8_t *W2;   // GATE: the gate matrix
+    const uint8_t *W2;   // GATE: the gate matrix; MOE: the shared expert (nullable)
     const uint8_t *xq;   // q8_1 activations, column c at xq + c*xq_col_bytes
     const float *xf;     // fp32 activations quantized in place (tile kernel), column c at xf + c*ldx; or null
     int64_t ldx;
@@ -17,6 +17,9 @@ struct GemvParams {
     int32_t *dbg;        // DEBUG: per-sub-block int sums
     const int32_t *ids;  // MOE: [n_tokens][top_k]
     int32_t *status;     // MOE: number of invalid ids (nullable)
+    const float *bias;       // PLAIN/GATE: [M] added to every column's (up) output (nullable)
+    const float *gate_bias;  // GATE: [M] added to the gate output before silu (nullable)
+    float *y_shared;         // MOE with a shared expert (W2): y_shared[t*M + r] = (W2 x_t)[r]
     int64_t M;
     int64_t ldy;
     int64_t row_bytes;

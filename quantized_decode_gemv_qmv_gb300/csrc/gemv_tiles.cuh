@@ -38,6 +38,7 @@ constexpr int TILE_MAX_THREADS = 384;
 constexpr int TILE_MAX_STAGES = 4;
 constexpr int STAGE_BATCH = 4;  // q8_1 staging: 16-byte loads in flight per thread
 constexpr int MOE_MAX_SLOTS = 256;  // n_tokens * top_k <= 8 * 32
+constexpr int MOE_COL_WEIGHT = 6;   // MoE grid split: an expert's work ~ 6 + the tokens (columns) it serves
 
 // Tile geometry for format F and RW rows per tile: UW = 32/RW units per tile
 // row (one per lane), the row segment SEG 16-byte pieces long, PER_LANE copy
@@ -259,38 +260,88 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     }
 
     int n_active = p.ncols;
-    int64_t row_base = 0;  // MoE: first row of this CTA's expert
+    int64_t row_base = 0;    // MoE: first row of this CTA's expert
+    const uint8_t *W0 = p.W;  // first matrix (MoE: the experts, or the shared expert)
+    bool moe_shared = false;  // MoE: this CTA serves the shared expert
     int64_t cta_index = blockIdx.x, cta_count = gridDim.x;
     if constexpr (MODE == MODE_MOE) {
         // Routing is known only here (ids come from the previous grid).  The
-        // experts some token picks are listed in ascending order and the grid
-        // is shared among them -- CTA b serves expert floor(b*T/grid) -- so
-        // every SM works whatever the routing.  CTA 0 also zero-fills the
-        // outputs of invalid ids and counts them.
-        __shared__ int s_exp[MOE_MAX_SLOTS];
-        __shared__ int s_ne;
+        // ids are read once into shared memory; the experts some token picks
+        // are listed in ascending order (then the shared expert, if any) and
+        // the grid is shared among them in proportion to their work, one CTA
+        // each plus a share of the rest weighted by MOE_COL_WEIGHT + the
+        // number of tokens they serve, so every SM works whatever the routing.
+        // CTA 0 also zero-fills the outputs of invalid ids and counts them.
+        __shared__ int s_ids[MOE_MAX_SLOTS];
+        __shared__ int s_exp[MOE_MAX_SLOTS + 1];   // the picked experts ascending, then the shared one
+        __shared__ int s_ntok[MOE_MAX_SLOTS + 1];  // tokens each listed expert serves
+        __shared__ int s_eidx;
+        __shared__ int64_t s_first, s_next;
         pdl_wait();
         const int n_slots = p.n_tokens * p.top_k;
-        if (threadIdx.x == 0) {
-            int ne = 0;
-            for (int s = 0; s < n_slots; ++s) {
-                const int e = ld_cg_s32(p.ids + s);
-                if (e < 0 || e >= p.n_expert) continue;
-                int j = ne;
-                while (j > 0 && s_exp[j - 1] > e) --j;
-                if (j > 0 && s_exp[j - 1] == e) continue;
-                for (int k = ne; k > j; --k) s_exp[k] = s_exp[k - 1];
-                s_exp[j] = e;
-                ++ne;
-            }
-            s_ne = ne;
+        for (int s = threadIdx.x; s < n_slots; s += blockDim.x) s_ids[s] = ld_cg_s32(p.ids + s);
+        __syncthreads();
+        // slot s represents its id if the id is valid and no earlier slot holds it;
+        // a representative's place in the list is the number of smaller represented ids
+        __shared__ unsigned char s_isrep[MOE_MAX_SLOTS];
+        __shared__ int s_nrouted;
+        if (threadIdx.x == 0) s_nrouted = 0;
+        for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
+            const int e = s_ids[s];
+            bool rep = e >= 0 && e < p.n_expert;
+            for (int j = 0; j < s && rep; ++j) rep = s_ids[j] != e;
+            s_isrep[s] = rep ? 1 : 0;
         }
         __syncthreads();
-        const int ne = s_ne;
+        for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
+            if (!s_isrep[s]) continue;
+            const int e = s_ids[s];
+            int rank = 0;
+            for (int j = 0; j < n_slots; ++j) rank += (s_isrep[j] && s_ids[j] < e) ? 1 : 0;
+            s_exp[rank] = e;
+            atomicAdd(&s_nrouted, 1);
+        }
+        __syncthreads();
+        const int n_routed = s_nrouted;
+        const int ne = n_routed + (p.W2 != nullptr ? 1 : 0);
+        if (p.W2 != nullptr && threadIdx.x == 0) s_exp[n_routed] = p.n_expert;  // every token, its own output
+        __syncthreads();
+        for (int i = threadIdx.x; i < ne; i += blockDim.x) {
+            const int e = s_exp[i];
+            int n = 0;
+            for (int t = 0; t < p.n_tokens; ++t) {
+                bool hit = e == p.n_expert;
+                for (int k = 0; k < p.top_k && !hit; ++k) hit = s_ids[t * p.top_k + k] == e;
+                n += hit ? 1 : 0;
+            }
+            s_ntok[i] = n;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int64_t wsum = 0;
+            for (int i = 0; i < ne; ++i) wsum += MOE_COL_WEIGHT + s_ntok[i];
+            const int64_t G = gridDim.x, spare = G - ne;  // the planner gives every listable expert a CTA
+            int64_t pre = 0, start = 0;
+            s_eidx = ne - 1;
+            s_first = 0;
+            s_next = G;
+            for (int i = 0; i < ne; ++i) {
+                pre += MOE_COL_WEIGHT + s_ntok[i];
+                const int64_t end = (i + 1) + pre * spare / wsum;
+                if (static_cast<int64_t>(blockIdx.x) < end) {
+                    s_eidx = i;
+                    s_first = start;
+                    s_next = end;
+                    break;
+                }
+                start = end;
+            }
+        }
+        __syncthreads();
         if (blockIdx.x == 0) {
             int bad = 0;
             for (int s = 0; s < n_slots; ++s) {
-                const int e = ld_cg_s32(p.ids + s);
+                const int e = s_ids[s];
                 if (e < 0 || e >= p.n_expert) {
                     ++bad;
                     float *ys = p.y + (size_t)s * p.M;
@@ -300,26 +351,28 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
             if (threadIdx.x == 0 && p.status) *p.status = bad;
         }
         if (ne == 0) return;
-        const int G = static_cast<int>(gridDim.x);
-        const int e_idx = static_cast<int>(static_cast<int64_t>(blockIdx.x) * ne / G);
-        const int64_t first = (static_cast<int64_t>(e_idx) * G + ne - 1) / ne;
-        const int64_t next = (static_cast<int64_t>(e_idx + 1) * G + ne - 1) / ne;
-        const int expert = s_exp[e_idx];
-        cta_index = blockIdx.x - first;
-        cta_count = next - first;
+        const int expert = s_exp[s_eidx];
+        moe_shared = expert == p.n_expert;
+        cta_index = blockIdx.x - s_first;
+        cta_count = s_next - s_first;
         if (threadIdx.x == 0) {
             int cnt = 0;
             for (int t = 0; t < p.n_tokens; ++t) {
                 uint32_t mask = 0;
-                for (int k = 0; k < p.top_k; ++k)
-                    if (ld_cg_s32(p.ids + t * p.top_k + k) == expert) mask |= 1u << k;
+                if (moe_shared) {
+                    mask = 1u;
+                } else {
+                    for (int k = 0; k < p.top_k; ++k)
+                        if (s_ids[t * p.top_k + k] == expert) mask |= 1u << k;
+                }
                 if (mask) { s_tok[cnt] = t; s_slots[cnt] = mask; ++cnt; }
             }
             s_cnt = cnt;
         }
         __syncthreads();
         n_active = s_cnt;
-        row_base = static_cast<int64_t>(expert) * p.M;
+        if (moe_shared) W0 = p.W2;
+        else row_base = static_cast<int64_t>(expert) * p.M;
     }
 
     // every warp (of the grid; MoE: of the expert's CTAs) owns a contiguous,
@@ -338,7 +391,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     int ld_kt = 0, ld_m = 0, ld_buf = 0;
     int64_t issued = 0;
     auto issue_tile = [&]() {
-        const uint8_t *W = (NM == 2 && ld_m) ? p.W2 : p.W;
+        const uint8_t *W = (NM == 2 && ld_m) ? p.W2 : W0;
         const int64_t grow = ld_g * RW;  // first row of the group inside the matrix
         const uint8_t *base = W + (row_base + grow) * rb + static_cast<int64_t>(ld_kt) * (UW * UNIT);
         const int64_t rows_left = p.M - grow;
@@ -386,6 +439,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[m][c] = 0.f;
 
+    float b_up = 0.f, b_gate = 0.f;  // this lane's row biases (lanes of unit 0)
     int64_t cg = g_begin;  // compute position
     int ckt = 0, cm = 0, cbuf = 0;
     for (int64_t t = 0; t < total; ++t) {
@@ -394,6 +448,14 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 
         const int64_t row = cg * RW + r_l;
         const int u = ckt * UW + u_l;
+        if constexpr (MODE == MODE_PLAIN || MODE == MODE_GATE) {
+            // the row's biases (read like the weights: not written by the previous kernel),
+            // requested at the group's first tile so that its decode hides the latency
+            if (ckt == 0 && cm == 0 && u_l == 0 && row < p.M) {
+                if (p.bias) b_up = ld_nc_f32(p.bias + row);
+                if (MODE == MODE_GATE && p.gate_bias) b_gate = ld_nc_f32(p.gate_bias + row);
+            }
+        }
         if (u < U && row < p.M) {
             uint32_t ub[1] = {ring + static_cast<uint32_t>(cbuf * TB) + r_l * SS + u_l * UNIT};
             const bool live[1] = {true};
@@ -433,11 +495,17 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
                     for (int c = 0; c < NC; ++c) {
                         if (c >= n_active) break;
                         if constexpr (MODE == MODE_PLAIN) {
-                            p.y[(size_t)c * p.ldy + row] = acc[0][c];
+                            p.y[(size_t)c * p.ldy + row] = p.bias ? acc[0][c] + b_up : acc[0][c];
                         } else if constexpr (MODE == MODE_GATE) {
-                            p.y[(size_t)c * p.ldy + row] = acc[0][c] * silu_f32(acc[NM - 1][c]);
+                            const float up = p.bias ? acc[0][c] + b_up : acc[0][c];
+                            const float gate = p.gate_bias ? acc[NM - 1][c] + b_gate : acc[NM - 1][c];
+                            p.y[(size_t)c * p.ldy + row] = up * silu_f32(gate);
                         } else {
                             const int tok = s_tok[c];
+                            if (moe_shared) {
+                                p.y_shared[(size_t)tok * p.M + row] = acc[0][c];
+                                continue;
+                            }
                             uint32_t mask = s_slots[c];
                             while (mask) {
                                 const int k = __ffs(mask) - 1;

@@ -97,6 +97,26 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_mul_mat_vec_gate_up_swiglu_f32(12, ctypes.c_void_p(0x1008), p, 16, 4096, p, 4096, 1, p, nul) == 5
     assert L.qmv_mul_mat_vec_id_f32(12, p, 8, 16, 4096, p, 4096, nul, 4, 2, p, nul, nul) == 1
     assert L.qmv_mul_mat_vec_id_f32(14, p, 8, 16, 2304, p, 2304, p, 4, 2, p, nul, nul) == 3
+    # fused epilogue extras: one activation kind, gate bias needs a gate, tile shapes, aligned biases
+    fm = L.qmv_mul_mat_vec_fused
+    assert fm(12, p, nul, 16, 4096, nul, nul, 0, 1, nul, nul, p, nul) == 1
+    assert fm(12, p, nul, 16, 4096, p, p, 4096, 1, nul, nul, p, nul) == 3
+    assert fm(12, p, nul, 16, 4096, p, nul, 0, 1, nul, p, p, nul) == 3
+    assert fm(12, p, p, 16, 4096, p, nul, 0, 1, ctypes.c_void_p(0x1002), nul, p, nul) == 5
+    assert fm(14, p, nul, 16, 2304, p, nul, 0, 1, nul, nul, p, nul) == 3
+    assert fm(12, p, nul, 16, 4096, nul, p, 4000, 1, nul, nul, p, nul) == 3
+    assert fm(12, p, nul, 16, 4096, p, nul, 0, 0, nul, nul, p, nul) == 4
+    assert fm(12, p, ctypes.c_void_p(0x1008), 16, 4096, p, nul, 0, 1, nul, nul, p, nul) == 5
+    assert fm(9, p, nul, 16, 4096, p, nul, 0, 1, nul, nul, p, nul) == 2
+    im = L.qmv_mul_mat_vec_id_fused
+    assert im(12, p, 8, 16, 4096, nul, nul, 0, p, 4, 2, p, nul, nul, nul, nul) == 1
+    assert im(12, p, 8, 16, 4096, p, p, 4096, p, 4, 2, p, nul, nul, nul, nul) == 3
+    assert im(12, p, 8, 16, 4096, p, nul, 0, p, 4, 2, p, p, nul, nul, nul) == 1
+    assert im(12, p, 8, 16, 4096, p, nul, 0, p, 4, 2, p, nul, p, nul, nul) == 1
+    assert im(12, p, 8, 16, 4096, p, nul, 0, p, 4, 2, p, ctypes.c_void_p(0x1008), p, nul, nul) == 5
+    assert im(12, p, 8, 16, 4096, p, nul, 0, p, 9, 2, p, p, p, nul, nul) == 4
+    assert im(12, p, 8, 16, 4096, p, nul, 0, nul, 4, 2, p, p, p, nul, nul) == 1
+    assert im(14, p, 8, 16, 2304, p, nul, 0, p, 4, 2, p, p, p, nul, nul) == 3
     # tuning knobs validate too
     assert L.qmv_set_tuning(12, 100, 0, 0, 0, 0, 0) == 3
     assert L.qmv_set_tuning(12, 544, 0, 0, 0, 0, 0) == 3

@@ -183,3 +183,42 @@ def test_moe_routes_each_slot_to_its_expert():
                 ye, _ = oracle.gemv_formula(oracle.Q4_K, W[e], M, K, xt, 1)
                 assert np.array_equal(y[tok, s], ye[0])
     assert np.array_equal(y[1, 0], y[1, 1])
+
+
+def test_fused_epilogue_closed_forms():
+    up = np.array([[1.0, 2.0, -3.0], [0.25, -1.0, 4.0]])
+    gate = np.array([[0.0, 50.0, -2.0], [3.0, -60.0, 1.0]])
+    b = np.array([0.5, -2.0, 3.0])
+    gb = np.array([-0.0, 1.0, 2.0])
+    # no extras: identity; bias only: a plain row-wise add, the same for every column
+    assert np.array_equal(oracle.fused_epilogue(up), up)
+    assert np.array_equal(oracle.fused_epilogue(up, bias=b), [[1.5, 0.0, 0.0], [0.75, -3.0, 7.0]])
+    # no biases: exactly the SwiGLU epilogue
+    assert np.array_equal(oracle.fused_epilogue(up, gate), oracle.swiglu(gate, up))
+    # the gate bias moves the gate argument: gate + gate_bias = 0 gives silu(0) = 0
+    z = oracle.fused_epilogue(up, np.array([[-1.0, -1.0, -1.0]]), b, np.array([1.0, 1.0, 1.0]))
+    assert z.shape == (2, 3) and not z.any()
+    # a large gate passes (up + bias) through, scaled by the gate argument itself
+    r = oracle.fused_epilogue(up[:1, 1:2], gate[:1, 1:2], b[1:2], gb[1:2])
+    assert np.isclose(r[0, 0], (2.0 - 2.0) * 51.0, atol=1e-12)
+    r = oracle.fused_epilogue(np.array([[3.0]]), np.array([[40.0]]), np.array([1.0]), np.array([2.0]))
+    assert np.isclose(r[0, 0], 4.0 * 42.0 * (1.0 / (1.0 + np.exp(-42.0))), rtol=1e-15)
+    # a dropped gate bias or up bias is detected
+    full = oracle.fused_epilogue(up, gate, b, gb)
+    assert not np.allclose(full, oracle.fused_epilogue(up, gate, b, None))
+    assert not np.allclose(full, oracle.fused_epilogue(up, gate, None, gb))
+    assert np.allclose(full, (up + b) * ((gate + gb) / (1.0 + np.exp(-(gate + gb)))))
+
+
+def test_shared_expert_is_every_token_routed_to_one_matrix():
+    M, K, T = 11, 512, 3
+    Ws = oracle.random_blocks(oracle.Q4_K, M, K, seed=91)
+    xq = _xq(92, T, K)
+    ys, l1 = oracle.shared_expert_gemv(oracle.Q4_K, Ws, M, K, xq, T)
+    # the same as routing every token to expert 0 of a one-expert set
+    ym, lm, bad = oracle.moe_gemv(oracle.Q4_K, Ws, 1, M, K, xq, np.zeros((T, 1), dtype=np.int32))
+    assert bad == 0 and np.array_equal(ys, ym[:, 0, :]) and np.array_equal(l1, lm[:, 0, :])
+    # and, for a K-quant, the fp64 dequantize-then-dot of each token's column
+    Wd = oracle.dequantize_rows(oracle.Q4_K, Ws, K).astype(np.float64)
+    xd = oracle.dequantize_q8_1(xq, K).astype(np.float64)
+    assert np.allclose(ys, xd @ Wd.T, rtol=1e-12, atol=1e-12 * np.abs(l1).max())
