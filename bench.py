@@ -53,7 +53,7 @@ SHAPES = {"4096x4096": (D_MODEL, D_MODEL), "11008x4096": (D_FF, D_MODEL), "4096x
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "dbd12f8e1c2a9fac", "bytes_per_launch": 28543680,
+TRAFFIC = {"csrc_sha": "5e9b442346730afa", "bytes_per_launch": 28528384,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down (profiles/gemv_tiles_q4_K_down_fused.md)"}
 
 
@@ -604,22 +604,24 @@ def run_kernel_only(args):
 
     torch.cuda.set_device(0)
     kinds = {name: (M, K, nmat) for name, M, K, nmat in STEP}
-    if args.kernel_only in SHAPES:
-        M, K = SHAPES[args.kernel_only]
+    shapes = dict(SHAPES, **{"14336x4096": (14336, 4096)})
+    nc = args.ncols
+    if args.kernel_only in shapes:
+        M, K = shapes[args.kernel_only]
         nmat = 1
     elif args.kernel_only in kinds:
         M, K, nmat = kinds[args.kernel_only]
     else:
-        raise SystemExit(f"unknown shape {args.kernel_only}; choose from {list(SHAPES) + list(kinds)}")
+        raise SystemExit(f"unknown shape {args.kernel_only}; choose from {list(shapes) + list(kinds)}")
     Ws = [[q.quantize_weights(Q4_K, synthetic.device_normal_f32(7 + 2 * i + m, (M, K), 0.02, "cuda"))
            for m in range(nmat)] for i in range(4)]
-    x = torch.from_numpy(synthetic.activations_f32(9, 1, K, outlier_frac=0.01)).cuda()
+    x = torch.from_numpy(synthetic.activations_f32(9, nc, K, outlier_frac=0.01)).cuda()
     xq = q.quantize_q8_1(x)
-    y = torch.empty((1, M), dtype=torch.float32, device="cuda")
+    y = torch.empty((nc, M), dtype=torch.float32, device="cuda")
     for i in range(args.launches):
         W = Ws[i % len(Ws)]
-        if args.kernel_only in SHAPES:
-            q.mul_mat_vec(Q4_K, W[0], M, K, xq, 1, out=y)
+        if args.kernel_only in shapes:
+            q.mul_mat_vec(Q4_K, W[0], M, K, xq, nc, out=y)
         elif nmat == 2:
             q.mul_mat_vec_gate_up_swiglu_f32(Q4_K, W[0], W[1], M, K, x, out=y)
         else:
@@ -641,6 +643,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timing section")
     ap.add_argument("--kernel-only", default=None, help="profiling aid: only GEMV launches of one shape or step kind")
     ap.add_argument("--launches", type=int, default=8)
+    ap.add_argument("--ncols", type=int, default=1, help="profiling aid: activation columns of a --kernel-only shape")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
