@@ -186,9 +186,10 @@ int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M,
  *   (fp32 activations, column c at x + c*ldx, as for qmv_mul_mat_vec_f32;
  *   ldx is ignored for xq) is non-NULL.  bias and gate_bias are NULL or
  *   fp32 [M] (4-byte aligned), the same for every column; gate_bias needs
- *   W_gate.  The biases are read like the weights, before the kernel waits
- *   for the previous kernel on the stream: no kernel may be writing them.
- *   With both biases NULL the result equals qmv_mul_mat_vec(_f32) or
+ *   W_gate.  The biases are read after the kernel has waited for the
+ *   previous kernel on the stream (so earlier work on the stream may write
+ *   them), through the read-only path: nothing may write them while the call
+ *   runs.  With both biases NULL the result equals qmv_mul_mat_vec(_f32) or
  *   qmv_mul_mat_vec_gate_up_swiglu(_f32) bit for bit.  Shapes and alignment
  *   as for the _f32 calls (the streaming kernel only: Q4_0 / Q4_K with K a
  *   multiple of 256, Q6_K with K a multiple of 2048, W_up and W_gate 16-byte
