@@ -33,6 +33,7 @@ def q():
     qq.set_pdl(True)
     for t in qq.WEIGHT_TYPES:
         qq.set_tuning(t)
+        qq.set_stream_tuning(t)
     return qq
 
 
@@ -135,3 +136,51 @@ def test_fullsize_moe(q):
     y_ref, l1, bad = oracle.moe_gemv(t, W, E, M, K, xq_ref, ids, rows=rows)
     assert bad == 0
     assert np.all(np.abs(y[:, :, rows] - y_ref) <= TOL * l1)
+
+
+def test_fullsize_fused_gate_up_biases(q):
+    # the bench's "gate+up 2x14336x4096 swiglu + up/gate biases" call (q8_1 input)
+    t, M, K = oracle.Q4_K, 14336, 4096
+    Wg, Wgd = quantized(q, t, M, K, seed=5251)
+    Wu, Wud = quantized(q, t, M, K, seed=5252)
+    xq_ref = oracle.quantize_q8_1(synthetic.activations_f32(55, 1, K))
+    b = synthetic.activations_f32(56, 1, M)[0]
+    gb = synthetic.activations_f32(57, 1, M)[0]
+    y = host(q.mul_mat_vec_fused(t, Wud, M, K, xq=dev(xq_ref), W_gate=Wgd, bias=dev(b), gate_bias=dev(gb)))
+    rows = sample_rows(M, 58)
+    g, l1g = oracle.gemv_formula(t, Wg, M, K, xq_ref, 1, rows=rows)
+    u, l1u = oracle.gemv_formula(t, Wu, M, K, xq_ref, 1, rows=rows)
+    ref = oracle.fused_epilogue(u, g, b[rows], gb[rows])
+    gs, us = g + gb[rows][None, :], u + b[rows][None, :]
+    sig = 1.0 / (1.0 + np.exp(-gs))
+    eg = TOL * l1g + 2 ** -22 * np.abs(gs)
+    eu = TOL * l1u + 2 ** -22 * np.abs(us)
+    tol = np.abs(us) * np.abs(sig * (1 + gs * (1 - sig))) * eg + np.abs(gs * sig) * eu + 1e-6 * np.abs(ref)
+    assert np.all(np.abs(y[:, rows] - ref) <= tol)
+
+
+def test_fullsize_moe_shared_expert(q):
+    # the bench's MoE call plus a shared 14336x4096 expert, one launch
+    import torch
+
+    t, E, M, K, T, k = oracle.Q4_K, 8, 14336, 4096, 4, 2
+    rb = oracle.row_bytes(t, K)
+    W = np.empty((E, M * rb), dtype=np.uint8)
+    Wd = torch.empty((E, M * rb), dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        We, Wed = quantized(q, t, M, K, seed=6100 + e)
+        W[e] = We.reshape(-1)
+        Wd[e] = Wed.reshape(-1)
+    Ws, Wsd = quantized(q, t, M, K, seed=6199)
+    ids = synthetic.moe_ids(64, T, k, E)
+    xq_ref = oracle.quantize_q8_1(synthetic.activations_f32(65, T, K))
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    y, ys = q.mul_mat_vec_id_fused(t, Wd, E, M, K, dev(ids), xq=dev(xq_ref), W_shared=Wsd, status=status)
+    y, ys = host(y), host(ys)
+    assert int(host(status)[0]) == 0
+    rows = sample_rows(M, 66)
+    y_ref, l1, bad = oracle.moe_gemv(t, W, E, M, K, xq_ref, ids, rows=rows)
+    assert bad == 0
+    assert np.all(np.abs(y[:, :, rows] - y_ref) <= TOL * l1)
+    ys_ref, l1s = oracle.shared_expert_gemv(t, Ws, M, K, xq_ref, T, rows=rows)
+    assert np.all(np.abs(ys[:, rows] - ys_ref) <= TOL * l1s)
