@@ -264,6 +264,43 @@ def run_reference(args):
 
 
 # ---- GPU arm ------------------------------------------------------------------------
+def measure_ceilings(torch, stream, device, reps=10):
+    """Diagnostic bandwidth ceilings of this GPU, measured here with CUDA events:
+    a device-to-device copy of 2 GB (cudaMemcpyAsync through torch's copy_,
+    counted as read + write bytes) and a read-only reduction over 4 GB (torch
+    sum).  The roofline denominator stays the measured copy figure."""
+    n = 2 << 30
+    src = torch.empty(n, dtype=torch.uint8, device=device)
+    dst = torch.empty(n, dtype=torch.uint8, device=device)
+    big = torch.ones((4 << 30) // 4, dtype=torch.float32, device=device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    out = {}
+    with torch.cuda.stream(stream):
+        src.fill_(1)
+        for _ in range(2):
+            dst.copy_(src)
+        e0.record(stream)
+        for _ in range(reps):
+            dst.copy_(src)
+        e1.record(stream)
+        stream.synchronize()
+        out["d2d_copy_gbs"] = round(2 * n * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        for _ in range(2):
+            big.sum()
+        e0.record(stream)
+        for _ in range(reps):
+            big.sum()
+        e1.record(stream)
+        stream.synchronize()
+        out["read_reduce_gbs"] = round(big.numel() * 4 * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    out["note"] = ("2 GB device copy counted read+write; 4 GB float32 sum (read-only); diagnostics, "
+                   "timed with CUDA events, not this library's kernels")
+    del src, dst, big
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_configs(q, torch, stream, device, reps):
     """Per-call time of the GEMV at each workload the benchmark is quoted on,
     each launch chained over distinct weight copies (so consecutive calls do not
@@ -555,6 +592,7 @@ def run_gpu(args):
     if q.device_fault() != 0:
         raise RuntimeError("device fault word set during the benchmark")
 
+    ceilings = None if args.no_configs else measure_ceilings(torch, stream, device)
     if rank != 0:
         return 0
     cpu = None
@@ -579,6 +617,7 @@ def run_gpu(args):
         "per_shape": per_shape,
         "configs": configs,
         "hbm_frac_of_measured": round(value / peak, 4),
+        "ceilings": ceilings,
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": launches_per_step * args.steps,
