@@ -150,3 +150,31 @@ def test_q4_K_every_scale_min_pair_roundtrips_through_pack_and_decode():
         got = oracle.dequantize_rows(oracle.Q4_K, blk, 256)[0].reshape(8, 32)
         exp = (1.0 * sc - 0.5 * m)[:, None]
         assert np.array_equal(got, np.broadcast_to(exp, (8, 32)))
+
+
+def test_q6_K_codes_follow_the_printed_vec_dot_assembly():
+    # The mul_mat_vec_q page (section "一次 vec_dot 的解剖", the Q6_K lines) builds
+    # a code from a word of ql and a word of qh at the same byte positions:
+    #   vil = (vl >> 4i) & 0x0F0F0F0F, vih = ((vh >> 4i) << 4) & 0x30303030,
+    # code - 32 = (vil | vih) - 32 per byte; i = 0 takes the low nibbles with qh
+    # bits 0-1, i = 1 the high nibbles with qh bits 4-5.  With d = 1 and every
+    # scale 1 the oracle's dequantized values are exactly the codes - 32, so
+    # the byte pairing of reading R3 is checked against the printed arithmetic
+    # (the second ql run of each half uses qh bits 2-3 and 6-7, vh >> 2).
+    rng = np.random.default_rng(611)
+    blk = rng.integers(0, 256, size=210, dtype=np.uint8)
+    blk[192:208] = 1                                   # int8 scales
+    blk[208:210] = np.frombuffer(np.float16(1.0).tobytes(), dtype=np.uint8)
+    vals = oracle.dequantize_rows(oracle.Q6_K, blk, 256)[0]
+    ql, qh = blk[:128], blk[128:192]
+    words = lambda a: a.view("<u4")
+    for h in range(2):
+        for run in range(2):                           # ql[64h + 32 run + l], l < 32
+            vl = words(ql[64 * h + 32 * run: 64 * h + 32 * run + 32].copy())
+            vh = words(qh[32 * h: 32 * h + 32].copy()) >> np.uint32(2 * run)
+            for i in range(2):
+                vil = (vl >> np.uint32(4 * i)) & np.uint32(0x0F0F0F0F)
+                vih = ((vh >> np.uint32(4 * i)) << np.uint32(4)) & np.uint32(0x30303030)
+                codes = (vil | vih).view(np.uint8).astype(np.int32) - 32
+                g = run + 2 * i                        # the 32-element group these bytes fill
+                assert np.array_equal(vals[128 * h + 32 * g: 128 * h + 32 * g + 32], codes), (h, run, i)
