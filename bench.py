@@ -398,7 +398,16 @@ def measure_configs(q, torch, stream, device, reps):
     out["q4_K moe 8x14336x4096 4 tokens top-2 + shared expert 14336x4096"] = {
         "us_per_call": round(us, 3), "experts_touched": n_touched + 1,
         "weight_gbs": round((n_touched + 1) * ws[0].numel() / us / 1e3, 1)}
-    del ws, E, w_sh
+    # the gated form: experts' gate matrices beside the up ones, the shared expert gated too
+    Eg = torch.stack(weights(q.Q4_K, 14336, 4096, 8, 3_000_900)).view(8, -1)
+    w_shg = weights(q.Q4_K, 14336, 4096, 1, 3_000_950)[0]
+    us = chain_time([lambda: q.mul_mat_vec_id_fused(q.Q4_K, E, 8, 14336, 4096, idd, xq=xq4, W_gate=Eg,
+                                                    W_shared=w_sh, W_shared_gate=w_shg, out=ym, out_shared=ysh,
+                                                    stream=stream)] * 4)
+    out["q4_K moe gate/up 8x2x14336x4096 4 tokens top-2 + shared gate/up expert"] = {
+        "us_per_call": round(us, 3), "experts_touched": n_touched + 1,
+        "weight_gbs": round(2 * (n_touched + 1) * ws[0].numel() / us / 1e3, 1)}
+    del ws, E, w_sh, Eg, w_shg
     torch.cuda.empty_cache()
     return out
 

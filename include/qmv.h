@@ -198,20 +198,30 @@ int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M,
  *   QMV_ERR_NCOLS (ncols outside 1..8), QMV_ERR_TYPE; all before launching.
  *
  * qmv_mul_mat_vec_id_fused: qmv_mul_mat_vec_id(_f32) (one of xq / x, as
- *   above) plus, when W_shared is not NULL, a shared expert applied to every
- *   token: y_shared[t*M + r] = (W_shared . x_t)[r] for t < n_tokens, with
- *   W_shared one [M][row bytes] matrix (16-byte aligned) and y_shared fp32
- *   [n_tokens][M].  W_shared and y_shared are both NULL or both set
- *   (QMV_ERR_NULL otherwise).  The routed outputs, invalid-id handling and
- *   dev_status are those of qmv_mul_mat_vec_id; one launch serves the routed
- *   and the shared experts. */
+ *   above) with the MoE fusions of the same section:
+ *   - W_gate (nullable): the experts' gate matrices, laid out like W_up
+ *     ([n_expert][M][row bytes], 16-byte aligned).  With it, every routed
+ *     slot gets y[t][k] = (W_up[e] . x_t) * silu(W_gate[e] . x_t),
+ *     e = ids[t][k], in one pass over both matrices of each picked expert.
+ *   - W_shared_up (nullable): a shared expert applied to every token,
+ *     y_shared[t*M + r] = (W_shared_up . x_t)[r], or with a gate
+ *     (W_shared_gate) (W_shared_up . x_t) * silu(W_shared_gate . x_t), for
+ *     t < n_tokens; each one [M][row bytes] matrix (16-byte aligned) and
+ *     y_shared fp32 [n_tokens][M].
+ *   W_shared_up and y_shared are both NULL or both set, and a gated launch
+ *   (W_gate set) with a shared expert needs W_shared_gate, a plain one must
+ *   not pass it (QMV_ERR_NULL / QMV_ERR_SHAPE otherwise).  The routed
+ *   outputs, invalid-id handling and dev_status are those of
+ *   qmv_mul_mat_vec_id; one launch serves the routed and the shared
+ *   experts. */
 int qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K,
                           const void *xq, const float *x, int64_t ldx, int ncols, const float *bias,
                           const float *gate_bias, float *y, void *stream);
 
-int qmv_mul_mat_vec_id_fused(int type, const void *W, int64_t n_expert, int64_t M, int64_t K,
-                             const void *xq, const float *x, int64_t ldx, const int32_t *ids,
-                             int n_tokens, int top_k, float *y, const void *W_shared, float *y_shared,
+int qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int64_t n_expert,
+                             int64_t M, int64_t K, const void *xq, const float *x, int64_t ldx,
+                             const int32_t *ids, int n_tokens, int top_k, float *y,
+                             const void *W_shared_up, const void *W_shared_gate, float *y_shared,
                              int32_t *dev_status, void *stream);
 
 /* ---- verification --------------------------------------------------------------

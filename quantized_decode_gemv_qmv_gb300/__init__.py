@@ -76,8 +76,8 @@ def lib():
         L.qmv_mul_mat_vec_id_f32.argtypes = [_int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _int, _vp, _vp,
                                              _vp]
         L.qmv_mul_mat_vec_fused.argtypes = [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _vp]
-        L.qmv_mul_mat_vec_id_fused.argtypes = [_int, _vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int, _vp,
-                                               _vp, _vp, _vp, _vp]
+        L.qmv_mul_mat_vec_id_fused.argtypes = [_int, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int,
+                                               _vp, _vp, _vp, _vp, _vp, _vp]
         L.qmv_debug_subblock_sums.argtypes = [_int, _vp, _i64, _i64, _vp, _int, _vp, _vp]
         L.qmv_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         L.qmv_set_tuning.argtypes = [_int, _int, _int, _int, _int, _int, _int]
@@ -285,10 +285,11 @@ def mul_mat_vec_fused(qtype: int, W_up, M: int, K: int, xq=None, x=None, W_gate=
     return out
 
 
-def mul_mat_vec_id_fused(qtype: int, W, n_expert: int, M: int, K: int, ids, xq=None, x=None, W_shared=None,
-                         out=None, out_shared=None, status=None, stream=None):
-    """Expert-indexed GEMV (q8_1 xq or fp32 x, one row per token) plus an optional shared expert:
-    returns (y [n_tokens][top_k][M], y_shared [n_tokens][M] or None)."""
+def mul_mat_vec_id_fused(qtype: int, W, n_expert: int, M: int, K: int, ids, xq=None, x=None, W_gate=None,
+                         W_shared=None, W_shared_gate=None, out=None, out_shared=None, status=None, stream=None):
+    """Expert-indexed GEMV (q8_1 xq or fp32 x, one row per token), optionally gated
+    ((W.x) * silu(W_gate.x) per routed slot) and with a shared expert (gated like
+    the routed ones): returns (y [n_tokens][top_k][M], y_shared [n_tokens][M] or None)."""
     import torch
 
     pq, px, ldx, n_tok = _activations(xq, x)
@@ -301,9 +302,10 @@ def mul_mat_vec_id_fused(qtype: int, W, n_expert: int, M: int, K: int, ids, xq=N
     if W_shared is not None and out_shared is None:
         out_shared = torch.empty((n_tokens, M), dtype=torch.float32, device=W.device)
     _check("qmv_mul_mat_vec_id_fused",
-           lib().qmv_mul_mat_vec_id_fused(qtype, _ptr(W), n_expert, M, K, pq, px, ldx, _ptr(ids), n_tokens, top_k,
-                                          _ptr(out), _ptr(W_shared), _ptr(out_shared if W_shared is not None else None),
-                                          _ptr(status), _stream_handle(stream)))
+           lib().qmv_mul_mat_vec_id_fused(qtype, _ptr(W), _ptr(W_gate), n_expert, M, K, pq, px, ldx, _ptr(ids),
+                                          n_tokens, top_k, _ptr(out), _ptr(W_shared), _ptr(W_shared_gate),
+                                          _ptr(out_shared if W_shared is not None else None), _ptr(status),
+                                          _stream_handle(stream)))
     return out, (out_shared if W_shared is not None else None)
 
 

@@ -257,7 +257,8 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     const int64_t G = (p.M + rw - 1) / rw;
     int64_t gx = std::min(max_ctas, G);
     int64_t groups_per_cta = (G + gx - 1) / gx;
-    if (mode == MODE_MOE) {
+    const bool is_moe = mode == MODE_MOE || mode == MODE_MOE_GATE;
+    if (is_moe) {
         // the kernel shares the grid among the experts the ids pick (at most
         // n_potential_experts); at least one CTA per possible expert
         gx = std::max<int64_t>(max_ctas, static_cast<int64_t>(p.n_tokens) * p.top_k + (p.W2 ? 1 : 0));
@@ -294,7 +295,7 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     if (!fit(budget, wpc_f, st_f)) {
         budget = fn_limit;
         if (!fit(budget, wpc_f, st_f)) return TilePlan::NoFit;
-    } else if (!tuned_share && mode != MODE_MOE) {
+    } else if (!tuned_share && !is_moe) {
         int wpc_1 = 0, st_1 = 0;
         const int64_t gpc = (G + gx - 1) / gx;  // most row groups a CTA owns
         if (fit(fn_limit, wpc_1, st_1) && (gpc + wpc_1 - 1) / wpc_1 < (gpc + wpc_f - 1) / wpc_f) {
@@ -338,7 +339,8 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     // going for less delay (measured on GB300: qkv, gate/up and down launches
     // 1.5-3 % faster, the 4096x4096 launch, two tiles per warp, slower).
     const int64_t tiles_per_warp =
-        (groups_per_cta + wpc - 1) / wpc * ((U + 32 / rw - 1) / (32 / rw)) * (mode == MODE_GATE ? 2 : 1);
+        (groups_per_cta + wpc - 1) / wpc * ((U + 32 / rw - 1) / (32 / rw)) *
+        ((mode == MODE_GATE || mode == MODE_MOE_GATE) ? 2 : 1);
     p.pre_tiles = tu.pre_tiles.load() > 0 ? std::min(stages, tu.pre_tiles.load())
                                           : (tiles_per_warp <= stages ? stages : 1);
     p.act_bytes = static_cast<uint32_t>(act);
@@ -370,7 +372,8 @@ qmv_status plan_f32(int type, int mode, const DevInfo &dev, GemvParams p, int nc
     const int nc_t = (mode == MODE_PLAIN) ? nc_active : round_nc(nc_active);
     if (!tile_shape_ok(type, p.K, p.row_bytes)) return QMV_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(p.W) % 16 != 0 ||
-        (mode == MODE_GATE && reinterpret_cast<uintptr_t>(p.W2) % 16 != 0))
+        (mode == MODE_GATE && reinterpret_cast<uintptr_t>(p.W2) % 16 != 0) ||
+        (mode == MODE_MOE_GATE && reinterpret_cast<uintptr_t>(p.W3) % 16 != 0))
         return QMV_ERR_ALIGN;
     switch (plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L)) {
     case TilePlan::Ok: return QMV_OK;
@@ -671,30 +674,37 @@ int qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_mul_mat_vec_id_fused(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const void *xq,
-                             const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k, float *y,
-                             const void *W_shared, float *y_shared, int32_t *dev_status, void *stream)
+int qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int64_t n_expert, int64_t M, int64_t K,
+                             const void *xq, const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k,
+                             float *y, const void *W_shared_up, const void *W_shared_gate, float *y_shared,
+                             int32_t *dev_status, void *stream)
 {
     if (!xq && !x) return QMV_ERR_NULL;
     if (xq && x) return QMV_ERR_SHAPE;
-    qmv_status s = check_common(type, W, M, K, xq ? xq : static_cast<const void *>(x), y);
+    qmv_status s = check_common(type, W_up, M, K, xq ? xq : static_cast<const void *>(x), y);
     if (s != QMV_OK) return s;
     if (!ids) return QMV_ERR_NULL;
-    if (!W_shared != !y_shared) return QMV_ERR_NULL;
+    if (!W_shared_up != !y_shared) return QMV_ERR_NULL;
+    // a gated launch gates the shared expert too, a plain one does not
+    if (W_shared_up && (!W_gate != !W_shared_gate)) return QMV_ERR_NULL;
+    if (!W_shared_up && W_shared_gate) return QMV_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(ids) % 4 || reinterpret_cast<uintptr_t>(dev_status) % 4 ||
         reinterpret_cast<uintptr_t>(y_shared) % 4)
         return QMV_ERR_ALIGN;
     if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
     if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
-    if ((s = check_f32(type, W, W_shared, K, x ? ldx : K)) != QMV_OK) return s;
+    if ((s = check_f32(type, W_up, W_gate, K, x ? ldx : K)) != QMV_OK) return s;
+    if ((s = check_f32(type, W_shared_up, W_shared_gate, K, x ? ldx : K)) != QMV_OK) return s;
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
-    GemvParams p = base_params(type, W, M, K, xq, n_tokens);
+    GemvParams p = base_params(type, W_up, M, K, xq, n_tokens);
     if (x) {
         p.xf = x;
         p.ldx = ldx;
     }
-    p.W2 = static_cast<const uint8_t *>(W_shared);
+    p.W2 = static_cast<const uint8_t *>(W_shared_up);
+    p.W3 = static_cast<const uint8_t *>(W_gate);
+    p.W4 = static_cast<const uint8_t *>(W_shared_gate);
     p.y_shared = y_shared;
     p.y = y;
     p.ids = ids;
@@ -704,9 +714,9 @@ int qmv_mul_mat_vec_id_fused(int type, const void *W, int64_t n_expert, int64_t 
     p.n_expert = static_cast<int>(n_expert);
     p.expert_bytes = M * p.row_bytes;
     const int potential = static_cast<int>(std::min<int64_t>(n_expert, static_cast<int64_t>(n_tokens) * top_k)) +
-                          (W_shared ? 1 : 0);
+                          (W_shared_up ? 1 : 0);
     Launch L;
-    if ((s = plan_f32(type, MODE_MOE, dev, p, n_tokens, potential, L)) != QMV_OK) return s;
+    if ((s = plan_f32(type, W_gate ? MODE_MOE_GATE : MODE_MOE, dev, p, n_tokens, potential, L)) != QMV_OK) return s;
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 

@@ -238,8 +238,8 @@ __device__ __forceinline__ float ld_cg_f32(const float *p)
     return v;
 }
 
-// Read-only (non-coherent) load of a value that no kernel writes while this
-// one runs (weights, biases).
+// Read-only (non-coherent) load of a value that nothing writes while this
+// kernel runs (biases, read after the dependency wait).
 __device__ __forceinline__ float ld_nc_f32(const float *p)
 {
     float v;

@@ -5,11 +5,13 @@
 
 namespace qmv {
 
-enum Mode { MODE_PLAIN = 0, MODE_GATE = 1, MODE_MOE = 2, MODE_DEBUG = 3 };
+enum Mode { MODE_PLAIN = 0, MODE_GATE = 1, MODE_MOE = 2, MODE_DEBUG = 3, MODE_MOE_GATE = 4 };
 
 struct GemvParams {
     const uint8_t *W;    // weights (MoE: expert 0); GATE: the up matrix
-    const uint8_t *W2;   // GATE: the gate matrix; MOE: the shared expert (nullable)
+    const uint8_t *W2;   // GATE: the gate matrix; MOE, MOE_GATE: the shared expert's (up) matrix (nullable)
+    const uint8_t *W3;   // MOE_GATE: the experts' gate matrices [n_expert][M][row_bytes]
+    const uint8_t *W4;   // MOE_GATE with a shared expert: its gate matrix
     const uint8_t *xq;   // q8_1 activations, column c at xq + c*xq_col_bytes
     const float *xf;     // fp32 activations quantized in place (tile kernel), column c at xf + c*ldx; or null
     int64_t ldx;

@@ -236,7 +236,8 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     constexpr int SS = G::SS;                        // shared bytes per tile row
     constexpr int TB = G::TB;                        // shared bytes per tile
     constexpr int UNIT = G::UNIT;                    // bytes per unit
-    constexpr int NM = (MODE == MODE_GATE) ? 2 : 1;  // matrices (GATE: up, gate)
+    constexpr bool IS_MOE = MODE == MODE_MOE || MODE == MODE_MOE_GATE;
+    constexpr int NM = (MODE == MODE_GATE || MODE == MODE_MOE_GATE) ? 2 : 1;  // matrices (up, gate)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = p.dec_warps;  // warps that stream and decode; the others only help staging
@@ -262,9 +263,10 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     int n_active = p.ncols;
     int64_t row_base = 0;    // MoE: first row of this CTA's expert
     const uint8_t *W0 = p.W;  // first matrix (MoE: the experts, or the shared expert)
+    const uint8_t *W1 = MODE == MODE_MOE_GATE ? p.W3 : p.W2;  // gate matrix (GATE, MOE_GATE)
     bool moe_shared = false;  // MoE: this CTA serves the shared expert
     int64_t cta_index = blockIdx.x, cta_count = gridDim.x;
-    if constexpr (MODE == MODE_MOE) {
+    if constexpr (IS_MOE) {
         // Routing is known only here (ids come from the previous grid).  The
         // ids are read once into shared memory; the experts some token picks
         // are listed in ascending order (then the shared expert, if any) and
@@ -371,7 +373,10 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         }
         __syncthreads();
         n_active = s_cnt;
-        if (moe_shared) W0 = p.W2;
+        if (moe_shared) {
+            W0 = p.W2;
+            W1 = p.W4;
+        }
         else row_base = static_cast<int64_t>(expert) * p.M;
     }
 
@@ -391,7 +396,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     int ld_kt = 0, ld_m = 0, ld_buf = 0;
     int64_t issued = 0;
     auto issue_tile = [&]() {
-        const uint8_t *W = (NM == 2 && ld_m) ? p.W2 : W0;
+        const uint8_t *W = (NM == 2 && ld_m) ? W1 : W0;
         const int64_t grow = ld_g * RW;  // first row of the group inside the matrix
         const uint8_t *base = W + (row_base + grow) * rb + static_cast<int64_t>(ld_kt) * (UW * UNIT);
         const int64_t rows_left = p.M - grow;
@@ -415,9 +420,9 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     };
 
     while (issued < total && issued < p.pre_tiles) issue_tile();  // weights first
-    if constexpr (MODE != MODE_MOE) pdl_wait();
+    if constexpr (!IS_MOE) pdl_wait();
     if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
-    if constexpr (MODE == MODE_MOE)
+    if constexpr (IS_MOE)
         stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; }, 0u, 1u);
     else
         stage_tile_activations<F, NC>(p, smem, n_active, [](int c) { return c; }, crank, ncta);
@@ -449,8 +454,9 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         const int64_t row = cg * RW + r_l;
         const int u = ckt * UW + u_l;
         if constexpr (MODE == MODE_PLAIN || MODE == MODE_GATE) {
-            // the row's biases (read like the weights: not written by the previous kernel),
-            // requested at the group's first tile so that its decode hides the latency
+            // the row's biases (after the dependency wait; nothing writes them while
+            // this kernel runs), requested at the group's first tile so that its
+            // decode hides the latency
             if (ckt == 0 && cm == 0 && u_l == 0 && row < p.M) {
                 if (p.bias) b_up = ld_nc_f32(p.bias + row);
                 if (MODE == MODE_GATE && p.gate_bias) b_gate = ld_nc_f32(p.gate_bias + row);
@@ -502,15 +508,16 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
                             p.y[(size_t)c * p.ldy + row] = up * silu_f32(gate);
                         } else {
                             const int tok = s_tok[c];
+                            const float v = MODE == MODE_MOE_GATE ? acc[0][c] * silu_f32(acc[NM - 1][c]) : acc[0][c];
                             if (moe_shared) {
-                                p.y_shared[(size_t)tok * p.M + row] = acc[0][c];
+                                p.y_shared[(size_t)tok * p.M + row] = v;
                                 continue;
                             }
                             uint32_t mask = s_slots[c];
                             while (mask) {
                                 const int k = __ffs(mask) - 1;
                                 mask &= mask - 1;
-                                p.y[((size_t)tok * p.top_k + k) * p.M + row] = acc[0][c];
+                                p.y[((size_t)tok * p.top_k + k) * p.M + row] = v;
                             }
                         }
                     }
@@ -564,6 +571,7 @@ const void *tiles_kernel_fn(int mode, int nc, int rw)
     }
     if (mode == MODE_GATE) { QMV_TK_MODE(MODE_GATE) }
     if (mode == MODE_MOE) { QMV_TK_MODE(MODE_MOE) }
+    if (mode == MODE_MOE_GATE) { QMV_TK_MODE(MODE_MOE_GATE) }
     if (mode == MODE_DEBUG) { QMV_TK_MODE(MODE_DEBUG) }
 #undef QMV_TK_MODE
 #undef QMV_TK

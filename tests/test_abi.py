@@ -108,15 +108,19 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert fm(12, p, nul, 16, 4096, p, nul, 0, 0, nul, nul, p, nul) == 4
     assert fm(12, p, ctypes.c_void_p(0x1008), 16, 4096, p, nul, 0, 1, nul, nul, p, nul) == 5
     assert fm(9, p, nul, 16, 4096, p, nul, 0, 1, nul, nul, p, nul) == 2
-    im = L.qmv_mul_mat_vec_id_fused
-    assert im(12, p, 8, 16, 4096, nul, nul, 0, p, 4, 2, p, nul, nul, nul, nul) == 1
-    assert im(12, p, 8, 16, 4096, p, p, 4096, p, 4, 2, p, nul, nul, nul, nul) == 3
-    assert im(12, p, 8, 16, 4096, p, nul, 0, p, 4, 2, p, p, nul, nul, nul) == 1
-    assert im(12, p, 8, 16, 4096, p, nul, 0, p, 4, 2, p, nul, p, nul, nul) == 1
-    assert im(12, p, 8, 16, 4096, p, nul, 0, p, 4, 2, p, ctypes.c_void_p(0x1008), p, nul, nul) == 5
-    assert im(12, p, 8, 16, 4096, p, nul, 0, p, 9, 2, p, p, p, nul, nul) == 4
-    assert im(12, p, 8, 16, 4096, p, nul, 0, nul, 4, 2, p, p, p, nul, nul) == 1
-    assert im(14, p, 8, 16, 2304, p, nul, 0, p, 4, 2, p, p, p, nul, nul) == 3
+    im = L.qmv_mul_mat_vec_id_fused   # (type, W, W_gate, E, M, K, xq, x, ldx, ids, T, k, y, Ws, Wsg, ys, st, s)
+    assert im(12, p, nul, 8, 16, 4096, nul, nul, 0, p, 4, 2, p, nul, nul, nul, nul, nul) == 1
+    assert im(12, p, nul, 8, 16, 4096, p, p, 4096, p, 4, 2, p, nul, nul, nul, nul, nul) == 3
+    assert im(12, p, nul, 8, 16, 4096, p, nul, 0, p, 4, 2, p, p, nul, nul, nul, nul) == 1    # Ws without ys
+    assert im(12, p, nul, 8, 16, 4096, p, nul, 0, p, 4, 2, p, nul, nul, p, nul, nul) == 1    # ys without Ws
+    assert im(12, p, p, 8, 16, 4096, p, nul, 0, p, 4, 2, p, p, nul, p, nul, nul) == 1        # gated, no shared gate
+    assert im(12, p, nul, 8, 16, 4096, p, nul, 0, p, 4, 2, p, p, p, p, nul, nul) == 1        # shared gate, not gated
+    assert im(12, p, nul, 8, 16, 4096, p, nul, 0, p, 4, 2, p, nul, p, nul, nul, nul) == 3    # shared gate alone
+    assert im(12, p, nul, 8, 16, 4096, p, nul, 0, p, 4, 2, p, ctypes.c_void_p(0x1008), nul, p, nul, nul) == 5
+    assert im(12, p, ctypes.c_void_p(0x1008), 8, 16, 4096, p, nul, 0, p, 4, 2, p, nul, nul, nul, nul, nul) == 5
+    assert im(12, p, nul, 8, 16, 4096, p, nul, 0, p, 9, 2, p, p, nul, p, nul, nul) == 4
+    assert im(12, p, nul, 8, 16, 4096, p, nul, 0, nul, 4, 2, p, p, nul, p, nul, nul) == 1
+    assert im(14, p, nul, 8, 16, 2304, p, nul, 0, p, 4, 2, p, p, nul, p, nul, nul) == 3
     # tuning knobs validate too
     assert L.qmv_set_tuning(12, 100, 0, 0, 0, 0, 0) == 3
     assert L.qmv_set_tuning(12, 544, 0, 0, 0, 0, 0) == 3

@@ -168,3 +168,50 @@ def test_moe_shared_expert_edge_routings(q):
     rng = np.random.default_rng(1422)
     ids = rng.permutation(E2)[:256].astype(np.int32).reshape(8, 32)
     _moe_shared_case(q, t, E2, 20, 256, ids, 1423, "q8_1")
+
+
+def _moe_gated_case(q, t, E, M, K, ids, seed, inp, shared=True):
+    import torch
+
+    Wu = weights(t, E * M, K, seed).reshape(E, -1)
+    Wg = weights(t, E * M, K, seed + 2).reshape(E, -1)
+    Wsu, Wsg = weights(t, M, K, seed + 5), weights(t, M, K, seed + 6)
+    T = ids.shape[0]
+    x = synthetic.activations_f32(seed + 1, T, K)
+    xq = oracle.quantize_q8_1(x)
+    u, l1u, bad = oracle.moe_gemv(t, Wu, E, M, K, xq, ids)
+    g, l1g, _ = oracle.moe_gemv(t, Wg, E, M, K, xq, ids)
+    status = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    kw = {"xq": dev(xq)} if inp == "q8_1" else {"x": dev(x)}
+    if shared:
+        kw.update(W_shared=dev(Wsu), W_shared_gate=dev(Wsg))
+    y, ys = q.mul_mat_vec_id_fused(t, dev(Wu), E, M, K, dev(ids), W_gate=dev(Wg), status=status, **kw)
+    y = host(y)
+    assert int(host(status)[0]) == bad
+    ref = oracle.swiglu(g, u)
+    assert np.all(np.abs(y - ref) <= glu_tol(g, u, l1g, l1u)), f"routed, ids {ids.tolist()}"
+    if shared:
+        ys = host(ys)
+        su, l1su = oracle.shared_expert_gemv(t, Wsu, M, K, xq, T)
+        sg, l1sg = oracle.shared_expert_gemv(t, Wsg, M, K, xq, T)
+        assert np.all(np.abs(ys - oracle.swiglu(sg, su)) <= glu_tol(sg, su, l1sg, l1su)), "shared expert"
+    else:
+        assert ys is None
+    return y
+
+
+@pytest.mark.parametrize("t", [oracle.Q4_0, oracle.Q4_K, oracle.Q6_K])
+@pytest.mark.parametrize("inp", ["q8_1", "f32"])
+def test_moe_gated(q, t, inp):
+    # the MoE form of the fused gate/up: y[t][k] = (W_up[e] x_t) * silu(W_gate[e] x_t)
+    K = 2048 if t == oracle.Q6_K else 1024
+    ids = synthetic.moe_ids(1500 + t, 4, 2, 8)
+    _moe_gated_case(q, t, 8, 203, K, ids, 1510 + t, inp)
+
+
+def test_moe_gated_edge_routings(q):
+    t, E, M, K = oracle.Q4_K, 8, 77, 512
+    y = _moe_gated_case(q, t, E, M, K, np.array([[1, 9], [-1, 2], [2, 1]], dtype=np.int32), 1520, "q8_1")
+    assert not y[0, 1].any() and not y[1, 0].any()
+    _moe_gated_case(q, t, E, M, K, synthetic.moe_ids(1521, 8, 4, E), 1522, "f32", shared=False)
+    _moe_gated_case(q, t, E, M, K, np.array([[3, 3]], dtype=np.int32), 1523, "q8_1")
