@@ -236,7 +236,7 @@ def fused_epilogue(up, gate=None, bias=None, gate_bias=None):
     SwiGLU case), in fp64: result = up + x_bias; with a gate, gate_value =
     gate + gate_bias and result *= silu(gate_value).  up and gate are
     [ncols][M]; bias and gate_bias are [M] vectors, the same for every column
-    (the reading this build takes: the page's epilogue adds the bias of the
+    (the reading taken here: the page's epilogue adds the bias of the
     output row, and a layer's bias does not depend on the token)."""
     r = np.asarray(up, dtype=np.float64)
     if bias is not None:
@@ -260,7 +260,7 @@ def moe_gemv(t: int, W: np.ndarray, n_expert: int, M: int, K: int, xq: np.ndarra
              rows=None):
     """Expert-indexed GEMV (mul_mat_vec_q page, "MoE" section): for token t and
     slot k, y[t][k] = W[ids[t][k]] . x[t].  Ids outside [0, n_expert) yield a
-    zero output row (the reading this build takes for invalid ids); returns
+    zero output row (the reading taken here for invalid ids); returns
     (y, l1, n_invalid) with y, l1 of shape [n_tokens][top_k][nrows]."""
     W = np.ascontiguousarray(W, dtype=np.uint8).reshape(n_expert, -1)
     n_tokens, top_k = ids.shape
