@@ -363,6 +363,17 @@ def measure_configs(q, torch, stream, device, reps):
                          for W in ws])
         sweep[str(nc)] = {"us_per_call": round(us, 3), "weight_gbs": round(ws[0].numel() / us / 1e3, 1)}
     out["q4_K 14336x4096 ncols 1..8"] = sweep
+    # the same sweep for Q6_K (4096x14336, the down projection of an 8B-class FFN)
+    ws6 = weights(q.Q6_K, 4096, 14336, 6, 3_000_450)
+    sweep6 = {}
+    for nc in range(1, 9):
+        xq = xq_of(14336, nc, 3_000_460 + nc)
+        us = chain_time([lambda W=W: q.mul_mat_vec(q.Q6_K, W, 4096, 14336, xq, nc, out=y[:nc, :4096], stream=stream)
+                         for W in ws6])
+        sweep6[str(nc)] = {"us_per_call": round(us, 3), "weight_gbs": round(ws6[0].numel() / us / 1e3, 1)}
+    out["q6_K 4096x14336 ncols 1..8"] = sweep6
+    del ws6
+    torch.cuda.empty_cache()
     # fused gate/up, two 14336x4096 matrices per call
     xq = xq_of(4096, 1, 3_000_500)
     pairs = [(ws[2 * i], ws[2 * i + 1]) for i in range(4)]

@@ -281,6 +281,20 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
         st = stages;
         while (w > 1 && need(w, st, packed) > budget) --w;
         while (st > 1 && need(w, st, packed) > budget) --st;
+        // When the staged activations squeeze the rings (many columns of a long
+        // row) so that some warp would own two row groups where single-tile
+        // rings leave every warp at most one, take the single-tile rings: the
+        // busiest warp's serial work halves (Q6_K 4096x14336 at 7-8 columns,
+        // 7 groups of 7 tiles per CTA: 34 -> 25-27 us).
+        if (st > 1 && !tu.stages.load()) {
+            int w1 = max_wpc;
+            while (w1 > 1 && need(w1, 1, packed) > budget) --w1;
+            const int64_t g2 = (groups_per_cta + w - 1) / w, g1 = (groups_per_cta + w1 - 1) / w1;
+            if (g2 == 2 && g1 == 1) {
+                w = w1;
+                st = 1;
+            }
+        }
         return need(w, st, packed) <= budget;
     };
     auto share_budget = [&](int share) {
