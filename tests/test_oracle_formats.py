@@ -178,3 +178,28 @@ def test_q6_K_codes_follow_the_printed_vec_dot_assembly():
                 codes = (vil | vih).view(np.uint8).astype(np.int32) - 32
                 g = run + 2 * i                        # the 32-element group these bytes fill
                 assert np.array_equal(vals[128 * h + 32 * g: 128 * h + 32 * g + 32], codes), (h, run, i)
+
+
+def test_worked_launch_example_for_4096x4096_q4_K():
+    # The mul_mat_vec_q page works one launch out by hand for a 4096 x 4096 Q4_K
+    # layer (section "一次 launch 的参数账"): 16 super-blocks per row; with
+    # vdr = 2, qi = 32, 4 warps of 32 lanes, 8 super-blocks per iteration; one
+    # row per block, so 4096 blocks of 128 threads; 2 rounds of 16 weights per
+    # thread, 32 weights each; 524,288 threads x 32 = 4096^2 weights; 1,152
+    # weight bytes per round and 2,304 per block.  The oracle's constants must
+    # reproduce every printed number.
+    M = K = 4096
+    qk = oracle.block_elems(oracle.Q4_K)
+    bb = oracle.block_bytes(oracle.Q4_K)
+    blocks_per_row = K // qk
+    assert blocks_per_row == 16
+    vdr, qi, nwarps, warp = 2, 32, 4, 32
+    blocks_per_iter = vdr * nwarps * warp // qi
+    assert blocks_per_iter == 8
+    rounds = blocks_per_row // blocks_per_iter
+    weights_per_thread = rounds * 16
+    assert (rounds, weights_per_thread) == (2, 32)
+    threads = M * nwarps * warp
+    assert threads == 524288 and threads * weights_per_thread == M * K == 16777216
+    assert blocks_per_iter * bb == 1152
+    assert rounds * blocks_per_iter * bb == oracle.row_bytes(oracle.Q4_K, K) == 2304
