@@ -176,6 +176,17 @@ def test_gemv_edge_shapes(q):
             assert_close_l1(y, y_ref, l1, f"type {t} M={M}")
 
 
+def test_gemv_minimum_k(q):
+    # K at one block of the format (Q4_0: 32, K-quants: one 256-weight super-block)
+    for t, K in ((oracle.Q4_0, 32), (oracle.Q4_K, 256), (oracle.Q6_K, 256)):
+        for M, ncols in ((5, 1), (37, 3)):
+            W = weights(t, M, K, 550 + K + M)
+            xq = oracle.quantize_q8_1(synthetic.activations_f32(551 + M, ncols, K))
+            y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq, ncols)
+            y = host(q.mul_mat_vec(t, dev(W), M, K, dev(xq), ncols))
+            assert_close_l1(y, y_ref, l1, f"type {t} K={K} M={M} ncols={ncols}")
+
+
 def test_zero_weights_and_activations_give_exact_zeros(q):
     for t in oracle.WEIGHT_TYPES:
         M, K = 33, 2048
