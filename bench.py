@@ -53,7 +53,7 @@ SHAPES = {"4096x4096": (D_MODEL, D_MODEL), "11008x4096": (D_FF, D_MODEL), "4096x
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "2e6f673603321006", "bytes_per_launch": 28528320,
+TRAFFIC = {"csrc_sha": "682f93bc8d88e5c1", "bytes_per_launch": 28528832,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down (profiles/gemv_tiles_q4_K_down_fused.md)"}
 
 

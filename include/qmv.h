@@ -68,7 +68,9 @@ typedef enum {
     QMV_ERR_ALIGN = 5,        /* a pointer violates the alignment stated above */
     QMV_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
     QMV_ERR_IDS = 7,          /* reserved: invalid expert ids are reported through dev_status */
-    QMV_ERR_DEVICE_FAULT = 8  /* a kernel's bounded wait ran out (see qmv_device_fault) */
+    QMV_ERR_DEVICE_FAULT = 8, /* a kernel's bounded wait ran out (see qmv_device_fault) */
+    QMV_ERR_RANGE = 9         /* checked mode: an argument's byte range is not inside one device
+                                 allocation (see qmv_set_checked) */
 } qmv_status;
 
 /* Human-readable name of a status code (static storage). */
@@ -280,6 +282,28 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
  * never write weights except qmv_quantize_weights, which launches
  * ordinarily. */
 int qmv_set_pdl(int enable);
+
+/* Checked mode (process-wide; off by default, or on when the environment
+ * variable QMV_CHECKED is set to anything but "0" before the first call).
+ * When on, every call also checks on the host, before it launches, that the
+ * whole byte range it will read or write through each pointer argument lies
+ * inside one device allocation known to the CUDA driver (cuMemGetAddressRange):
+ *   W (each weight matrix)   M * qmv_row_bytes(type, K) bytes, times n_expert
+ *                            for the MoE calls
+ *   xq                       qmv_q8_1_bytes(K, ncols or n_tokens)
+ *   x                        ((ncols - 1) * ldx + K) * 4 bytes
+ *   y                        ncols * M * 4 (MoE: n_tokens * top_k * M * 4)
+ *   ids / dev_status         n_tokens * top_k * 4 / 4
+ *   bias, gate_bias          M * 4;  y_shared  n_tokens * M * 4
+ * A range that runs past its allocation, or a pointer outside every device
+ * allocation the driver tracks (pageable host memory, a freed buffer),
+ * returns QMV_ERR_RANGE and launches nothing.  The check works at the
+ * granularity of driver allocations: a sub-allocator (PyTorch's caching
+ * allocator, for one) hands out slices of larger allocations, and an overrun
+ * that stays inside the same allocation is not seen.  It costs one driver
+ * query per pointer, so it is meant for debugging and tests; under CUDA graph
+ * capture it runs once, when the call is captured.  Returns QMV_OK. */
+int qmv_set_checked(int enable);
 
 #ifdef __cplusplus
 }

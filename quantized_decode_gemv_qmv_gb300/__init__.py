@@ -30,6 +30,7 @@ EXPORTS = (
     "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32", "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32",
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
+    "qmv_set_checked",
 )
 
 
@@ -83,11 +84,13 @@ def lib():
         L.qmv_set_tuning.argtypes = [_int, _int, _int, _int, _int, _int, _int]
         L.qmv_set_stream_tuning.argtypes = [_int, _int, _int]
         L.qmv_set_pdl.argtypes = [_int]
+        L.qmv_set_checked.argtypes = [_int]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
                      "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_mul_mat_vec_fused",
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
-                     "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl"):
+                     "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
+                     "qmv_set_checked"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -340,3 +343,9 @@ def set_stream_tuning(qtype: int, dec_warps: int = 0, pre_tiles: int = 0):
 
 def set_pdl(enable: bool):
     _check("qmv_set_pdl", lib().qmv_set_pdl(1 if enable else 0))
+
+
+def set_checked(enable: bool):
+    """Checked mode: every call first verifies on the host that each argument's
+    byte range lies inside one device allocation (QMV_ERR_RANGE otherwise)."""
+    _check("qmv_set_checked", lib().qmv_set_checked(1 if enable else 0))

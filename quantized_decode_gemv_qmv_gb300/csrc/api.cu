@@ -2,6 +2,7 @@
 // The public contract is documented in include/qmv.h.
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -449,6 +450,67 @@ qmv_status launch(const Launch &L, cudaStream_t st)
     return cuda_status(e);
 }
 
+
+// ---- checked mode: byte ranges of the arguments inside device allocations ----
+std::atomic<int> g_checked{-1};  // -1: QMV_CHECKED not read yet
+
+bool checked_mode()
+{
+    int v = g_checked.load();
+    if (v < 0) {
+        const char *e = getenv("QMV_CHECKED");
+        int want = (e && *e && *e != '0') ? 1 : 0, expect = -1;
+        g_checked.compare_exchange_strong(expect, want);
+        v = g_checked.load();
+    }
+    return v == 1;
+}
+
+// cuMemGetAddressRange, looked up at run time (the library does not link the driver)
+using AddrRangeFn = int (*)(unsigned long long *, size_t *, unsigned long long);
+
+AddrRangeFn addr_range_fn()
+{
+    static const AddrRangeFn f = [] {
+        void *fp = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fp, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<AddrRangeFn>(nullptr);
+        return reinterpret_cast<AddrRangeFn>(fp);
+    }();
+    return f;
+}
+
+// In checked mode [p, p + bytes) must lie inside one device allocation;
+// QMV_ERR_RANGE otherwise (also for memory the driver does not know).
+qmv_status check_range(const void *p, uint64_t bytes)
+{
+    if (!checked_mode() || p == nullptr || bytes == 0) return QMV_OK;
+    const AddrRangeFn f = addr_range_fn();
+    if (!f) return QMV_ERR_CUDA;
+    unsigned long long base = 0;
+    size_t size = 0;
+    const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+    if (f(&base, &size, a) != 0 || a < base) return QMV_ERR_RANGE;
+    const unsigned long long off = a - base;
+    if (off > size || bytes > size - off) return QMV_ERR_RANGE;
+    return QMV_OK;
+}
+
+#define QMV_RANGE(ptr, nbytes)                                          \
+    do {                                                                \
+        const qmv_status r_ = check_range((ptr), (nbytes));             \
+        if (r_ != QMV_OK) return r_;                                    \
+    } while (0)
+
+// bytes of ncols fp32 columns of K values, column stride ldx
+uint64_t f32_cols_bytes(int64_t K, int ncols, int64_t ldx)
+{
+    return (static_cast<uint64_t>(ncols - 1) * static_cast<uint64_t>(ldx) + static_cast<uint64_t>(K)) * 4u;
+}
+
 qmv_status check_common(int type, const void *W, int64_t M, int64_t K, const void *xq, const void *out)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
@@ -458,6 +520,21 @@ qmv_status check_common(int type, const void *W, int64_t M, int64_t K, const voi
     if (reinterpret_cast<uintptr_t>(W) % 2 || reinterpret_cast<uintptr_t>(xq) % 4 ||
         reinterpret_cast<uintptr_t>(out) % 4)
         return QMV_ERR_ALIGN;
+    return QMV_OK;
+}
+
+// Checked mode: the byte ranges a GEMV-family call reads and writes.  n_mat
+// weight matrices of M rows each; ncols activation columns (q8_1 from xq, or
+// fp32 from x with column stride ldx); y_elems fp32 outputs.
+qmv_status check_gemv_ranges(int type, int64_t M, int64_t K, const void *const *Ws, int n_W, int64_t n_mat,
+                             const void *xq, const float *x, int64_t ldx, int ncols, const void *y, uint64_t y_elems)
+{
+    if (!checked_mode()) return QMV_OK;
+    const uint64_t w_bytes = static_cast<uint64_t>(n_mat) * static_cast<uint64_t>(M) * qmv_row_bytes(type, K);
+    for (int i = 0; i < n_W; ++i) QMV_RANGE(Ws[i], w_bytes);
+    QMV_RANGE(xq, qmv_q8_1_bytes(K, ncols));
+    QMV_RANGE(x, f32_cols_bytes(K, ncols, ldx));
+    QMV_RANGE(y, y_elems * 4u);
     return QMV_OK;
 }
 
@@ -494,6 +571,7 @@ const char *qmv_status_str(int s)
     case QMV_ERR_CUDA: return "CUDA error";
     case QMV_ERR_IDS: return "invalid expert id";
     case QMV_ERR_DEVICE_FAULT: return "device wait timed out";
+    case QMV_ERR_RANGE: return "argument outside its device allocation";
     default: return "unknown status";
     }
 }
@@ -519,6 +597,8 @@ int qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *x
     if (!x || !xq) return QMV_ERR_NULL;
     if (K <= 0 || ncols <= 0 || ldx < K || K > (int64_t(1) << 28)) return QMV_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(xq) % 4) return QMV_ERR_ALIGN;
+    QMV_RANGE(x, f32_cols_bytes(K, ncols, ldx));
+    QMV_RANGE(xq, qmv_q8_1_bytes(K, ncols));
     return cuda_status(launch_quantize_q8_1(x, K, ncols, ldx, static_cast<uint8_t *>(xq),
                                             static_cast<cudaStream_t>(stream), g_pdl.load() != 0));
 }
@@ -529,6 +609,8 @@ int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t
     if (!w || !W) return QMV_ERR_NULL;
     if (M <= 0 || K <= 0 || K % block_elems(type) || ldw < K) return QMV_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(w) % 4 || reinterpret_cast<uintptr_t>(W) % 2) return QMV_ERR_ALIGN;
+    QMV_RANGE(w, static_cast<uint64_t>(M - 1) * static_cast<uint64_t>(ldw) * 4u + static_cast<uint64_t>(K) * 4u);
+    QMV_RANGE(W, static_cast<uint64_t>(M) * qmv_row_bytes(type, K));
     return cuda_status(launch_quantize_weights(type, w, M, K, ldw, static_cast<uint8_t *>(W),
                                                static_cast<int64_t>(qmv_row_bytes(type, K)),
                                                static_cast<cudaStream_t>(stream)));
@@ -540,6 +622,8 @@ int qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *x
     qmv_status s = check_common(type, W, M, K, xq, y);
     if (s != QMV_OK) return s;
     if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    if ((s = check_gemv_ranges(type, M, K, &W, 1, 1, xq, nullptr, 0, ncols, y, uint64_t(ncols) * M)) != QMV_OK)
+        return s;
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     GemvParams p = base_params(type, W, M, K, xq, ncols);
@@ -557,6 +641,11 @@ int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_u
     if (!W_gate) return QMV_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(W_gate) % 2) return QMV_ERR_ALIGN;
     if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    {
+        const void *Ws[2] = {W_up, W_gate};
+        if ((s = check_gemv_ranges(type, M, K, Ws, 2, 1, xq, nullptr, 0, ncols, y, uint64_t(ncols) * M)) != QMV_OK)
+            return s;
+    }
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     GemvParams p = base_params(type, W_up, M, K, xq, ncols);
@@ -576,6 +665,11 @@ int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int
     if (reinterpret_cast<uintptr_t>(ids) % 4 || reinterpret_cast<uintptr_t>(dev_status) % 4) return QMV_ERR_ALIGN;
     if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
     if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
+    if ((s = check_gemv_ranges(type, M, K, &W, 1, n_expert, xq, nullptr, 0, n_tokens, y,
+                               uint64_t(n_tokens) * top_k * M)) != QMV_OK)
+        return s;
+    QMV_RANGE(ids, uint64_t(n_tokens) * top_k * 4u);
+    QMV_RANGE(dev_status, 4u);
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     GemvParams p = base_params(type, W, M, K, xq, n_tokens);
@@ -599,6 +693,8 @@ int qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const flo
     if (s != QMV_OK) return s;
     if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
     if ((s = check_f32(type, W, nullptr, K, ldx)) != QMV_OK) return s;
+    if ((s = check_gemv_ranges(type, M, K, &W, 1, 1, nullptr, x, ldx, ncols, y, uint64_t(ncols) * M)) != QMV_OK)
+        return s;
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     GemvParams p = base_params(type, W, M, K, nullptr, ncols);
@@ -619,6 +715,11 @@ int qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void 
     if (reinterpret_cast<uintptr_t>(W_gate) % 2) return QMV_ERR_ALIGN;
     if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
     if ((s = check_f32(type, W_up, W_gate, K, ldx)) != QMV_OK) return s;
+    {
+        const void *Ws[2] = {W_up, W_gate};
+        if ((s = check_gemv_ranges(type, M, K, Ws, 2, 1, nullptr, x, ldx, ncols, y, uint64_t(ncols) * M)) != QMV_OK)
+            return s;
+    }
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     GemvParams p = base_params(type, W_up, M, K, nullptr, ncols);
@@ -642,6 +743,11 @@ int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M,
     if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
     if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
     if ((s = check_f32(type, W, nullptr, K, ldx)) != QMV_OK) return s;
+    if ((s = check_gemv_ranges(type, M, K, &W, 1, n_expert, nullptr, x, ldx, n_tokens, y,
+                               uint64_t(n_tokens) * top_k * M)) != QMV_OK)
+        return s;
+    QMV_RANGE(ids, uint64_t(n_tokens) * top_k * 4u);
+    QMV_RANGE(dev_status, 4u);
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     GemvParams p = base_params(type, W, M, K, nullptr, n_tokens);
@@ -672,6 +778,14 @@ int qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_
     if (reinterpret_cast<uintptr_t>(bias) % 4 || reinterpret_cast<uintptr_t>(gate_bias) % 4) return QMV_ERR_ALIGN;
     if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
     if ((s = check_f32(type, W_up, W_gate, K, x ? ldx : K)) != QMV_OK) return s;
+    {
+        const void *Ws[2] = {W_up, W_gate};
+        if ((s = check_gemv_ranges(type, M, K, Ws, W_gate ? 2 : 1, 1, xq, x, ldx, ncols, y, uint64_t(ncols) * M)) !=
+            QMV_OK)
+            return s;
+    }
+    QMV_RANGE(bias, uint64_t(M) * 4u);
+    QMV_RANGE(gate_bias, uint64_t(M) * 4u);
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     GemvParams p = base_params(type, W_up, M, K, xq, ncols);
@@ -709,6 +823,18 @@ int qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int
     if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
     if ((s = check_f32(type, W_up, W_gate, K, x ? ldx : K)) != QMV_OK) return s;
     if ((s = check_f32(type, W_shared_up, W_shared_gate, K, x ? ldx : K)) != QMV_OK) return s;
+    {
+        const void *Ws[2] = {W_up, W_gate};
+        if ((s = check_gemv_ranges(type, M, K, Ws, W_gate ? 2 : 1, n_expert, xq, x, ldx, n_tokens, y,
+                                   uint64_t(n_tokens) * top_k * M)) != QMV_OK)
+            return s;
+        const void *Ss[2] = {W_shared_up, W_shared_gate};
+        if ((s = check_gemv_ranges(type, M, K, Ss, 2, 1, nullptr, nullptr, 0, n_tokens, y_shared,
+                                   uint64_t(n_tokens) * M)) != QMV_OK)
+            return s;
+    }
+    QMV_RANGE(ids, uint64_t(n_tokens) * top_k * 4u);
+    QMV_RANGE(dev_status, 4u);
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     GemvParams p = base_params(type, W_up, M, K, xq, n_tokens);
@@ -743,6 +869,9 @@ int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const
     DevInfo dev;
     if ((s = device_info(dev)) != QMV_OK) return s;
     const int64_t per_row = (type == FMT_Q4_0) ? K / 32 : K / 16;
+    if ((s = check_gemv_ranges(type, M, K, &W, 1, 1, xq, nullptr, 0, ncols, out, uint64_t(ncols) * M * per_row)) !=
+        QMV_OK)
+        return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(out, 0, static_cast<size_t>(ncols) * M * per_row * sizeof(int32_t), st) != cudaSuccess)
         return QMV_ERR_CUDA;
@@ -796,6 +925,12 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles)
 int qmv_set_pdl(int enable)
 {
     g_pdl = enable ? 1 : 0;
+    return QMV_OK;
+}
+
+int qmv_set_checked(int enable)
+{
+    g_checked = enable ? 1 : 0;
     return QMV_OK;
 }
 

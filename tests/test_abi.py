@@ -56,6 +56,8 @@ def test_status_strings_and_version(qlib):
     L = qlib.lib()
     assert L.qmv_status_str(0) == b"ok"
     assert L.qmv_status_str(3) == b"bad shape"
+    assert L.qmv_status_str(9) == b"argument outside its device allocation"
+    assert L.qmv_status_str(10) == b"unknown status"
     assert L.qmv_version() >= 10000
 
 
@@ -134,3 +136,14 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_set_stream_tuning(12, -1, 0) == 3
     assert L.qmv_set_stream_tuning(9, 0, 0) == 2
     assert L.qmv_set_stream_tuning(12, 0, 0) == 0
+
+
+def test_checked_mode_runs_after_the_argument_checks(qlib):
+    """Checked mode only adds the byte-range check; every argument error is
+    still reported with its own status before any range is queried."""
+    L = qlib.lib()
+    assert L.qmv_set_checked(1) == 0
+    try:
+        test_host_validation_rejects_bad_arguments(qlib)
+    finally:
+        assert L.qmv_set_checked(0) == 0
