@@ -51,9 +51,12 @@ LAYER = [("q", D_MODEL, D_MODEL, 0), ("k", D_MODEL, D_MODEL, 0), ("v", D_MODEL, 
          ("down", D_MODEL, D_FF, 3)]
 SHAPES = {"4096x4096": (D_MODEL, D_MODEL), "11008x4096": (D_FF, D_MODEL), "4096x11008": (D_MODEL, D_FF)}
 
+# column count from which the plain Q4_K GEMV decodes with mma.sync (the library's default: never)
+MMA_MIN_COLS = 9
+
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "682f93bc8d88e5c1", "bytes_per_launch": 28528832,
+TRAFFIC = {"csrc_sha": "d07c26b3eadabc90", "bytes_per_launch": 28528096,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down (profiles/gemv_tiles_q4_K_down_fused.md)"}
 
 
@@ -359,9 +362,17 @@ def measure_configs(q, torch, stream, device, reps):
     sweep = {}
     for nc in range(1, 9):
         xq = xq_of(4096, nc, 3_000_400 + nc)
-        us = chain_time([lambda W=W: q.mul_mat_vec(q.Q4_K, W, 14336, 4096, xq, nc, out=y[:nc, :14336], stream=stream)
-                         for W in ws])
-        sweep[str(nc)] = {"us_per_call": round(us, 3), "weight_gbs": round(ws[0].numel() / us / 1e3, 1)}
+        calls = [lambda W=W: q.mul_mat_vec(q.Q4_K, W, 14336, 4096, xq, nc, out=y[:nc, :14336], stream=stream)
+                 for W in ws]
+        # both decodes at every column count (the crossover), then the default choice
+        both = {}
+        for tag, min_cols in (("dp4a", 9), ("mma", 1)):
+            q.set_mma_min_cols(q.Q4_K, min_cols)
+            both[tag + "_us"] = round(chain_time(calls), 3)
+        q.set_mma_min_cols(q.Q4_K, 0)
+        us = chain_time(calls)
+        sweep[str(nc)] = {"us_per_call": round(us, 3), "weight_gbs": round(ws[0].numel() / us / 1e3, 1),
+                          "decode": "mma" if nc >= MMA_MIN_COLS else "dp4a", **both}
     out["q4_K 14336x4096 ncols 1..8"] = sweep
     # the same sweep for Q6_K (4096x14336, the down projection of an 8B-class FFN)
     ws6 = weights(q.Q6_K, 4096, 14336, 6, 3_000_450)

@@ -272,6 +272,20 @@ int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_
  * QMV_ERR_TYPE for a non-weight type, QMV_ERR_SHAPE for values out of range. */
 int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
 
+/* Column count from which the plain GEMV of `type` (qmv_mul_mat_vec, its
+ * fp32-input and fused forms) decodes with the tensor cores instead of the
+ * per-column dp4a: 8-row tiles multiplied by all columns at once with
+ * mma.sync (fp16 operands holding the exact 4-bit and int8 codes, fp32
+ * accumulators holding the exact integer block dots), then the same fp32
+ * block scaling.  Q4_K only (other types ignore it).  min_cols: 1..8, 9 =
+ * never, 0 = the built-in default (never: on GB300 this decode measured
+ * slower than dp4a at every column count up to 8; it is kept for that
+ * comparison and for other parts).  Results agree with the dp4a decode to
+ * fp32 rounding of the scaled sums (not bit for bit); q8_1 and fp32 input
+ * stay bit-identical to each other at every setting.  Returns QMV_ERR_TYPE for
+ * a non-weight type, QMV_ERR_SHAPE for values out of range. */
+int qmv_set_mma_min_cols(int type, int min_cols);
+
 /* Enables (1, default) or disables (0) programmatic dependent launch for the
  * library's q8_1 and GEMV kernels.  When enabled, a GEMV may start streaming
  * its weights while the kernel before it on the stream is still finishing,

@@ -30,7 +30,7 @@ EXPORTS = (
     "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32", "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32",
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
-    "qmv_set_checked",
+    "qmv_set_checked", "qmv_set_mma_min_cols",
 )
 
 
@@ -85,12 +85,13 @@ def lib():
         L.qmv_set_stream_tuning.argtypes = [_int, _int, _int]
         L.qmv_set_pdl.argtypes = [_int]
         L.qmv_set_checked.argtypes = [_int]
+        L.qmv_set_mma_min_cols.argtypes = [_int, _int]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
                      "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_mul_mat_vec_fused",
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
-                     "qmv_set_checked"):
+                     "qmv_set_checked", "qmv_set_mma_min_cols"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -339,6 +340,11 @@ def set_tuning(qtype: int, threads: int = 0, slice_units: int = 0, stages: int =
 def set_stream_tuning(qtype: int, dec_warps: int = 0, pre_tiles: int = 0):
     """Decoding warps per CTA and tiles per warp requested before the dependency wait (0: default)."""
     _check("qmv_set_stream_tuning", lib().qmv_set_stream_tuning(qtype, dec_warps, pre_tiles))
+
+
+def set_mma_min_cols(qtype: int, min_cols: int = 0):
+    """Columns from which the plain Q4_K GEMV decodes with mma.sync (0: the default, never; 9: never)."""
+    _check("qmv_set_mma_min_cols", lib().qmv_set_mma_min_cols(qtype, min_cols))
 
 
 def set_pdl(enable: bool):

@@ -15,6 +15,7 @@ namespace qmv {
 
 const void *gemv_tiles_fn_q4_0(int mode, int nc, int rw);
 const void *gemv_tiles_fn_q4_K(int mode, int nc, int rw);
+const void *gemv_tiles_mma_fn_q4_K(int mode);
 const void *gemv_tiles_fn_q6_K(int mode, int nc, int rw);
 const void *gemv_generic_fn_q4_0(int mode);
 const void *gemv_generic_fn_q4_K(int mode);
@@ -63,6 +64,7 @@ std::atomic<int> g_pdl{1};
 struct Tuning {
     std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0}, cluster{0};
     std::atomic<int> dec_warps{0}, pre_tiles{0};
+    std::atomic<int> mma_min_cols{0};  // 0: MMA_MIN_COLS; 9: never
 };
 Tuning g_tuning[3];
 
@@ -226,22 +228,31 @@ bool tile_shape_ok(int type, int64_t K, int64_t row_bytes)
 enum class TilePlan { Ok, NoFit, Error };
 
 TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int nc_t, int n_potential_experts,
-                    Launch &L)
+                    Launch &L, bool allow_mma = true)
 {
     const Tuning &tu = g_tuning[tidx(type)];
     const int U = static_cast<int>(p.K / 256);
+    // the tensor-core decode (16-row tiles) for the plain Q4_K GEMV from
+    // mma_min columns on; the same choice for q8_1 and fp32 input, so the two
+    // stay bit-identical
+    const int mma_min = tu.mma_min_cols.load() > 0 ? tu.mma_min_cols.load() : MMA_MIN_COLS;
+    const bool mma = allow_mma && type == FMT_Q4_K && mode == MODE_PLAIN && nc_t >= mma_min;
     int rw = 4;
-    if (tu.slice_units.load()) rw = 32 / std::max(4, std::min(16, pow2_at_least(tu.slice_units.load())));
-    const void *fn = gemv_tiles_fn(type, mode, nc_t, rw);
-    if (!fn && rw != 4) {
+    if (mma) rw = MMA_RW;
+    else if (tu.slice_units.load()) rw = 32 / std::max(4, std::min(16, pow2_at_least(tu.slice_units.load())));
+    const void *fn = mma ? gemv_tiles_mma_fn_q4_K(mode) : gemv_tiles_fn(type, mode, nc_t, rw);
+    if (!fn && rw != 4 && !mma) {
         rw = 4;
         fn = gemv_tiles_fn(type, mode, nc_t, rw);
     }
     if (!fn) return TilePlan::Error;
     const int sc_stride = type == FMT_Q6_K ? act_sc_stride<FMT_Q6_K>() : act_sc_stride<FMT_Q4_K>();
-    const size_t packed = align_up(static_cast<size_t>(nc_t) * U * (ACT_QS_STRIDE + sc_stride), 128);
+    const size_t packed = mma ? align_up(static_cast<size_t>(mma_act_bytes(nc_t, static_cast<int64_t>(U) * 8)), 128)
+                              : align_up(static_cast<size_t>(nc_t) * U * (ACT_QS_STRIDE + sc_stride), 128);
     const size_t raw = align_up(static_cast<size_t>(nc_t) * U * 8 * Q8_1_BYTES, 128);
-    const size_t tb = static_cast<size_t>(tile_bytes_rt(type, rw));
+    // per warp: its ring of tile buffers, plus the row-factor scratch of the tensor-core decode
+    const size_t tb = static_cast<size_t>(tile_bytes_rt(type, rw, mma));
+    const size_t warp_extra = mma ? static_cast<size_t>(MMA_FAC_BYTES) : 0;
     int stages = tu.stages.load() ? tu.stages.load() : 2;
     stages = std::max(1, std::min(TILE_MAX_STAGES, stages));
     int max_wpc = tu.threads.load() ? tu.threads.load() / 32 : TILE_MAX_THREADS / 32;
@@ -276,7 +287,7 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     // bit-identical results).
     const size_t st_smem = static_smem(fn);
     const size_t fn_limit = std::min(dev.smem_limit, dev.smem_limit + SMEM_RESERVE - st_smem);
-    auto need = [&](int w, int st, size_t act) { return act + static_cast<size_t>(w) * st * tb + 128; };
+    auto need = [&](int w, int st, size_t act) { return act + static_cast<size_t>(w) * (st * tb + warp_extra) + 128; };
     auto fit = [&](size_t budget, int &w, int &st) {
         w = max_wpc;
         st = stages;
@@ -309,7 +320,8 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     size_t budget = share_budget(tuned_share ? tu.smem_share.load() : (one_cta ? 1 : 2));
     if (!fit(budget, wpc_f, st_f)) {
         budget = fn_limit;
-        if (!fit(budget, wpc_f, st_f)) return TilePlan::NoFit;
+        if (!fit(budget, wpc_f, st_f))
+            return mma ? plan_tiles(type, mode, dev, p, nc_t, n_potential_experts, L, false) : TilePlan::NoFit;
     } else if (!tuned_share && !is_moe) {
         int wpc_1 = 0, st_1 = 0;
         const int64_t gpc = (G + gx - 1) / gx;  // most row groups a CTA owns
@@ -324,7 +336,7 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     // the raw copy of the q8_1 blocks (coalesced staging) only if it still fits;
     // fp32 input is quantized straight into the packed layout
     size_t act = packed;
-    if (p.xf == nullptr && need(max_wpc, stages, packed + raw) <= budget) act = packed + raw;
+    if (p.xf == nullptr && !mma && need(max_wpc, stages, packed + raw) <= budget) act = packed + raw;
     const int wpc = max_wpc;
     const size_t smem = need(wpc, stages, act);
     if (ensure_smem_attr(dev, fn) != QMV_OK) return TilePlan::Error;
@@ -919,6 +931,14 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles)
     Tuning &t = g_tuning[tidx(type)];
     t.dec_warps = dec_warps;
     t.pre_tiles = pre_tiles;
+    return QMV_OK;
+}
+
+int qmv_set_mma_min_cols(int type, int min_cols)
+{
+    if (!weight_type(type)) return QMV_ERR_TYPE;
+    if (min_cols < 0 || min_cols > 9) return QMV_ERR_SHAPE;
+    g_tuning[tidx(type)].mma_min_cols = min_cols;
     return QMV_OK;
 }
 

@@ -1,5 +1,6 @@
 // GEMV instantiations for q4_K: the tile kernel for every column count and mode
-// (gemv_tiles.cuh), and the generic fallback.
+// (gemv_tiles.cuh), its tensor-core decode (gemv_mma.cuh), and the generic
+// fallback.
 #include "gemv_generic.cuh"
 #include "gemv_tiles.cuh"
 #include "kernels.h"
@@ -7,6 +8,8 @@
 namespace qmv {
 
 const void *gemv_tiles_fn_q4_K(int mode, int nc, int rw) { return tiles_kernel_fn<FMT_Q4_K>(mode, nc, rw); }
+
+const void *gemv_tiles_mma_fn_q4_K(int mode) { return tiles_mma_kernel_fn<FMT_Q4_K>(mode); }
 
 const void *gemv_generic_fn_q4_K(int mode)
 {

@@ -29,6 +29,7 @@
 //     cross-warp traffic).
 #pragma once
 
+#include "gemv_mma.cuh"
 #include "gemv_units.cuh"
 #include "q8_1.cuh"
 
@@ -48,8 +49,11 @@ constexpr int MOE_COL_WEIGHT = 6;   // MoE grid split: an expert's work ~ 6 + th
 //   Q6_K (210-byte units, RW = 4): SS = 1,696 bytes = 32 mod 128, which spreads
 //     the 32 lanes' 32-bit word reads of 2-byte aligned super-blocks over the
 //     banks (at most 2-way, 1.5 on average) and leaves room for the
-//     over-read of the last super-block of a row.
-template <int F, int RW>
+//     over-read of the last super-block of a row;
+//   TC (the tensor-core decode, gemv_mma.cuh; Q4_K, RW = 8): SS = 608 = 96
+//     mod 128, so the 16 lanes of a 64-bit read phase (4 rows x 32 bytes) hit
+//     distinct banks.
+template <int F, int RW, bool TC = false>
 struct TileGeom {
     static constexpr int UW = 32 / RW;
     static constexpr int UNIT = unit_bytes<F>();
@@ -59,13 +63,17 @@ struct TileGeom {
     static constexpr int PIECES = RW * SEG;
     static constexpr int PER_LANE = (PIECES + 31) / 32;
     static constexpr int SS = F == FMT_Q6_K ? UW * UNIT + 16
-                              : (RW == 1 ? UW * UNIT : UW * UNIT + ((8 / RW - UW % 8 + 8) % 8) * 16);
+                              : TC ? UW * UNIT + 32
+                                   : (RW == 1 ? UW * UNIT : UW * UNIT + ((8 / RW - UW % 8 + 8) % 8) * 16);
+    static_assert(!TC || (F == FMT_Q4_K && RW == MMA_RW && SS % 128 == 96), "tensor-core tiles: Q4_K, 8 rows");
     static constexpr int TB = RW * SS;
 };
 
-// Host-visible geometry: bytes of one tile buffer (0: no such tile).
-inline int tile_bytes_rt(int type, int rw)
+// Host-visible geometry: bytes of one tile buffer (0: no such tile); tc: the
+// tensor-core tiles.
+inline int tile_bytes_rt(int type, int rw, bool tc = false)
 {
+    if (tc) return (type == FMT_Q4_K && rw == MMA_RW) ? TileGeom<FMT_Q4_K, MMA_RW, true>::TB : 0;
     if (type == FMT_Q6_K) return rw == 4 ? TileGeom<FMT_Q6_K, 4>::TB : 0;
     switch (rw) {
     case 2: return TileGeom<FMT_Q4_K, 2>::TB;
@@ -220,7 +228,7 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
     }
 }
 
-template <int F, int NC, int MODE, int RW>
+template <int F, int NC, int MODE, int RW, bool TC = false>
 __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEBUG) ? 2 : 1)
     gemv_tiles_kernel(const GemvParams p)
 {
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     __shared__ uint32_t s_slots[8];
     __shared__ int s_cnt;
 
-    using G = TileGeom<F, RW>;
+    using G = TileGeom<F, RW, TC>;
     constexpr int UW = G::UW;                        // units per tile row
     constexpr int SEG = G::SEG;                      // 16-byte pieces per tile row
     constexpr int SS = G::SS;                        // shared bytes per tile row
@@ -238,6 +246,8 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     constexpr int UNIT = G::UNIT;                    // bytes per unit
     constexpr bool IS_MOE = MODE == MODE_MOE || MODE == MODE_MOE_GATE;
     constexpr int NM = (MODE == MODE_GATE || MODE == MODE_MOE_GATE) ? 2 : 1;  // matrices (up, gate)
+    constexpr bool MMA = TC;  // tensor-core decode (gemv_mma.cuh): Q4_K, plain, up to 8 columns
+    static_assert(!MMA || (F == FMT_Q4_K && MODE == MODE_PLAIN && NC == MMA_COLS), "tensor-core tiles: Q4_K plain");
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = p.dec_warps;  // warps that stream and decode; the others only help staging
@@ -389,7 +399,10 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     const int64_t my_groups = warp < nwarps ? ((gwarp + 1) * p.n_groups) / wtot - g_begin : 0;
     const int64_t total = my_groups * n_kt * NM;
 
-    const uint32_t ring = smem_u32(smem + p.act_bytes) + static_cast<uint32_t>(min(warp, nwarps - 1) * stages * TB);
+    // this warp's ring of tile buffers (tensor-core decode: then its row-factor scratch)
+    constexpr int WARP_EXTRA = MMA ? MMA_FAC_BYTES : 0;
+    const uint32_t ring =
+        smem_u32(smem + p.act_bytes) + static_cast<uint32_t>(min(warp, nwarps - 1) * (stages * TB + WARP_EXTRA));
 
     // ---- copies: tile (group, k-tile, matrix) -> ring buffer, one group per tile ----
     int64_t ld_g = g_begin;
@@ -424,6 +437,8 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
     if constexpr (IS_MOE)
         stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; }, 0u, 1u);
+    else if constexpr (MMA)
+        stage_mma_activations(p, smem, n_active, [](int c) { return c; }, crank, ncta);
     else
         stage_tile_activations<F, NC>(p, smem, n_active, [](int c) { return c; }, crank, ncta);
     if (ncta > 1) {
@@ -445,6 +460,15 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         for (int c = 0; c < NC; ++c) acc[m][c] = 0.f;
 
     float b_up = 0.f, b_gate = 0.f;  // this lane's row biases (lanes of unit 0)
+    // tensor-core decode: lane 4*mg + mt owns y[column mg][rows 2mt, 2mt + 1 of the group]
+    const int mg = lane >> 2, mt = lane & 3;
+    const uint32_t m_cs = MMA ? static_cast<uint32_t>(mma_col_stride(U * 8)) : 0u;
+    const uint32_t m_ss = MMA ? static_cast<uint32_t>(mma_sc_stride(U * 8)) : 0u;
+    const uint32_t m_act = act_qs + static_cast<uint32_t>(mg) * m_cs + 16u * mt;  // column mg, lane part mt
+    const uint32_t m_scl = act_qs + static_cast<uint32_t>(p.ncols) * m_cs + static_cast<uint32_t>(mg) * m_ss;
+    const uint32_t m_fac = ring + static_cast<uint32_t>(stages * TB);  // this warp's row-factor scratch
+    float mv[2] = {0.f, 0.f};
+    float mb[2] = {0.f, 0.f};  // biases of rows 2mt, 2mt + 1
     int64_t cg = g_begin;  // compute position
     int ckt = 0, cm = 0, cbuf = 0;
     for (int64_t t = 0; t < total; ++t) {
@@ -453,6 +477,28 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 
         const int64_t row = cg * RW + r_l;
         const int u = ckt * UW + u_l;
+        if constexpr (MMA) {
+            // every lane takes part in the mma (rows past M compute on stale
+            // tile bytes and are not written); units past the row are skipped
+            // by the whole warp
+            const int64_t r0 = cg * RW + 2 * mt;
+            if (ckt == 0 && p.bias) {
+                mb[0] = r0 < p.M ? ld_nc_f32(p.bias + r0) : 0.f;
+                mb[1] = r0 + 1 < p.M ? ld_nc_f32(p.bias + r0 + 1) : 0.f;
+            }
+            const uint32_t tb = ring + static_cast<uint32_t>(cbuf * TB);
+            mma_row_factors_q4_K<G::SS, UNIT>(tb, m_fac, lane);
+            __syncwarp();  // the factors are in the scratch
+            const uint32_t wrow = tb + static_cast<uint32_t>(mg * G::SS + 16 + 8 * mt);
+#pragma unroll
+            for (int i = 0; i < UW; ++i) {
+                const int um = ckt * UW + i;
+                const uint32_t fu = m_fac + static_cast<uint32_t>(i * (RW * MMA_FAC_ROW) + 2 * mt * MMA_FAC_ROW);
+                if (um < U)
+                    mma_unit_q4_K(wrow + i * UNIT, m_act + static_cast<uint32_t>(um * 8 * MMA_BLK_BYTES),
+                                  m_scl + static_cast<uint32_t>(um * 8 * 8), mg < n_active, fu, fu + MMA_FAC_ROW, mv);
+            }
+        } else {
         if constexpr (MODE == MODE_PLAIN || MODE == MODE_GATE) {
             // the row's biases (after the dependency wait; nothing writes them while
             // this kernel runs), requested at the group's first tile so that its
@@ -483,11 +529,21 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
                 }
             }
         }
+        }  // dp4a decode
         __syncwarp();  // every lane is done with the buffer
         if (issued < total) issue_tile();
 
         const bool group_done = (ckt == n_kt - 1) && (cm == NM - 1);
-        if constexpr (MODE != MODE_DEBUG) {
+        if constexpr (MMA) {
+            if (group_done) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int64_t r = cg * RW + 2 * mt + k;
+                    if (r < p.M && mg < n_active) p.y[(size_t)mg * p.ldy + r] = p.bias ? mv[k] + mb[k] : mv[k];
+                    mv[k] = 0.f;
+                }
+            }
+        } else if constexpr (MODE != MODE_DEBUG) {
             if (group_done) {
                 // the lanes of one row are those with the same r_l (xor over the unit bits)
 #pragma unroll
@@ -538,7 +594,17 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 
 // Kernel table of the tile path for one format (instantiated only in that
 // format's translation unit).  RW = 4 serves every mode and column count;
-// for Q4_0 / Q4_K, RW = 2 and 8 exist for one plain column, for geometry sweeps.
+// for Q4_0 / Q4_K, RW = 2 and 8 exist for one plain column, for geometry sweeps;
+// the tensor-core decode (TC) of the plain Q4_K GEMV takes 1..8 columns.
+template <int F>
+const void *tiles_mma_kernel_fn(int mode)
+{
+    if constexpr (F == FMT_Q4_K)
+        if (mode == MODE_PLAIN)
+            return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, MMA_COLS, MODE_PLAIN, MMA_RW, true>);
+    return nullptr;
+}
+
 template <int F>
 const void *tiles_kernel_fn(int mode, int nc, int rw)
 {

@@ -136,6 +136,10 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_set_stream_tuning(12, -1, 0) == 3
     assert L.qmv_set_stream_tuning(9, 0, 0) == 2
     assert L.qmv_set_stream_tuning(12, 0, 0) == 0
+    assert L.qmv_set_mma_min_cols(12, 10) == 3
+    assert L.qmv_set_mma_min_cols(12, -1) == 3
+    assert L.qmv_set_mma_min_cols(9, 0) == 2
+    assert L.qmv_set_mma_min_cols(12, 0) == 0
 
 
 def test_checked_mode_runs_after_the_argument_checks(qlib):
