@@ -716,6 +716,7 @@ def run_kernel_only(args):
     import quantized_decode_gemv_qmv_gb300 as q
 
     torch.cuda.set_device(0)
+    q.set_mma_min_cols(Q4_K, args.mma_min_cols)
     kinds = {name: (M, K, nmat) for name, M, K, nmat in STEP}
     shapes = dict(SHAPES, **{"14336x4096": (14336, 4096)})
     nc = args.ncols
@@ -757,6 +758,8 @@ def main():
     ap.add_argument("--kernel-only", default=None, help="profiling aid: only GEMV launches of one shape or step kind")
     ap.add_argument("--launches", type=int, default=8)
     ap.add_argument("--ncols", type=int, default=1, help="profiling aid: activation columns of a --kernel-only shape")
+    ap.add_argument("--mma-min-cols", type=int, default=0,
+                    help="profiling aid: columns from which --kernel-only uses the tensor-core decode (0: default)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
