@@ -344,8 +344,10 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     // fp32 input: clusters of CTAs share the quantization of the activations
     // (the grid becomes a whole number of clusters; CTAs without row groups
     // still take their share); one CTA per cluster if no such cluster fits
+    // The tensor-core decode shares its staging (a conversion of every block of
+    // every column) the same way, from q8_1 input too.
     int cl = 1;
-    if (p.xf != nullptr && (mode == MODE_PLAIN || mode == MODE_GATE)) {
+    if ((p.xf != nullptr || mma) && (mode == MODE_PLAIN || mode == MODE_GATE)) {
         cl = tu.cluster.load() ? tu.cluster.load() : F32_CLUSTER;
         cl = std::max(1, std::min(MAX_CLUSTER, cl));
         if (cl > 1) {
