@@ -91,15 +91,22 @@ def test_fullsize_gemv_ncols1(q, name, t, M, K, outl):
 
 
 def test_fullsize_q4_K_small_batch_sweep(q):
+    """The column sweep the benchmark times, with both decodes: per-column
+    dp4a (the default) and the tensor-core decode (forced from one column)."""
     t, M, K = oracle.Q4_K, 14336, 4096
     W, Wd = quantized(q, t, M, K, seed=4141)
     rows = sample_rows(M, 19)
     for ncols in range(1, 9):
         x = synthetic.activations_f32(20 + ncols, ncols, K)
         xq_ref = oracle.quantize_q8_1(x)
-        y = host(q.mul_mat_vec(t, Wd, M, K, dev(xq_ref), ncols))
         y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq_ref, ncols, rows=rows)
-        assert np.all(np.abs(y[:, rows] - y_ref) <= TOL * l1), ncols
+        for min_cols in (0, 1):
+            q.set_mma_min_cols(t, min_cols)
+            try:
+                y = host(q.mul_mat_vec(t, Wd, M, K, dev(xq_ref), ncols))
+            finally:
+                q.set_mma_min_cols(t, 0)
+            assert np.all(np.abs(y[:, rows] - y_ref) <= TOL * l1), (ncols, min_cols)
 
 
 def test_fullsize_fused_gate_up(q):
