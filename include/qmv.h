@@ -32,12 +32,15 @@
  *     path with identical results.
  *   - Threads: calls are thread-safe; the tuning overrides below are
  *     process-wide.
- *   - Waits: the kernels contain no spin-waits.  Weight copies (cp.async)
- *     complete in hardware and are awaited with cp.async.wait_group; the
- *     only other synchronisation is __syncwarp/__syncthreads inside a CTA and
- *     the programmatic-dependent-launch wait on the previous grid.
- *     qmv_device_fault() reads a sticky device word reserved for faults a
- *     kernel detects itself; the current kernels never set it.
+ *   - Waits: weight copies (cp.async) complete in hardware and are awaited
+ *     with cp.async.wait_group; CTAs synchronise with __syncwarp /
+ *     __syncthreads, cluster barriers and the programmatic-dependent-launch
+ *     wait on the previous grid.  The one spin-wait is bounded: the fp32-input
+ *     plain and gate/up calls, whose clusters of CTAs share the quantization
+ *     of the activations, wait on an mbarrier for the partners' shares for at
+ *     most one second; past that the kernel records code 2 in the sticky
+ *     device fault word (qmv_device_fault) and finishes with invalid outputs
+ *     instead of hanging.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -238,8 +241,10 @@ int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const
                             int ncols, int32_t *out, void *stream);
 
 /* Reads and clears the sticky device fault word of the current device: 0 if
- * no kernel's bounded wait has run out since the last call, else a nonzero
- * code.  Synchronous (waits for the device). */
+ * no kernel's bounded wait has run out since the last call, else the OR of
+ * nonzero codes (2: a cluster partner's share of the staged fp32 activations
+ * did not arrive within the wait limit; that launch's outputs are invalid).
+ * Synchronous (waits for the device). */
 int qmv_device_fault(unsigned int *code);
 
 /* ---- tuning (process-wide) -----------------------------------------------------

@@ -356,6 +356,7 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
             else cl = 1;
         }
     }
+    p.fault = dev.fault;
     p.units_per_row = U;
     p.n_groups = G;
     p.stages = stages;

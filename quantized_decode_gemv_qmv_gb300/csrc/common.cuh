@@ -37,7 +37,8 @@ enum Fmt { FMT_Q4_0 = 2, FMT_Q4_K = 12, FMT_Q6_K = 14 };
 // Fault codes written to the sticky device word when a bounded wait runs out.
 enum FaultCode : unsigned int {
     FAULT_NONE = 0,
-    FAULT_WAIT_TIMEOUT = 1,  // a pipeline slot never completed
+    FAULT_WAIT_TIMEOUT = 1,     // a pipeline slot never completed
+    FAULT_CLUSTER_STAGING = 2,  // a cluster partner's share of the staged activations never arrived
 };
 
 // How long a kernel waits on one mbarrier phase before giving up (ns).  A
@@ -334,6 +335,23 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v)
 __device__ __forceinline__ void st_cluster_v2(uint32_t a, uint32_t v0, uint32_t v1)
 {
     asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(v0), "r"(v1) : "memory");
+}
+
+// Stores into another CTA's shared memory (cluster address a) whose byte count
+// completes on that CTA's mbarrier (cluster address bar): the receiver waits
+// for the bytes it expects instead of a cluster-wide barrier.
+__device__ __forceinline__ void st_async_u32(uint32_t a, uint32_t v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(a), "r"(v),
+                 "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_v2(uint32_t a, uint32_t v0, uint32_t v1, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(a),
+                 "r"(v0), "r"(v1), "r"(bar)
+                 : "memory");
 }
 
 // Split cluster barrier (every thread of every CTA of the cluster arrives, then

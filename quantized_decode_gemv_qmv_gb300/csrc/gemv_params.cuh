@@ -22,6 +22,7 @@ struct GemvParams {
     const float *bias;       // PLAIN/GATE: [M] added to every column's (up) output (nullable)
     const float *gate_bias;  // GATE: [M] added to the gate output before silu (nullable)
     float *y_shared;         // MOE with a shared expert (W2): y_shared[t*M + r] = (W2 x_t)[r]
+    unsigned int *fault;     // sticky device word: kernels OR in a code when a bounded wait runs out
     int64_t M;
     int64_t ldy;
     int64_t row_bytes;

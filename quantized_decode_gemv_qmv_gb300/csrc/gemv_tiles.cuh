@@ -102,7 +102,7 @@ inline int tile_bytes_rt(int type, int rw, bool tc = false)
 // exchange with a cluster barrier.
 template <int F, int NC, typename ColFn>
 __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint8_t *smem, int n_active, ColFn src_col,
-                                                       uint32_t crank, uint32_t ncta)
+                                                       uint32_t crank, uint32_t ncta, uint32_t xbar)
 {
     if (p.xf != nullptr) {
         const int U = p.units_per_row;
@@ -161,13 +161,23 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
                             if (i < nw) asm volatile("st.shared.u32 [%0], %1;" ::"r"(sc + off[i]), "r"(val[i]) : "memory");
                     }
                 } else {
+                    // this CTA's copy directly; the others' through st.async,
+                    // counted on their mbarrier (cluster_share_bytes per block)
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dq), "r"(w0), "r"(w1) : "memory");
+                    if (j == 0) {
+#pragma unroll
+                        for (int i = 0; i < 3; ++i)
+                            if (i < nw) asm volatile("st.shared.u32 [%0], %1;" ::"r"(sc + off[i]), "r"(val[i]) : "memory");
+                    }
                     for (uint32_t q = 0; q < ncta; ++q) {
-                        st_cluster_v2(mapa_shared(dq, q), w0, w1);
+                        if (q == crank) continue;
+                        const uint32_t bq = mapa_shared(xbar, q);
+                        st_async_v2(mapa_shared(dq, q), w0, w1, bq);
                         if (j == 0) {
                             const uint32_t scq = mapa_shared(sc, q);
 #pragma unroll
                             for (int i = 0; i < 3; ++i)
-                                if (i < nw) st_cluster_u32(scq + off[i], val[i]);
+                                if (i < nw) st_async_u32(scq + off[i], val[i], bq);
                         }
                     }
                 }
@@ -228,6 +238,19 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
     }
 }
 
+// Bytes the other CTAs of a cluster store into this CTA's shared memory while
+// staging fp32 input (stage_tile_activations): every block of their shares of
+// the n_all blocks, as 4 lanes x 8 bytes of codes plus the block's scalar
+// words (act_scalar_words: 2, or 3 for Q6_K).
+template <int F>
+__device__ __forceinline__ uint32_t cluster_share_bytes(int n_all, uint32_t crank, uint32_t ncta)
+{
+    const int blk0 = static_cast<int>(static_cast<int64_t>(crank) * n_all / ncta);
+    const int blk1 = static_cast<int>(static_cast<int64_t>(crank + 1) * n_all / ncta);
+    constexpr int per_block = 4 * 8 + 4 * (F == FMT_Q6_K ? 3 : 2);
+    return static_cast<uint32_t>((n_all - (blk1 - blk0)) * per_block);
+}
+
 template <int F, int NC, int MODE, int RW, bool TC = false>
 __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEBUG) ? 2 : 1)
     gemv_tiles_kernel(const GemvParams p)
@@ -262,10 +285,16 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     // fp32 input in a cluster: the CTAs share the quantization (see
     // stage_tile_activations); this arrive lets the others know this CTA runs
     uint32_t crank = 0, ncta = 1;
+    __shared__ __align__(8) uint64_t s_xbar;  // fp32 staging in a cluster: the partners' shares arrive here
+    const uint32_t xbar = smem_u32(&s_xbar);
     if constexpr (MODE == MODE_PLAIN || MODE == MODE_GATE) {
         ncta = cluster_nctarank();
         if (ncta > 1) {
             crank = cluster_ctarank();
+            if (!MMA && threadIdx.x == 0) {
+                mbar_init(xbar, 1);
+                fence_mbar_init();  // visible to the partners before they pass the cluster wait below
+            }
             cluster_arrive_relaxed();
         }
     }
@@ -435,15 +464,24 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     while (issued < total && issued < p.pre_tiles) issue_tile();  // weights first
     if constexpr (!IS_MOE) pdl_wait();
     if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
+    if (!MMA && ncta > 1 && threadIdx.x == 0)
+        mbar_arrive_expect_tx(xbar, cluster_share_bytes<F>(p.ncols * p.units_per_row * 8, crank, ncta));
     if constexpr (IS_MOE)
-        stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; }, 0u, 1u);
+        stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; }, 0u, 1u, 0u);
     else if constexpr (MMA)
         stage_mma_activations(p, smem, n_active, [](int c) { return c; }, crank, ncta);
     else
-        stage_tile_activations<F, NC>(p, smem, n_active, [](int c) { return c; }, crank, ncta);
-    if (ncta > 1) {
+        stage_tile_activations<F, NC>(p, smem, n_active, [](int c) { return c; }, crank, ncta, xbar);
+    if (ncta > 1 && MMA) {
         cluster_arrive();  // this CTA's share is stored everywhere ...
         cluster_wait();    // ... and every share is here; no remote access after this point
+    } else if (ncta > 1) {
+        // this CTA's own share is here after the CTA barrier; the partners'
+        // shares once their bytes have completed on the mbarrier (every byte
+        // a partner stores here is counted, so none is still in flight after
+        // the wait and no CTA can exit while a partner writes to it)
+        __syncthreads();
+        if (!mbar_wait_bounded(xbar, 0) && threadIdx.x == 0 && p.fault) atomicOr(p.fault, FAULT_CLUSTER_STAGING);
     } else {
         __syncthreads();
     }
