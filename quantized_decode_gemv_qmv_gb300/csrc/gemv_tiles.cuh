@@ -285,8 +285,15 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     // fp32 input in a cluster: the CTAs share the quantization (see
     // stage_tile_activations); this arrive lets the others know this CTA runs
     uint32_t crank = 0, ncta = 1;
-    __shared__ __align__(8) uint64_t s_xbar;  // fp32 staging in a cluster: the partners' shares arrive here
-    const uint32_t xbar = smem_u32(&s_xbar);
+    // fp32 staging in a cluster: the partners' shares complete on this
+    // mbarrier.  It sits right after the used dynamic area (activations, then
+    // every decoding warp's ring and scratch), inside the 128 bytes of
+    // alignment slack the host adds: the slack before `smem` is a multiple of
+    // 16 below 128, so at least 16 bytes of it remain after the used area.
+    // (Static shared memory would cost the whole CTA 128 bytes of budget.)
+    constexpr int WARP_EXTRA = MMA ? MMA_FAC_BYTES : 0;
+    const uint32_t xbar =
+        smem_u32(smem) + p.act_bytes + static_cast<uint32_t>(p.dec_warps * (p.stages * TB + WARP_EXTRA));
     if constexpr (MODE == MODE_PLAIN || MODE == MODE_GATE) {
         ncta = cluster_nctarank();
         if (ncta > 1) {
@@ -429,7 +436,6 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     const int64_t total = my_groups * n_kt * NM;
 
     // this warp's ring of tile buffers (tensor-core decode: then its row-factor scratch)
-    constexpr int WARP_EXTRA = MMA ? MMA_FAC_BYTES : 0;
     const uint32_t ring =
         smem_u32(smem + p.act_bytes) + static_cast<uint32_t>(min(warp, nwarps - 1) * (stages * TB + WARP_EXTRA));
 
