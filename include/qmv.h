@@ -72,8 +72,9 @@ typedef enum {
     QMV_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
     QMV_ERR_IDS = 7,          /* reserved: invalid expert ids are reported through dev_status */
     QMV_ERR_DEVICE_FAULT = 8, /* a kernel's bounded wait ran out (see qmv_device_fault) */
-    QMV_ERR_RANGE = 9         /* checked mode: an argument's byte range is not inside one device
+    QMV_ERR_RANGE = 9,        /* checked mode: an argument's byte range is not inside one device
                                  allocation (see qmv_set_checked) */
+    QMV_ERR_CONFIG = 10       /* the QMV_GEOM environment override is malformed or out of range */
 } qmv_status;
 
 /* Human-readable name of a status code (static storage). */
@@ -290,6 +291,16 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
  * stay bit-identical to each other at every setting.  Returns QMV_ERR_TYPE for
  * a non-weight type, QMV_ERR_SHAPE for values out of range. */
 int qmv_set_mma_min_cols(int type, int min_cols);
+
+/* Environment override of the geometry knobs above, for tuning runs:
+ * QMV_GEOM="type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K
+ * and keys threads, slice_units, stages, ctas_per_sm, smem_share, cluster,
+ * dec_warps, pre_tiles and mma_min_cols (the arguments of qmv_set_tuning,
+ * qmv_set_stream_tuning and qmv_set_mma_min_cols, same ranges).  It is read
+ * once, before the first GEMV-family call is planned, and applied through
+ * those setters; later setter calls override it.  A malformed spec or an
+ * out-of-range value makes every GEMV-family call return QMV_ERR_CONFIG
+ * (nothing is launched) for the life of the process. */
 
 /* Enables (1, default) or disables (0) programmatic dependent launch for the
  * library's q8_1 and GEMV kernels.  When enabled, a GEMV may start streaming

@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <map>
 #include <mutex>
+#include <string>
 #include <tuple>
 
 #include "../../include/qmv.h"
@@ -92,8 +93,78 @@ struct DevInfo {
     unsigned int *fault;
 };
 
+// ---- QMV_GEOM: launch-geometry overrides from the environment (tuning) ----
+// "type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K and keys
+// threads, slice_units, stages, ctas_per_sm, smem_share, cluster (as for
+// qmv_set_tuning), dec_warps, pre_tiles (qmv_set_stream_tuning) and
+// mma_min_cols (qmv_set_mma_min_cols).  Read once, before the first GEMV call
+// is planned; values go through the setters' range checks.
+std::once_flag g_geom_once;
+std::atomic<int> g_geom_status{QMV_OK};
+
+bool parse_int(const std::string &s, int &v)
+{
+    if (s.empty() || s.size() > 9) return false;
+    char *end = nullptr;
+    const long x = strtol(s.c_str(), &end, 10);
+    if (end != s.c_str() + s.size()) return false;
+    v = static_cast<int>(x);
+    return true;
+}
+
+bool apply_geom_entry(const std::string &entry)
+{
+    const size_t colon = entry.find(':');
+    if (colon == std::string::npos) return false;
+    const std::string tname = entry.substr(0, colon);
+    const int type = tname == "q4_0" ? FMT_Q4_0 : tname == "q4_K" ? FMT_Q4_K : tname == "q6_K" ? FMT_Q6_K : -1;
+    if (type < 0) return false;
+    const Tuning &cur = g_tuning[tidx(type)];
+    int v[9] = {cur.threads.load(),     cur.slice_units.load(), cur.stages.load(),
+                cur.ctas_per_sm.load(), cur.smem_share.load(),  cur.cluster.load(),
+                cur.dec_warps.load(),   cur.pre_tiles.load(),   cur.mma_min_cols.load()};
+    static const char *const keys[9] = {"threads",    "slice_units", "stages",    "ctas_per_sm", "smem_share",
+                                        "cluster",    "dec_warps",   "pre_tiles", "mma_min_cols"};
+    size_t pos = colon + 1;
+    while (pos <= entry.size()) {
+        size_t comma = entry.find(',', pos);
+        if (comma == std::string::npos) comma = entry.size();
+        const std::string kv = entry.substr(pos, comma - pos);
+        const size_t eq = kv.find('=');
+        if (eq == std::string::npos) return false;
+        int k = 0;
+        while (k < 9 && kv.compare(0, eq, keys[k]) != 0) ++k;
+        if (k == 9 || !parse_int(kv.substr(eq + 1), v[k])) return false;
+        pos = comma + 1;
+    }
+    return qmv_set_tuning(type, v[0], v[1], v[2], v[3], v[4], v[5]) == QMV_OK &&
+           qmv_set_stream_tuning(type, v[6], v[7]) == QMV_OK && qmv_set_mma_min_cols(type, v[8]) == QMV_OK;
+}
+
+qmv_status geom_env()
+{
+    std::call_once(g_geom_once, [] {
+        const char *e = getenv("QMV_GEOM");
+        if (!e || !*e) return;
+        const std::string spec(e);
+        size_t pos = 0;
+        while (pos <= spec.size()) {
+            size_t semi = spec.find(';', pos);
+            if (semi == std::string::npos) semi = spec.size();
+            if (semi > pos && !apply_geom_entry(spec.substr(pos, semi - pos))) {
+                g_geom_status = QMV_ERR_CONFIG;
+                return;
+            }
+            pos = semi + 1;
+        }
+    });
+    return static_cast<qmv_status>(g_geom_status.load());
+}
+
 qmv_status device_info(DevInfo &d)
 {
+    const qmv_status g = geom_env();
+    if (g != QMV_OK) return g;
     if (cudaGetDevice(&d.dev) != cudaSuccess) return QMV_ERR_CUDA;
     if (d.dev < 0 || d.dev >= MAX_DEVICES) return QMV_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -587,6 +658,7 @@ const char *qmv_status_str(int s)
     case QMV_ERR_IDS: return "invalid expert id";
     case QMV_ERR_DEVICE_FAULT: return "device wait timed out";
     case QMV_ERR_RANGE: return "argument outside its device allocation";
+    case QMV_ERR_CONFIG: return "malformed or out-of-range QMV_GEOM override";
     default: return "unknown status";
     }
 }
