@@ -56,7 +56,7 @@ MMA_MIN_COLS = 9
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "19a422eaed810ef6", "bytes_per_launch": 28531360,
+TRAFFIC = {"csrc_sha": "fdd3aa50156014be", "bytes_per_launch": 28530304,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down (profiles/gemv_tiles_q4_K_down_fused.md)"}
 
 

@@ -292,6 +292,28 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
  * a non-weight type, QMV_ERR_SHAPE for values out of range. */
 int qmv_set_mma_min_cols(int type, int min_cols);
 
+/* The launch the library would make for a plain (gate_up = 0) or fused
+ * gate/up SwiGLU (gate_up = 1) GEMV of `type` with M rows, K columns and
+ * ncols activation columns, from q8_1 (fp32_input = 0) or fp32 input
+ * (fp32_input = 1), on the current device with the current tuning: weights
+ * and activations are taken as 16-byte aligned.  Nothing is launched and no
+ * memory is touched.  Fills *info; returns the status the GEMV call itself
+ * would return for these shapes (QMV_ERR_NULL if info is NULL). */
+typedef struct {
+    int tile_kernel;    /* 1: the streaming tile kernel; 0: the generic kernel */
+    int tensor_cores;   /* 1: the tensor-core decode (qmv_set_mma_min_cols) */
+    int rows_per_tile;  /* weight rows per warp tile (tile kernel) */
+    int grid;           /* CTAs */
+    int block;          /* threads per CTA */
+    int cluster;        /* CTAs per cluster (1: none) */
+    int stages;         /* tile buffers per decoding warp (tile kernel) */
+    int dec_warps;      /* warps per CTA that stream and decode (tile kernel) */
+    int pre_tiles;      /* tiles per warp requested before the dependency wait */
+    size_t smem;        /* dynamic shared bytes per CTA */
+} qmv_launch_info;
+int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, int fp32_input,
+                      qmv_launch_info *info);
+
 /* Environment override of the geometry knobs above, for tuning runs:
  * QMV_GEOM="type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K
  * and keys threads, slice_units, stages, ctas_per_sm, smem_share, cluster,

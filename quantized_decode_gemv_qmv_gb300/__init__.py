@@ -30,8 +30,15 @@ EXPORTS = (
     "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32", "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32",
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
-    "qmv_set_checked", "qmv_set_mma_min_cols",
+    "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
 )
+
+
+class LaunchInfo(ctypes.Structure):
+    """qmv_launch_info of include/qmv.h."""
+    _fields_ = [(n, ctypes.c_int) for n in ("tile_kernel", "tensor_cores", "rows_per_tile", "grid", "block",
+                                            "cluster", "stages", "dec_warps", "pre_tiles")] + \
+               [("smem", ctypes.c_size_t)]
 
 
 class QmvError(RuntimeError):
@@ -86,12 +93,13 @@ def lib():
         L.qmv_set_pdl.argtypes = [_int]
         L.qmv_set_checked.argtypes = [_int]
         L.qmv_set_mma_min_cols.argtypes = [_int, _int]
+        L.qmv_describe_gemv.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.POINTER(LaunchInfo)]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
                      "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_mul_mat_vec_fused",
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
-                     "qmv_set_checked", "qmv_set_mma_min_cols"):
+                     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -340,6 +348,14 @@ def set_tuning(qtype: int, threads: int = 0, slice_units: int = 0, stages: int =
 def set_stream_tuning(qtype: int, dec_warps: int = 0, pre_tiles: int = 0):
     """Decoding warps per CTA and tiles per warp requested before the dependency wait (0: default)."""
     _check("qmv_set_stream_tuning", lib().qmv_set_stream_tuning(qtype, dec_warps, pre_tiles))
+
+
+def describe_gemv(qtype: int, M: int, K: int, ncols: int = 1, gate_up: bool = False, fp32_input: bool = False):
+    """The launch geometry the library would use for this GEMV (nothing is launched), as a dict."""
+    info = LaunchInfo()
+    _check("qmv_describe_gemv", lib().qmv_describe_gemv(qtype, 1 if gate_up else 0, M, K, ncols,
+                                                       1 if fp32_input else 0, ctypes.byref(info)))
+    return {name: getattr(info, name) for name, _ in LaunchInfo._fields_}
 
 
 def set_mma_min_cols(qtype: int, min_cols: int = 0):

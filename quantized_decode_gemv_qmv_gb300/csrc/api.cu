@@ -269,6 +269,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Launch {
     const void *fn = nullptr;
     bool stream = false;
+    int rw = 0;       // tile kernel: weight rows per warp tile
     int cluster = 1;  // CTAs per cluster (1: no cluster dimension)
     GemvParams p{};
     dim3 grid, block;
@@ -448,6 +449,7 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
     L.fn = fn;
     L.stream = true;
+    L.rw = rw;
     L.cluster = cl;
     L.p = p;
     L.block = dim3(static_cast<unsigned>(cta_warps * 32));
@@ -1006,6 +1008,45 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles)
     Tuning &t = g_tuning[tidx(type)];
     t.dec_warps = dec_warps;
     t.pre_tiles = pre_tiles;
+    return QMV_OK;
+}
+
+int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, int fp32_input, qmv_launch_info *info)
+{
+    if (!info) return QMV_ERR_NULL;
+    *info = qmv_launch_info{};
+    // stand-in addresses, 256-byte aligned: only their alignment is looked at
+    const void *W = reinterpret_cast<const void *>(uintptr_t(1) << 20);
+    const void *W2 = reinterpret_cast<const void *>(uintptr_t(2) << 20);
+    const void *act = reinterpret_cast<const void *>(uintptr_t(3) << 20);
+    float *y = reinterpret_cast<float *>(uintptr_t(4) << 20);
+    qmv_status s = check_common(type, W, M, K, act, y);
+    if (s != QMV_OK) return s;
+    if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    if (fp32_input && (s = check_f32(type, W, gate_up ? W2 : nullptr, K, K)) != QMV_OK) return s;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W, M, K, fp32_input ? nullptr : act, ncols);
+    if (fp32_input) {
+        p.xf = static_cast<const float *>(act);
+        p.ldx = K;
+    }
+    if (gate_up) p.W2 = static_cast<const uint8_t *>(W2);
+    p.y = y;
+    const int mode = gate_up ? MODE_GATE : MODE_PLAIN;
+    Launch L;
+    s = fp32_input ? plan_f32(type, mode, dev, p, ncols, 1, L) : plan(type, mode, dev, p, ncols, 1, L);
+    if (s != QMV_OK) return s;
+    info->tile_kernel = L.stream ? 1 : 0;
+    info->tensor_cores = (L.stream && type == FMT_Q4_K && L.fn == gemv_tiles_mma_fn_q4_K(mode)) ? 1 : 0;
+    info->rows_per_tile = L.stream ? L.rw : 0;
+    info->grid = static_cast<int>(L.grid.x * L.grid.y);
+    info->block = static_cast<int>(L.block.x);
+    info->cluster = L.cluster;
+    info->stages = L.stream ? L.p.stages : 0;
+    info->dec_warps = L.stream ? L.p.dec_warps : 0;
+    info->pre_tiles = L.stream ? L.p.pre_tiles : 0;
+    info->smem = L.smem;
     return QMV_OK;
 }
 

@@ -140,6 +140,12 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_set_mma_min_cols(12, -1) == 3
     assert L.qmv_set_mma_min_cols(9, 0) == 2
     assert L.qmv_set_mma_min_cols(12, 0) == 0
+    info = qlib.LaunchInfo()
+    assert L.qmv_describe_gemv(12, 0, 16, 4096, 1, 0, None) == 1
+    assert L.qmv_describe_gemv(12, 0, 16, 250, 1, 0, ctypes.byref(info)) == 3
+    assert L.qmv_describe_gemv(12, 0, 16, 4096, 9, 0, ctypes.byref(info)) == 4
+    assert L.qmv_describe_gemv(5, 0, 16, 4096, 1, 0, ctypes.byref(info)) == 2
+    assert L.qmv_describe_gemv(14, 0, 16, 2304, 1, 1, ctypes.byref(info)) == 3  # fp32 input: Q6_K K % 2048
 
 
 def test_checked_mode_runs_after_the_argument_checks(qlib):
