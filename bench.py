@@ -56,7 +56,7 @@ MMA_MIN_COLS = 9
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "fdd3aa50156014be", "bytes_per_launch": 28530304,
+TRAFFIC = {"csrc_sha": "ae05bef92d3b3fe6", "bytes_per_launch": 28530112,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down (profiles/gemv_tiles_q4_K_down_fused.md)"}
 
 
@@ -267,11 +267,13 @@ def run_reference(args):
 
 
 # ---- GPU arm ------------------------------------------------------------------------
-def measure_ceilings(torch, stream, device, reps=10):
+def measure_ceilings(q, torch, stream, device, reps=10):
     """Diagnostic bandwidth ceilings of this GPU, measured here with CUDA events:
     a device-to-device copy of 2 GB (cudaMemcpyAsync through torch's copy_,
-    counted as read + write bytes) and a read-only reduction over 4 GB (torch
-    sum).  The roofline denominator stays the measured copy figure."""
+    counted as read + write bytes), a read-only reduction over 4 GB (torch
+    sum), and this library's read probe over the same 4 GB (the GEMV weight
+    stream's 128-bit L2-only loads).  The roofline denominator stays the
+    measured copy figure."""
     n = 2 << 30
     src = torch.empty(n, dtype=torch.uint8, device=device)
     dst = torch.empty(n, dtype=torch.uint8, device=device)
@@ -297,8 +299,17 @@ def measure_ceilings(torch, stream, device, reps=10):
         e1.record(stream)
         stream.synchronize()
         out["read_reduce_gbs"] = round(big.numel() * 4 * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
-    out["note"] = ("2 GB device copy counted read+write; 4 GB float32 sum (read-only); diagnostics, "
-                   "timed with CUDA events, not this library's kernels")
+        sink = torch.zeros(1, dtype=torch.int32, device=device)
+        for _ in range(2):
+            q.read_bandwidth_probe(big, sink, stream=stream)
+        e0.record(stream)
+        for _ in range(reps):
+            q.read_bandwidth_probe(big, sink, stream=stream)
+        e1.record(stream)
+        stream.synchronize()
+        out["read_probe_gbs"] = round(big.numel() * 4 * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    out["note"] = ("2 GB device copy counted read+write; 4 GB float32 sum (read-only); 4 GB read by this "
+                   "library's probe kernel (128-bit L2-only loads); diagnostics timed with CUDA events")
     del src, dst, big
     torch.cuda.empty_cache()
     return out
@@ -663,7 +674,7 @@ def run_gpu(args):
     if q.device_fault() != 0:
         raise RuntimeError("device fault word set during the benchmark")
 
-    ceilings = None if args.no_configs else measure_ceilings(torch, stream, device)
+    ceilings = None if args.no_configs else measure_ceilings(q, torch, stream, device)
     if rank != 0:
         return 0
     cpu = None

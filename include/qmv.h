@@ -292,6 +292,15 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
  * a non-weight type, QMV_ERR_SHAPE for values out of range. */
 int qmv_set_mma_min_cols(int type, int min_cols);
 
+/* Diagnostic: reads every 16-byte piece of the device buffer buf (bytes, a
+ * multiple of 16; buf 16-byte aligned) once, with the GEMV weight stream's
+ * load width (128-bit loads cached in L2 only) over 4 CTAs per SM, so that
+ * timing it gives this device's read-only streaming ceiling.  *sink (device,
+ * 4 bytes) is written only in the practically impossible case that one
+ * thread's XOR of the words it read equals 0x9E3779B9 (this keeps the loads
+ * from being optimised away).  Asynchronous on stream. */
+int qmv_read_bandwidth_probe(const void *buf, size_t bytes, unsigned int *sink, void *stream);
+
 /* The launch the library would make for a plain (gate_up = 0) or fused
  * gate/up SwiGLU (gate_up = 1) GEMV of `type` with M rows, K columns and
  * ncols activation columns, from q8_1 (fp32_input = 0) or fp32 input

@@ -30,7 +30,7 @@ EXPORTS = (
     "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32", "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32",
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
-    "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
+    "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv", "qmv_read_bandwidth_probe",
 )
 
 
@@ -93,13 +93,15 @@ def lib():
         L.qmv_set_pdl.argtypes = [_int]
         L.qmv_set_checked.argtypes = [_int]
         L.qmv_set_mma_min_cols.argtypes = [_int, _int]
+        L.qmv_read_bandwidth_probe.argtypes = [_vp, ctypes.c_size_t, _vp, _vp]
         L.qmv_describe_gemv.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.POINTER(LaunchInfo)]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
                      "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_mul_mat_vec_fused",
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
-                     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv"):
+                     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
+                     "qmv_read_bandwidth_probe"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -348,6 +350,13 @@ def set_tuning(qtype: int, threads: int = 0, slice_units: int = 0, stages: int =
 def set_stream_tuning(qtype: int, dec_warps: int = 0, pre_tiles: int = 0):
     """Decoding warps per CTA and tiles per warp requested before the dependency wait (0: default)."""
     _check("qmv_set_stream_tuning", lib().qmv_set_stream_tuning(qtype, dec_warps, pre_tiles))
+
+
+def read_bandwidth_probe(buf, sink, stream=None):
+    """Diagnostic: read every 16-byte piece of the CUDA tensor buf once (see include/qmv.h)."""
+    _need_cuda(buf, "buf")
+    _check("qmv_read_bandwidth_probe", lib().qmv_read_bandwidth_probe(_ptr(buf), buf.numel() * buf.element_size(),
+                                                                     _ptr(sink), _stream_handle(stream)))
 
 
 def describe_gemv(qtype: int, M: int, K: int, ncols: int = 1, gate_up: bool = False, fp32_input: bool = False):

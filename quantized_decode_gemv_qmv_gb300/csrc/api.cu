@@ -1011,6 +1011,20 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles)
     return QMV_OK;
 }
 
+int qmv_read_bandwidth_probe(const void *buf, size_t bytes, unsigned int *sink, void *stream)
+{
+    if (!buf || !sink) return QMV_ERR_NULL;
+    if (bytes == 0 || bytes % 16) return QMV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(buf) % 16 || reinterpret_cast<uintptr_t>(sink) % 4) return QMV_ERR_ALIGN;
+    QMV_RANGE(buf, bytes);
+    QMV_RANGE(sink, 4u);
+    DevInfo dev;
+    qmv_status s = device_info(dev);
+    if (s != QMV_OK) return s;
+    return cuda_status(launch_read_probe(buf, static_cast<int64_t>(bytes), sink, dev.num_sms,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, int fp32_input, qmv_launch_info *info)
 {
     if (!info) return QMV_ERR_NULL;

@@ -140,6 +140,10 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_set_mma_min_cols(12, -1) == 3
     assert L.qmv_set_mma_min_cols(9, 0) == 2
     assert L.qmv_set_mma_min_cols(12, 0) == 0
+    rp = L.qmv_read_bandwidth_probe
+    assert rp(nul, 16, p, nul) == 1 and rp(p, 16, nul, nul) == 1
+    assert rp(p, 0, p, nul) == 3 and rp(p, 17, p, nul) == 3
+    assert rp(ctypes.c_void_p(0x1008), 16, p, nul) == 5
     info = qlib.LaunchInfo()
     assert L.qmv_describe_gemv(12, 0, 16, 4096, 1, 0, None) == 1
     assert L.qmv_describe_gemv(12, 0, 16, 250, 1, 0, ctypes.byref(info)) == 3

@@ -1,7 +1,8 @@
 """The launch geometry the planner picks (qmv_describe_gemv), on the GPU:
 plausible for every benchmark shape, shared by fp32 and q8_1 input (their
 outputs are bit-identical because of it), and moved by the tuning setters
-and by the QMV_GEOM environment override.  Nothing here launches a kernel.
+and by the QMV_GEOM environment override (no GEMV is launched).  Also the
+diagnostic read-bandwidth probe.
 """
 import os
 import subprocess
@@ -96,3 +97,17 @@ def test_environment_override_reaches_the_planner(q):
     out = subprocess.run([sys.executable, "-c", code, ROOT], env=env, capture_output=True, text=True, timeout=300)
     assert out.returncode == 0, out.stderr[-2000:]
     assert out.stdout.split()[-3:] == ["3", "320", "2"], out.stdout
+
+
+def test_read_bandwidth_probe(q):
+    """The diagnostic read probe runs over a buffer with a ragged piece count;
+    its sink is written only when one thread's XOR of the words it read is
+    0x9E3779B9, which words below 2^21 cannot produce."""
+    import torch
+
+    buf = torch.arange(0, (1 << 20) + 12, dtype=torch.int32, device="cuda")  # 4 MiB + 48 bytes
+    sink = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    q.read_bandwidth_probe(buf, sink)
+    torch.cuda.synchronize()
+    assert int(sink.item()) == 7
+    assert q.device_fault() == 0
