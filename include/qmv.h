@@ -278,6 +278,14 @@ int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_
  * QMV_ERR_TYPE for a non-weight type, QMV_ERR_SHAPE for values out of range. */
 int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
 
+/* How many of the decoding warps (the first ones) request their early tiles
+ * before the dependency wait (1..12; 0 = all of them, the default); the
+ * others request theirs after the activations are staged.  For sweeps of the
+ * trade-off between weight bytes in flight across the kernel boundary and
+ * the activation loads that queue behind them; results are identical for
+ * every setting.  Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above. */
+int qmv_set_early_warps(int type, int early_warps);
+
 /* Column count from which the plain GEMV of `type` (qmv_mul_mat_vec, its
  * fp32-input and fused forms) decodes with the tensor cores instead of the
  * per-column dp4a: 8-row tiles multiplied by all columns at once with
@@ -326,8 +334,9 @@ int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, in
 /* Environment override of the geometry knobs above, for tuning runs:
  * QMV_GEOM="type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K
  * and keys threads, slice_units, stages, ctas_per_sm, smem_share, cluster,
- * dec_warps, pre_tiles and mma_min_cols (the arguments of qmv_set_tuning,
- * qmv_set_stream_tuning and qmv_set_mma_min_cols, same ranges).  It is read
+ * dec_warps, pre_tiles, early_warps and mma_min_cols (the arguments of
+ * qmv_set_tuning, qmv_set_stream_tuning, qmv_set_early_warps and
+ * qmv_set_mma_min_cols, same ranges).  It is read
  * once, before the first GEMV-family call is planned, and applied through
  * those setters; later setter calls override it.  A malformed spec or an
  * out-of-range value makes every GEMV-family call return QMV_ERR_CONFIG

@@ -31,6 +31,7 @@ EXPORTS = (
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv", "qmv_read_bandwidth_probe",
+    "qmv_set_early_warps",
 )
 
 
@@ -93,6 +94,7 @@ def lib():
         L.qmv_set_pdl.argtypes = [_int]
         L.qmv_set_checked.argtypes = [_int]
         L.qmv_set_mma_min_cols.argtypes = [_int, _int]
+        L.qmv_set_early_warps.argtypes = [_int, _int]
         L.qmv_read_bandwidth_probe.argtypes = [_vp, ctypes.c_size_t, _vp, _vp]
         L.qmv_describe_gemv.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.POINTER(LaunchInfo)]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
@@ -101,7 +103,7 @@ def lib():
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
                      "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
-                     "qmv_read_bandwidth_probe"):
+                     "qmv_read_bandwidth_probe", "qmv_set_early_warps"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -365,6 +367,11 @@ def describe_gemv(qtype: int, M: int, K: int, ncols: int = 1, gate_up: bool = Fa
     _check("qmv_describe_gemv", lib().qmv_describe_gemv(qtype, 1 if gate_up else 0, M, K, ncols,
                                                        1 if fp32_input else 0, ctypes.byref(info)))
     return {name: getattr(info, name) for name, _ in LaunchInfo._fields_}
+
+
+def set_early_warps(qtype: int, early_warps: int = 0):
+    """Decoding warps that request tiles before the dependency wait (0: all)."""
+    _check("qmv_set_early_warps", lib().qmv_set_early_warps(qtype, early_warps))
 
 
 def set_mma_min_cols(qtype: int, min_cols: int = 0):

@@ -66,6 +66,7 @@ struct Tuning {
     std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0}, cluster{0};
     std::atomic<int> dec_warps{0}, pre_tiles{0};
     std::atomic<int> mma_min_cols{0};  // 0: MMA_MIN_COLS; 9: never
+    std::atomic<int> early_warps{0};   // 0: every decoding warp requests its early tiles
 };
 Tuning g_tuning[3];
 
@@ -96,9 +97,10 @@ struct DevInfo {
 // ---- QMV_GEOM: launch-geometry overrides from the environment (tuning) ----
 // "type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K and keys
 // threads, slice_units, stages, ctas_per_sm, smem_share, cluster (as for
-// qmv_set_tuning), dec_warps, pre_tiles (qmv_set_stream_tuning) and
-// mma_min_cols (qmv_set_mma_min_cols).  Read once, before the first GEMV call
-// is planned; values go through the setters' range checks.
+// qmv_set_tuning), dec_warps, pre_tiles (qmv_set_stream_tuning),
+// early_warps (qmv_set_early_warps) and mma_min_cols (qmv_set_mma_min_cols).
+// Read once, before the first GEMV call is planned; values go through the
+// setters' range checks.
 std::once_flag g_geom_once;
 std::atomic<int> g_geom_status{QMV_OK};
 
@@ -120,11 +122,14 @@ bool apply_geom_entry(const std::string &entry)
     const int type = tname == "q4_0" ? FMT_Q4_0 : tname == "q4_K" ? FMT_Q4_K : tname == "q6_K" ? FMT_Q6_K : -1;
     if (type < 0) return false;
     const Tuning &cur = g_tuning[tidx(type)];
-    int v[9] = {cur.threads.load(),     cur.slice_units.load(), cur.stages.load(),
-                cur.ctas_per_sm.load(), cur.smem_share.load(),  cur.cluster.load(),
-                cur.dec_warps.load(),   cur.pre_tiles.load(),   cur.mma_min_cols.load()};
-    static const char *const keys[9] = {"threads",    "slice_units", "stages",    "ctas_per_sm", "smem_share",
-                                        "cluster",    "dec_warps",   "pre_tiles", "mma_min_cols"};
+    constexpr int NK = 10;
+    int v[NK] = {cur.threads.load(),     cur.slice_units.load(), cur.stages.load(),
+                 cur.ctas_per_sm.load(), cur.smem_share.load(),  cur.cluster.load(),
+                 cur.dec_warps.load(),   cur.pre_tiles.load(),   cur.mma_min_cols.load(),
+                 cur.early_warps.load()};
+    static const char *const keys[NK] = {"threads",   "slice_units", "stages",       "ctas_per_sm", "smem_share",
+                                         "cluster",   "dec_warps",   "pre_tiles",    "mma_min_cols",
+                                         "early_warps"};
     size_t pos = colon + 1;
     while (pos <= entry.size()) {
         size_t comma = entry.find(',', pos);
@@ -133,12 +138,13 @@ bool apply_geom_entry(const std::string &entry)
         const size_t eq = kv.find('=');
         if (eq == std::string::npos) return false;
         int k = 0;
-        while (k < 9 && kv.compare(0, eq, keys[k]) != 0) ++k;
-        if (k == 9 || !parse_int(kv.substr(eq + 1), v[k])) return false;
+        while (k < NK && kv.compare(0, eq, keys[k]) != 0) ++k;
+        if (k == NK || !parse_int(kv.substr(eq + 1), v[k])) return false;
         pos = comma + 1;
     }
     return qmv_set_tuning(type, v[0], v[1], v[2], v[3], v[4], v[5]) == QMV_OK &&
-           qmv_set_stream_tuning(type, v[6], v[7]) == QMV_OK && qmv_set_mma_min_cols(type, v[8]) == QMV_OK;
+           qmv_set_stream_tuning(type, v[6], v[7]) == QMV_OK && qmv_set_mma_min_cols(type, v[8]) == QMV_OK &&
+           qmv_set_early_warps(type, v[9]) == QMV_OK;
 }
 
 qmv_status geom_env()
@@ -445,6 +451,7 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
         ((mode == MODE_GATE || mode == MODE_MOE_GATE) ? 2 : 1);
     p.pre_tiles = tu.pre_tiles.load() > 0 ? std::min(stages, tu.pre_tiles.load())
                                           : (tiles_per_warp <= stages ? stages : 1);
+    p.early_warps = tu.early_warps.load() > 0 ? tu.early_warps.load() : wpc;
     p.act_bytes = static_cast<uint32_t>(act);
     p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
     L.fn = fn;
@@ -1061,6 +1068,14 @@ int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, in
     info->dec_warps = L.stream ? L.p.dec_warps : 0;
     info->pre_tiles = L.stream ? L.p.pre_tiles : 0;
     info->smem = L.smem;
+    return QMV_OK;
+}
+
+int qmv_set_early_warps(int type, int early_warps)
+{
+    if (!weight_type(type)) return QMV_ERR_TYPE;
+    if (early_warps < 0 || early_warps > TILE_MAX_THREADS / 32) return QMV_ERR_SHAPE;
+    g_tuning[tidx(type)].early_warps = early_warps;
     return QMV_OK;
 }
 

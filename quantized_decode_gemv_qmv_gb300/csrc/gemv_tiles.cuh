@@ -467,7 +467,8 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         ++issued;
     };
 
-    while (issued < total && issued < p.pre_tiles) issue_tile();  // weights first
+    if (warp < p.early_warps)
+        while (issued < total && issued < p.pre_tiles) issue_tile();  // weights first
     if constexpr (!IS_MOE) pdl_wait();
     if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
     if (!MMA && ncta > 1 && threadIdx.x == 0)
