@@ -56,7 +56,7 @@ MMA_MIN_COLS = 9
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "ae05bef92d3b3fe6", "bytes_per_launch": 28530112,
+TRAFFIC = {"csrc_sha": "b53e6f5c2322b91f", "bytes_per_launch": 28530592,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down (profiles/gemv_tiles_q4_K_down_fused.md)"}
 
 
