@@ -159,8 +159,9 @@ def test_q6_K_codes_follow_the_printed_vec_dot_assembly():
     # code - 32 = (vil | vih) - 32 per byte; i = 0 takes the low nibbles with qh
     # bits 0-1, i = 1 the high nibbles with qh bits 4-5.  With d = 1 and every
     # scale 1 the oracle's dequantized values are exactly the codes - 32, so
-    # the byte pairing of reading R3 is checked against the printed arithmetic
-    # (the second ql run of each half uses qh bits 2-3 and 6-7, vh >> 2).
+    # the oracle's Q6_K byte pairing (ql[128], qh[64], scales[16], d: a layout
+    # the pages do not print) is checked against the printed arithmetic (the
+    # second ql run of each half uses qh bits 2-3 and 6-7, vh >> 2).
     rng = np.random.default_rng(611)
     blk = rng.integers(0, 256, size=210, dtype=np.uint8)
     blk[192:208] = 1                                   # int8 scales
