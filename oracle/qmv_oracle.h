@@ -19,8 +19,8 @@
  *     vec_dot_q4_K_q8_1_impl_vmmq and the Q6_K snippet.
  *   - GEMV: y[c][r] = sum_k What[r][k] * xhat[c][k] evaluated in fp64.
  *
- * Readings where the pages are silent or contradict themselves are listed in
- * the repository's design notes; each is restated at the function below.
+ * Where the pages are silent or contradict themselves, the reading taken is
+ * stated at the function it concerns, below.
  *
  * Parity pins: every function here is checked by the CPU test-suite against
  * closed forms, worked examples and brute force (tests/test_oracle_*.py),
