@@ -128,8 +128,10 @@ int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t
  *   Q4_0: sum_b d4 * (d8*sumi - 8*s)              sumi = sum of code*qy
  *   Q4_K: sum_sb d*sc*d8*dot1 - dmin*m*d8*dot2     dot1 = sum code*qy, dot2 = sum qy
  *   Q6_K: sum_sb d*sc*d8*sum((v-32)*qy)            per 16-value sub-block
- * accumulated in fp32.  W is read exactly once per call whatever ncols is;
- * each weight block is decoded once and reused for every column. */
+ * accumulated in fp32.  W is read from HBM exactly once per call whatever
+ * ncols is: each weight tile, staged in shared memory, serves every column
+ * (the default decode unpacks it again per column; the opt-in tensor-core
+ * decode, qmv_set_mma_min_cols, once for all columns). */
 int qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols,
                     float *y, void *stream);
 
