@@ -191,3 +191,86 @@ def test_fullsize_moe_shared_expert(q):
     assert np.all(np.abs(y[:, :, rows] - y_ref) <= TOL * l1)
     ys_ref, l1s = oracle.shared_expert_gemv(t, Ws, M, K, xq_ref, T, rows=rows)
     assert np.all(np.abs(ys[:, rows] - ys_ref) <= TOL * l1s)
+
+
+def glu_bound(g, u, l1g, l1u):
+    """Bound of u * silu(g) when g and u each carry TOL * l1 (first order)."""
+    sig = 1.0 / (1.0 + np.exp(-g))
+    return np.abs(u) * np.abs(sig * (1 + g * (1 - sig))) * TOL * l1g + np.abs(g * sig) * TOL * l1u + \
+        1e-6 * np.abs(u * g * sig)
+
+
+def test_fullsize_moe_gated_shared_expert(q):
+    # the bench's gated MoE call: 8 experts x (up + gate) 14336x4096, 4 tokens
+    # top-2, plus a gated shared expert, one launch
+    import torch
+
+    t, E, M, K, T, k = oracle.Q4_K, 8, 14336, 4096, 4, 2
+    rb = oracle.row_bytes(t, K)
+    W = {n: np.empty((E, M * rb), dtype=np.uint8) for n in ("up", "gate")}
+    Wd = {n: torch.empty((E, M * rb), dtype=torch.uint8, device="cuda") for n in ("up", "gate")}
+    for n, base in (("up", 6300), ("gate", 6400)):
+        for e in range(E):
+            We, Wed = quantized(q, t, M, K, seed=base + e)
+            W[n][e] = We.reshape(-1)
+            Wd[n][e] = Wed.reshape(-1)
+    Wsu, Wsud = quantized(q, t, M, K, seed=6498)
+    Wsg, Wsgd = quantized(q, t, M, K, seed=6499)
+    ids = synthetic.moe_ids(67, T, k, E)
+    xq_ref = oracle.quantize_q8_1(synthetic.activations_f32(68, T, K))
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    y, ys = q.mul_mat_vec_id_fused(t, Wd["up"], E, M, K, dev(ids), xq=dev(xq_ref), W_gate=Wd["gate"],
+                                   W_shared=Wsud, W_shared_gate=Wsgd, status=status)
+    y, ys = host(y), host(ys)
+    assert int(host(status)[0]) == 0
+    rows = sample_rows(M, 69)
+    u, l1u, _ = oracle.moe_gemv(t, W["up"], E, M, K, xq_ref, ids, rows=rows)
+    g, l1g, _ = oracle.moe_gemv(t, W["gate"], E, M, K, xq_ref, ids, rows=rows)
+    assert np.all(np.abs(y[:, :, rows] - oracle.swiglu(g, u)) <= glu_bound(g, u, l1g, l1u))
+    su, l1su = oracle.shared_expert_gemv(t, Wsu, M, K, xq_ref, T, rows=rows)
+    sg, l1sg = oracle.shared_expert_gemv(t, Wsg, M, K, xq_ref, T, rows=rows)
+    assert np.all(np.abs(ys[:, rows] - oracle.swiglu(sg, su)) <= glu_bound(sg, su, l1sg, l1su))
+
+
+def test_fullsize_q6_K_small_batch_sweep(q):
+    # the bench's Q6_K column sweep (4096x14336, the down projection of an
+    # 8B-class FFN), 1..8 columns, including the single-tile-ring geometry at 7-8
+    t, M, K = oracle.Q6_K, 4096, 14336
+    W, Wd = quantized(q, t, M, K, seed=4646)
+    rows = sample_rows(M, 47)
+    for ncols in range(1, 9):
+        xq_ref = oracle.quantize_q8_1(synthetic.activations_f32(48 + ncols, ncols, K))
+        y = host(q.mul_mat_vec(t, Wd, M, K, dev(xq_ref), ncols))
+        y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq_ref, ncols, rows=rows)
+        assert np.all(np.abs(y[:, rows] - y_ref) <= TOL * l1), ncols
+
+
+STEP_KINDS = [("qkv", 12288, 4096, False), ("o", 4096, 4096, False), ("gate_up", 11008, 4096, True),
+              ("down", 4096, 11008, False)]
+
+
+@pytest.mark.parametrize("name,M,K,gate", STEP_KINDS, ids=[s[0] for s in STEP_KINDS])
+def test_fullsize_step_launches_fp32_input(q, name, M, K, gate):
+    """The benchmark step's launches as it times them: fp32 activations
+    quantized inside the GEMV by clusters of CTAs, bit-identical to quantizing
+    first and running the q8_1 GEMV, and within the bound of the oracle."""
+    t = oracle.Q4_K
+    W, Wd = quantized(q, t, M, K, seed=zlib.crc32(name.encode()) % 100000)
+    x = synthetic.activations_f32(70 + K, 1, K, outlier_frac=0.01)
+    xq_ref = oracle.quantize_q8_1(x)
+    xd = dev(x)
+    rows = sample_rows(M, 71)
+    if gate:
+        Wg, Wgd = quantized(q, t, M, K, seed=zlib.crc32(b"gate") % 100000)
+        y = host(q.mul_mat_vec_gate_up_swiglu_f32(t, Wgd, Wd, M, K, xd))
+        y2 = host(q.mul_mat_vec_gate_up_swiglu(t, Wgd, Wd, M, K, q.quantize_q8_1(xd), 1))
+        g, l1g = oracle.gemv_formula(t, Wg, M, K, xq_ref, 1, rows=rows)
+        u, l1u = oracle.gemv_formula(t, W, M, K, xq_ref, 1, rows=rows)
+        assert np.all(np.abs(y[:, rows] - oracle.swiglu(g, u)) <= glu_bound(g, u, l1g, l1u))
+    else:
+        y = host(q.mul_mat_vec_f32(t, Wd, M, K, xd))
+        y2 = host(q.mul_mat_vec(t, Wd, M, K, q.quantize_q8_1(xd), 1))
+        y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq_ref, 1, rows=rows)
+        assert np.all(np.abs(y[:, rows] - y_ref) <= TOL * l1)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+    assert q.describe_gemv(t, M, K, 1, gate_up=gate, fp32_input=True)["cluster"] == 2
