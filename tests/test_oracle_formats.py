@@ -85,6 +85,17 @@ def test_row_and_padding_sizes():
     assert oracle.q8_1_padded_k(1) == 512
     with pytest.raises(ValueError):
         oracle.row_bytes(oracle.Q4_K, 4096 + 32)
+    # q8_1 bytes per activation column: padded blocks of 36 bytes (4,608 B at
+    # K = 4096; 352 blocks, 344 of them real, 12,672 B at 11008; 16,128 B at 14336)
+    assert oracle.q8_1_row_bytes(4096) == 4608
+    assert oracle.q8_1_row_bytes(11008) == 12672
+    assert oracle.q8_1_row_bytes(14336) == 16128
+    # integer sums per row of the exact-sum export: one per Q4_0 block, the
+    # pair (dot1, dot2) per Q4_K 32-value sub-block, one per Q6_K 16-value
+    # sub-block
+    assert oracle.subblock_count(oracle.Q4_0, 4096) == 128
+    assert oracle.subblock_count(oracle.Q4_K, 4096) == 2 * (4096 // 32)
+    assert oracle.subblock_count(oracle.Q6_K, 4096) == 4096 // 16
 
 
 # ---- decoders against hand-built blocks ------------------------------------
