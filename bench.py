@@ -731,6 +731,20 @@ def run_kernel_only(args):
     kinds = {name: (M, K, nmat) for name, M, K, nmat in STEP}
     shapes = dict(SHAPES, **{"14336x4096": (14336, 4096)})
     nc = args.ncols
+    if args.kernel_only == "moe":
+        # the configs' MoE call: 8 experts of 14336x4096, 4 tokens top-2 (the same seeded routing)
+        M, K = 14336, 4096
+        E = torch.stack([q.quantize_weights(Q4_K, synthetic.device_normal_f32(11 + e, (M, K), 0.02, "cuda"))
+                         for e in range(8)]).view(8, -1)
+        ids = torch.from_numpy(synthetic.moe_ids(3_000_600, 4, 2, 8)).cuda()
+        xq = q.quantize_q8_1(torch.from_numpy(synthetic.activations_f32(13, 4, K)).cuda())
+        ym = torch.empty((4, 2, M), dtype=torch.float32, device="cuda")
+        for _ in range(args.launches):
+            q.mul_mat_vec_id(Q4_K, E, 8, M, K, xq, ids, out=ym)
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel_only": "moe", "launches": args.launches,
+                          "experts_touched": len(set(ids.view(-1).tolist()))}))
+        return 0
     if args.kernel_only in shapes:
         M, K = shapes[args.kernel_only]
         nmat = 1
@@ -766,7 +780,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=6.0, help="CPU-baseline timing budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timing section")
-    ap.add_argument("--kernel-only", default=None, help="profiling aid: only GEMV launches of one shape or step kind")
+    ap.add_argument("--kernel-only", default=None,
+                    help="profiling aid: only GEMV launches of one shape, step kind, or the MoE call (moe)")
     ap.add_argument("--launches", type=int, default=8)
     ap.add_argument("--ncols", type=int, default=1, help="profiling aid: activation columns of a --kernel-only shape")
     ap.add_argument("--mma-min-cols", type=int, default=0,
