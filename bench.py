@@ -16,9 +16,13 @@ Reported: weight GB/s of the whole step (value); the roofline of the GEMV
 kernel over the step's own launches (algorithmic bytes over CUDA-event time
 against the measured HBM copy bandwidth); microseconds per call of the
 q8_1-input GEMV at the three Llama-7B shapes; an end-to-end number through
-the public API with host buffers; and the CPU oracle timed on the host cores.
+the public API with host buffers; the CPU oracle timed on the host cores;
+per-call times of every other quoted workload (Q4_0, Q6_K, the column sweeps
+with both decodes, the fused gate/up, the MoE variants); and bandwidth
+ceilings (device copy, torch reduction, the library's read probe).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --kernel-only SHAPE|KIND|moe [--ncols N] [--mma-min-cols N]   (profiler captures)
 """
 from __future__ import annotations
 
