@@ -104,3 +104,34 @@ def test_exact_integer_results(q, t, M, K, rows, f32, ncols):
     assert np.array_equal(host(q.mul_mat_vec(t, Wd, M, K, dev(xq), ncols)), want)
     if f32:
         assert np.array_equal(host(q.mul_mat_vec_f32(t, Wd, M, K, dev(x))), want)
+
+
+@pytest.mark.parametrize("f32", [False, True], ids=["q8_1", "f32"])
+def test_exact_integer_moe(q, f32):
+    """The expert-indexed GEMV with integer experts: every valid slot is the
+    exact integer W[ids[t][k]] x_t, a repeated expert serves its tokens in one
+    pass, and an out-of-range id leaves its slot zero."""
+    import torch
+
+    t, E, M, K = oracle.Q4_0, 6, 33, 1024
+    rng = np.random.default_rng(7100)
+    W = q4_0_rows(E * M, K, rng).reshape(E, -1)
+    ids = np.array([[2, 5], [2, 0], [7, 2], [5, 4]], dtype=np.int32)  # expert 2 three times; 7 is invalid
+    T = ids.shape[0]
+    x = small_integer_activations(T, K, rng)
+    xq = oracle.quantize_q8_1(x)
+    y_ref, _, bad = oracle.moe_gemv(t, W, E, M, K, xq, ids)
+    assert bad == 1 and np.all(np.abs(y_ref) < 2 ** 24) and np.array_equal(y_ref, np.round(y_ref))
+    w = oracle.dequantize_rows(t, W.reshape(E * M, -1), K).reshape(E, M, K)
+    for tok in range(T):
+        for k in range(2):
+            e = ids[tok, k]
+            exp = x[tok].astype(np.float64) @ w[e].T if e < E else np.zeros(M)
+            assert np.array_equal(y_ref[tok, k], exp)
+    status = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    if f32:
+        y = host(q.mul_mat_vec_id_f32(t, dev(W), E, M, K, dev(x), dev(ids), status=status))
+    else:
+        y = host(q.mul_mat_vec_id(t, dev(W), E, M, K, dev(xq), dev(ids), status=status))
+    assert int(host(status)[0]) == 1
+    assert np.array_equal(y, y_ref.astype(np.float32))
