@@ -135,3 +135,38 @@ def test_exact_integer_moe(q, f32):
         y = host(q.mul_mat_vec_id(t, dev(W), E, M, K, dev(xq), dev(ids), status=status))
     assert int(host(status)[0]) == 1
     assert np.array_equal(y, y_ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("f32", [False, True], ids=["q8_1", "f32"])
+def test_exact_integer_fused_extras(q, f32):
+    """The fused call's up bias and the MoE shared expert on integer data:
+    y = W x + b and y_shared = W_shared x_t exactly."""
+    import torch
+
+    t, M, K, nc = oracle.Q4_0, 71, 1024, 3
+    rng = np.random.default_rng(7200)
+    W = q4_0_rows(M, K, rng)
+    b = rng.integers(-1000, 1001, size=M).astype(np.float32)
+    x = small_integer_activations(nc, K, rng)
+    xq = oracle.quantize_q8_1(x)
+    w = oracle.dequantize_rows(t, W, K)
+    want = (x.astype(np.float64) @ w.T + b).astype(np.float32)
+    kw = {"x": dev(x)} if f32 else {"xq": dev(xq)}
+    assert np.array_equal(host(q.mul_mat_vec_fused(t, dev(W), M, K, bias=dev(b), **kw)), want)
+    # MoE with a shared expert: the routed slots and the shared output, all exact
+    E = 4
+    We = q4_0_rows(E * M, K, rng).reshape(E, -1)
+    Ws = q4_0_rows(M, K, rng)
+    ids = np.array([[1, 3], [0, 1], [2, 2]], dtype=np.int32)
+    T = ids.shape[0]
+    xt = small_integer_activations(T, K, rng)
+    xtq = oracle.quantize_q8_1(xt)
+    kw = {"x": dev(xt)} if f32 else {"xq": dev(xtq)}
+    status = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    y, ys = q.mul_mat_vec_id_fused(t, dev(We), E, M, K, dev(ids), W_shared=dev(Ws), status=status, **kw)
+    we = oracle.dequantize_rows(t, We.reshape(E * M, -1), K).reshape(E, M, K)
+    ws = oracle.dequantize_rows(t, Ws, K)
+    want_y = np.stack([np.stack([xt[i].astype(np.float64) @ we[ids[i, k]].T for k in range(2)]) for i in range(T)])
+    assert int(host(status)[0]) == 0
+    assert np.array_equal(host(y), want_y.astype(np.float32))
+    assert np.array_equal(host(ys), (xt.astype(np.float64) @ ws.T).astype(np.float32))
