@@ -205,3 +205,20 @@ def test_geometry_environment_override(qlib, spec, want):
     else:
         assert rc == want
     assert qlib.lib().qmv_status_str(10) == b"malformed or out-of-range QMV_GEOM override"
+
+
+def test_header_is_plain_c99(tmp_path):
+    """include/qmv.h is a C header: it compiles as C99 with every warning an
+    error, and a C program declares and calls through it."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "qmv.h"\n'
+                   "int main(void) { qmv_launch_info info; (void)info;\n"
+                   "  return qmv_status_str(QMV_OK) != 0 && qmv_version() > 0 ? 0 : 1; }\n")
+    import subprocess
+
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
