@@ -222,3 +222,31 @@ def test_header_is_plain_c99(tmp_path):
     r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
                         "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_c_program_links_and_calls_the_library(qlib, tmp_path):
+    """A C program linked against libqmv.so (no Python involved) gets the
+    sizes and the host-validation statuses the header documents."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    import subprocess
+
+    libdir = os.path.dirname(qlib.library_path())
+    src = tmp_path / "prog.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "qmv.h"\n'
+        "int main(void) {\n"
+        "  void *p = (void *)0x1000;\n"
+        '  printf("%zu %zu %lld %d %d %d\\n", qmv_row_bytes(QMV_TYPE_Q4_K, 4096), qmv_q8_1_bytes(11008, 1),\n'
+        "         (long long)qmv_q8_1_padded_k(11008), qmv_mul_mat_vec(5, p, 16, 256, p, 1, (float *)p, 0),\n"
+        "         qmv_mul_mat_vec(QMV_TYPE_Q4_K, p, 16, 250, p, 1, (float *)p, 0),\n"
+        "         qmv_mul_mat_vec(QMV_TYPE_Q4_K, p, 16, 256, p, 9, (float *)p, 0));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "prog"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-L", libdir, "-lqmv", "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["2304", "12672", "11264", "2", "3", "4"]
