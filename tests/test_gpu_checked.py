@@ -158,6 +158,9 @@ def test_ranges_at_the_end_of_an_allocation(q):
         "weights_w": (lambda p, s: L.qmv_quantize_weights(t, p, M, K, ldx, lo, s), ((M - 1) * ldx + K) * 4, 4),
         "weights_W": (lambda p, s: L.qmv_quantize_weights(t, lo, M, K, ldx, p, s), M * rb, rb),
         "debug_out": (lambda p, s: L.qmv_debug_subblock_sums(t, lo, M, K, lo, nc, p, s), nc * M * per_row * 4, 4),
+        # (the 4-byte sink cannot straddle an allocation end without breaking
+        # its alignment first, so only the buffer's range is probed here)
+        "probe_buf": (lambda p, s: L.qmv_read_bandwidth_probe(p, 4096, lo, s), 4096, 16),
     }
     names = list(cases)
     # every call once for real with all its pointers at the allocation's start, where every range
