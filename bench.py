@@ -358,12 +358,15 @@ def measure_configs(q, torch, stream, device, reps):
         return q.quantize_q8_1(x, stream=stream)
 
     out = {}
-    y = torch.empty((8, 32000), dtype=torch.float32, device=device)
+    y_flat = torch.empty(8 * 32000, dtype=torch.float32, device=device)
+
+    def yv(nc, M):  # a contiguous [nc][M] output
+        return y_flat[: nc * M].view(nc, M)
 
     def plain(name, t, M, K, n, seed, ncols=1, outl=0.0):
         ws = weights(t, M, K, n, seed)
         xq = xq_of(K, ncols, seed + 99, outl)
-        us = chain_time([lambda W=W: q.mul_mat_vec(t, W, M, K, xq, ncols, out=y[:ncols, :M], stream=stream)
+        us = chain_time([lambda W=W: q.mul_mat_vec(t, W, M, K, xq, ncols, out=yv(ncols, M), stream=stream)
                          for W in ws])
         wb = ws[0].numel()
         out[name] = {"us_per_call": round(us, 3), "weight_gbs": round(wb / us / 1e3, 1)}
@@ -377,7 +380,7 @@ def measure_configs(q, torch, stream, device, reps):
     sweep = {}
     for nc in range(1, 9):
         xq = xq_of(4096, nc, 3_000_400 + nc)
-        calls = [lambda W=W: q.mul_mat_vec(q.Q4_K, W, 14336, 4096, xq, nc, out=y[:nc, :14336], stream=stream)
+        calls = [lambda W=W: q.mul_mat_vec(q.Q4_K, W, 14336, 4096, xq, nc, out=yv(nc, 14336), stream=stream)
                  for W in ws]
         # both decodes at every column count (the crossover), then the default choice
         both = {}
@@ -394,7 +397,7 @@ def measure_configs(q, torch, stream, device, reps):
     sweep6 = {}
     for nc in range(1, 9):
         xq = xq_of(14336, nc, 3_000_460 + nc)
-        us = chain_time([lambda W=W: q.mul_mat_vec(q.Q6_K, W, 4096, 14336, xq, nc, out=y[:nc, :4096], stream=stream)
+        us = chain_time([lambda W=W: q.mul_mat_vec(q.Q6_K, W, 4096, 14336, xq, nc, out=yv(nc, 4096), stream=stream)
                          for W in ws6])
         sweep6[str(nc)] = {"us_per_call": round(us, 3), "weight_gbs": round(ws6[0].numel() / us / 1e3, 1)}
     out["q6_K 4096x14336 ncols 1..8"] = sweep6
@@ -404,14 +407,14 @@ def measure_configs(q, torch, stream, device, reps):
     xq = xq_of(4096, 1, 3_000_500)
     pairs = [(ws[2 * i], ws[2 * i + 1]) for i in range(4)]
     us = chain_time([lambda g=g, u=u: q.mul_mat_vec_gate_up_swiglu(q.Q4_K, g, u, 14336, 4096, xq, 1,
-                                                                    out=y[:1, :14336], stream=stream) for g, u in pairs])
+                                                                    out=yv(1, 14336), stream=stream) for g, u in pairs])
     out["q4_K gate+up 2x14336x4096 swiglu"] = {"us_per_call": round(us, 3),
                                                "weight_gbs": round(2 * ws[0].numel() / us / 1e3, 1)}
     # the same with the fused epilogue's up and gate biases
     bu = torch.from_numpy(synthetic.activations_f32(3_000_510, 1, 14336)[0]).to(device)
     bg = torch.from_numpy(synthetic.activations_f32(3_000_511, 1, 14336)[0]).to(device)
     us = chain_time([lambda g=g, u=u: q.mul_mat_vec_fused(q.Q4_K, u, 14336, 4096, xq=xq, W_gate=g, bias=bu,
-                                                          gate_bias=bg, out=y[:1, :14336], stream=stream)
+                                                          gate_bias=bg, out=yv(1, 14336), stream=stream)
                      for g, u in pairs])
     out["q4_K gate+up 2x14336x4096 swiglu + up/gate biases"] = {
         "us_per_call": round(us, 3), "weight_gbs": round(2 * ws[0].numel() / us / 1e3, 1)}
