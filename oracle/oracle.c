@@ -375,29 +375,25 @@ int oracle_dequantize_q8_1(const uint8_t *xq, int64_t K, int64_t ncols, double *
     return 0;
 }
 
-/* dequantize_row_q4_K exactly as printed in "GGUF 量化内幕 第16章" 16.2.1:
- * float arithmetic, d1 = d*sc, m1 = min*m, y = d1*q - m1. */
+/* Q4_K weights in fp32 ("GGUF 量化内幕 第16章", 16.2.1, the float decoder):
+ * element e of a super-block belongs to 32-value sub-block e/32, whose 6-bit
+ * scale sc and min m give the fp32 factors d*sc and dmin*m; the weight is
+ * (d*sc)*code - dmin*m, each product and the difference rounded to fp32 in
+ * that order (the oracle is built without contraction, so no fused
+ * multiply-add merges them). */
 int oracle_dequantize_row_q4_K_f32(const uint8_t *W, int64_t K, float *out)
 {
     if (!W || !out) return -3;
     if (K <= 0 || K % QK_K) return -2;
-    for (int64_t i = 0; i < K / QK_K; ++i) {
-        const uint8_t *blk = W + i * Q4_K_BYTES;
-        const uint8_t *q = blk + 16;
-        const float d = oracle_f16_to_f32(rd16(blk));
-        const float mn = oracle_f16_to_f32(rd16(blk + 2));
-        int is = 0;
-        for (int j = 0; j < QK_K; j += 64) {
-            int sc, m;
-            unpack_scale_min_q4_K(blk + 4, is + 0, &sc, &m);
-            const float d1 = d * (float)sc, m1 = mn * (float)m;
-            unpack_scale_min_q4_K(blk + 4, is + 1, &sc, &m);
-            const float d2 = d * (float)sc, m2 = mn * (float)m;
-            for (int l = 0; l < 32; ++l) *out++ = d1 * (float)(q[l] & 15) - m1;
-            for (int l = 0; l < 32; ++l) *out++ = d2 * (float)(q[l] >> 4) - m2;
-            q += 32;
-            is += 2;
-        }
+    for (int64_t k = 0; k < K; ++k) {
+        const uint8_t *blk = W + (k / QK_K) * Q4_K_BYTES;
+        const int e = (int)(k % QK_K);
+        int sc, m;
+        unpack_scale_min_q4_K(blk + 4, e / 32, &sc, &m);
+        const float scale = oracle_f16_to_f32(rd16(blk)) * (float)sc;
+        const float offset = oracle_f16_to_f32(rd16(blk + 2)) * (float)m;
+        const float scaled = scale * (float)q4_K_code(blk, e);
+        out[k] = scaled - offset;
     }
     return 0;
 }
