@@ -39,8 +39,8 @@
  *     plain and gate/up calls, whose clusters of CTAs share the quantization
  *     of the activations, wait on an mbarrier for the partners' shares for at
  *     most one second; past that the kernel records code 2 in the sticky
- *     device fault word (qmv_device_fault) and finishes with invalid outputs
- *     instead of hanging.
+ *     device fault word (qmv_device_fault), writes NaN to the outputs of that
+ *     CTA's rows and returns instead of hanging.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -86,7 +86,10 @@ int qmv_version(void);
 /* ---- sizes ---------------------------------------------------------------- */
 
 /* Bytes of one weight row: (K / block elems) * block bytes; 0 if the type is
- * not a weight type or K is not a positive multiple of its block size. */
+ * not a weight type or K is not a positive multiple of its block size.  The
+ * block sizes are those of the block structs ("GGUF 量化内幕 第16章", 16.1.2,
+ * whose static_asserts fix 18 / 144 / 210 bytes; the mul_mat_vec_q page,
+ * section "权重的排法").  A size helper: no computation on the pages. */
 size_t qmv_row_bytes(int type, int64_t K);
 
 /* K rounded up to a multiple of 512: activations are quantized and strided
@@ -94,7 +97,9 @@ size_t qmv_row_bytes(int type, int64_t K);
  * section "激活的量化"); the padding quantizes to zero blocks. */
 int64_t qmv_q8_1_padded_k(int64_t K);
 
-/* Bytes of ncols q8_1 activation rows: ncols * padded_k/32 * 36. */
+/* Bytes of ncols q8_1 activation rows: ncols * padded_k/32 * 36, the 36-byte
+ * block_q8_1 of the mul_mat_vec_q page, section "激活的量化".  A size helper:
+ * no computation on the pages. */
 size_t qmv_q8_1_bytes(int64_t K, int ncols);
 
 /* ---- activation quantization -------------------------------------------------
@@ -107,7 +112,7 @@ size_t qmv_q8_1_bytes(int64_t K, int ncols);
  * rather than the float sum of x; a block whose amax/127 underflows to zero
  * quantizes to zero; codes are clamped to [-127, 127].
  * Inputs must be finite.  ncols may exceed 8 here (any ncols >= 1). */
-int qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *xq, void *stream);
+qmv_status qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *xq, void *stream);
 
 /* ---- weight quantization ------------------------------------------------------
  * Quantizes an fp32 matrix w (M rows of K floats, row r at w + r*ldw,
@@ -118,8 +123,8 @@ int qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *x
  * absmax (Q6_K) rules taken from the stored half scales.  Bit-identical to
  * the repository's CPU oracle.  Not performance-critical (a preparation step).
  * Inputs must be finite with |x| < 1e4. */
-int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t ldw, void *W,
-                         void *stream);
+qmv_status qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t ldw, void *W,
+                                void *stream);
 
 /* ---- GEMV ---------------------------------------------------------------------
  * y[c*M + r] = sum over blocks of the block formula for row r and activation
@@ -132,16 +137,16 @@ int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t
  * ncols is: each weight tile, staged in shared memory, serves every column
  * (the default decode unpacks it again per column; the opt-in tensor-core
  * decode, qmv_set_mma_min_cols, once for all columns). */
-int qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols,
-                    float *y, void *stream);
+qmv_status qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols,
+                           float *y, void *stream);
 
 /* Fused gate/up GEMV with SwiGLU epilogue (mul_mat_vec_q page, section
  * "融合"): both products are accumulated in one pass over the shared q8_1
  * activations and y[c*M + r] = up * silu(gate), silu(g) = g/(1+exp(-g)).
  * W_gate and W_up have identical shape and type.  The page fuses only at a
  * single column; this call accepts 1 <= ncols <= 8. */
-int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_up, int64_t M,
-                                   int64_t K, const void *xq, int ncols, float *y, void *stream);
+qmv_status qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_up, int64_t M,
+                                          int64_t K, const void *xq, int ncols, float *y, void *stream);
 
 /* Expert-indexed GEMV for mixture-of-experts (mul_mat_vec_q page, section
  * "MoE"): W holds n_expert matrices back to back (expert e at
@@ -152,10 +157,10 @@ int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_u
  * not read.  An id outside [0, n_expert) zero-fills that slot's output; if
  * dev_status is not NULL the kernel stores there the number of such slots
  * (0 when all ids are valid).  1 <= n_tokens <= 8, 1 <= top_k <= 32,
- * 1 <= n_expert <= 65535. */
-int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int64_t K,
-                       const void *xq, const int32_t *ids, int n_tokens, int top_k, float *y,
-                       int32_t *dev_status, void *stream);
+ * 1 <= n_expert <= 65534. */
+qmv_status qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int64_t K,
+                              const void *xq, const int32_t *ids, int n_tokens, int top_k, float *y,
+                              int32_t *dev_status, void *stream);
 
 /* ---- GEMV with the activation quantization fused in ---------------------------
  * The same products with fp32 activations: x holds ncols columns of K floats
@@ -171,16 +176,16 @@ int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int
  * launching (QMV_ERR_TYPE for a type that is not a weight type), and the
  * q8_1-input calls apply.  Arguments, limits, outputs and error behaviour
  * are otherwise those of the calls above. */
-int qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const float *x, int64_t ldx,
-                        int ncols, float *y, void *stream);
+qmv_status qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const float *x, int64_t ldx,
+                               int ncols, float *y, void *stream);
 
-int qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void *W_up, int64_t M,
-                                       int64_t K, const float *x, int64_t ldx, int ncols, float *y,
-                                       void *stream);
+qmv_status qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void *W_up, int64_t M,
+                                              int64_t K, const float *x, int64_t ldx, int ncols, float *y,
+                                              void *stream);
 
-int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M, int64_t K,
-                           const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k,
-                           float *y, int32_t *dev_status, void *stream);
+qmv_status qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M, int64_t K,
+                                  const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k,
+                                  float *y, int32_t *dev_status, void *stream);
 
 /* ---- fused epilogue extras -----------------------------------------------------
  * The mul_mat_vec_q page, section "融合:把 gate、bias 和 SwiGLU 塞进同一个 kernel",
@@ -222,33 +227,30 @@ int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M,
  *   outputs, invalid-id handling and dev_status are those of
  *   qmv_mul_mat_vec_id; one launch serves the routed and the shared
  *   experts. */
-int qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K,
-                          const void *xq, const float *x, int64_t ldx, int ncols, const float *bias,
-                          const float *gate_bias, float *y, void *stream);
+qmv_status qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K,
+                                 const void *xq, const float *x, int64_t ldx, int ncols, const float *bias,
+                                 const float *gate_bias, float *y, void *stream);
 
-int qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int64_t n_expert,
-                             int64_t M, int64_t K, const void *xq, const float *x, int64_t ldx,
-                             const int32_t *ids, int n_tokens, int top_k, float *y,
-                             const void *W_shared_up, const void *W_shared_gate, float *y_shared,
-                             int32_t *dev_status, void *stream);
+qmv_status qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int64_t n_expert,
+                                    int64_t M, int64_t K, const void *xq, const float *x, int64_t ldx,
+                                    const int32_t *ids, int n_tokens, int top_k, float *y,
+                                    const void *W_shared_up, const void *W_shared_gate, float *y_shared,
+                                    int32_t *dev_status, void *stream);
 
-/* ---- verification --------------------------------------------------------------
- * The exact int32 intermediates of the block formulas, computed by the same
- * device code as qmv_mul_mat_vec (for bit-exact parity tests).  out is
- * [ncols][M][n] int32 with
- *   Q4_0: n = K/32, per block sum of code*qy (code = raw nibble 0..15);
- *   Q4_K: n = K/16, per 32-value sub-block the pair (dot1, dot2);
- *   Q6_K: n = K/16, per 16-value sub-block sum (v-32)*qy.
- * out is cleared and written asynchronously on stream. */
-int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const void *xq,
-                            int ncols, int32_t *out, void *stream);
+/* ---- fault reporting -------------------------------------------------------- */
 
 /* Reads and clears the sticky device fault word of the current device: 0 if
  * no kernel's bounded wait has run out since the last call, else the OR of
  * nonzero codes (2: a cluster partner's share of the staged fp32 activations
- * did not arrive within the wait limit; that launch's outputs are invalid).
- * Synchronous (waits for the device). */
-int qmv_device_fault(unsigned int *code);
+ * did not arrive within the wait limit).  A CTA whose wait ran out computes
+ * nothing: it writes NaN to every output of its rows and returns, so a bad
+ * result cannot pass for a good one.  Callers of the fp32-input plain and
+ * gate/up calls (and of qmv_mul_mat_vec_fused with fp32 x) should read this
+ * word after synchronizing before they trust those outputs.  Synchronous
+ * (waits for the device).  The pages have no counterpart: their kernels have
+ * no spin-waits; this word is the library's own report of its one bounded
+ * wait. */
+qmv_status qmv_device_fault(unsigned int *code);
 
 /* ---- tuning (process-wide) -----------------------------------------------------
  * Overrides the launch geometry the library picks for the streaming GEMV of
@@ -268,8 +270,8 @@ int qmv_device_fault(unsigned int *code);
  *     the activations among the cluster's CTAs (default 2).
  * Returns QMV_ERR_TYPE for a non-weight type, QMV_ERR_SHAPE for values out of
  * range. */
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share,
-                   int cluster);
+qmv_status qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share,
+                          int cluster);
 
 /* Two more launch-geometry overrides of the streaming GEMV of `type`, for
  * sweeps (0 keeps the built-in choice; results are identical for every
@@ -278,7 +280,7 @@ int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_
  * the previous kernel on the stream (1..4, at most the ring's stages; the
  * rest of the ring is requested once the activations are staged).  Returns
  * QMV_ERR_TYPE for a non-weight type, QMV_ERR_SHAPE for values out of range. */
-int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
+qmv_status qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
 
 /* How many of the decoding warps (the first ones) request their early tiles
  * before the dependency wait (1..12; 0 = all of them, the default); the
@@ -286,7 +288,7 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
  * trade-off between weight bytes in flight across the kernel boundary and
  * the activation loads that queue behind them; results are identical for
  * every setting.  Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above. */
-int qmv_set_early_warps(int type, int early_warps);
+qmv_status qmv_set_early_warps(int type, int early_warps);
 
 /* Column count from which the plain GEMV of `type` (qmv_mul_mat_vec, its
  * fp32-input and fused forms) decodes with the tensor cores instead of the
@@ -300,7 +302,7 @@ int qmv_set_early_warps(int type, int early_warps);
  * fp32 rounding of the scaled sums (not bit for bit); q8_1 and fp32 input
  * stay bit-identical to each other at every setting.  Returns QMV_ERR_TYPE for
  * a non-weight type, QMV_ERR_SHAPE for values out of range. */
-int qmv_set_mma_min_cols(int type, int min_cols);
+qmv_status qmv_set_mma_min_cols(int type, int min_cols);
 
 /* Diagnostic: reads every 16-byte piece of the device buffer buf (bytes, a
  * multiple of 16; buf 16-byte aligned) once, with the GEMV weight stream's
@@ -309,7 +311,7 @@ int qmv_set_mma_min_cols(int type, int min_cols);
  * 4 bytes) is written only in the practically impossible case that one
  * thread's XOR of the words it read equals 0x9E3779B9 (this keeps the loads
  * from being optimised away).  Asynchronous on stream. */
-int qmv_read_bandwidth_probe(const void *buf, size_t bytes, unsigned int *sink, void *stream);
+qmv_status qmv_read_bandwidth_probe(const void *buf, size_t bytes, unsigned int *sink, void *stream);
 
 /* The launch the library would make for a plain (gate_up = 0) or fused
  * gate/up SwiGLU (gate_up = 1) GEMV of `type` with M rows, K columns and
@@ -330,8 +332,8 @@ typedef struct {
     int pre_tiles;      /* tiles per warp requested before the dependency wait */
     size_t smem;        /* dynamic shared bytes per CTA */
 } qmv_launch_info;
-int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, int fp32_input,
-                      qmv_launch_info *info);
+qmv_status qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, int fp32_input,
+                             qmv_launch_info *info);
 
 /* Environment override of the geometry knobs above, for tuning runs:
  * QMV_GEOM="type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K
@@ -353,7 +355,7 @@ int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, in
  * kernels and copies are waited for as usual, and the library's own kernels
  * never write weights except qmv_quantize_weights, which launches
  * ordinarily. */
-int qmv_set_pdl(int enable);
+qmv_status qmv_set_pdl(int enable);
 
 /* Checked mode (process-wide; off by default, or on when the environment
  * variable QMV_CHECKED is set to anything but "0" before the first call).
@@ -375,7 +377,7 @@ int qmv_set_pdl(int enable);
  * that stays inside the same allocation is not seen.  It costs one driver
  * query per pointer, so it is meant for debugging and tests; under CUDA graph
  * capture it runs once, when the call is captured.  Returns QMV_OK. */
-int qmv_set_checked(int enable);
+qmv_status qmv_set_checked(int enable);
 
 #ifdef __cplusplus
 }

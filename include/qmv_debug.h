@@ -1,0 +1,50 @@
+/*
+ * libqmv test-only entry points: exact integer intermediates of the GEMV and a
+ * way to make the library's one bounded wait run out on purpose.  Not part of
+ * the compute API; they exist so that tests can check the kernels bit for bit
+ * and exercise the fault path.  Conventions (ownership, asynchronous
+ * execution on `stream`, host validation before any launch, status codes)
+ * are those of qmv.h.
+ */
+#ifndef QMV_DEBUG_H
+#define QMV_DEBUG_H
+
+#include "qmv.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The exact int32 intermediates of the block formulas ("sumi" of the page
+ * "llama.cpp 源码完全拆解(十四)：mul_mat_vec_q", section "一次 vec_dot 的解剖",
+ * and dot1 / dot2 of vec_dot_q4_K_q8_1_impl_vmmq), computed by the same
+ * device code as qmv_mul_mat_vec, for bit-exact parity tests.  out is
+ * [ncols][M][n] int32 (device) with
+ *   Q4_0: n = K/32, per block sum of code*qy (code = raw nibble 0..15);
+ *   Q4_K: n = K/16, per 32-value sub-block the pair (dot1, dot2);
+ *   Q6_K: n = K/16, per 16-value sub-block sum (v-32)*qy.
+ * Arguments and limits as for qmv_mul_mat_vec.  out is cleared and written
+ * asynchronously on stream. */
+qmv_status qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const void *xq,
+                                   int ncols, int32_t *out, void *stream);
+
+/* qmv_mul_mat_vec_f32 (same arguments, limits and outputs), launched so that
+ * the bounded wait of its activation exchange runs out: in every cluster of
+ * CTAs that share the quantization of x, the CTA of rank 1 withholds its
+ * share from the others, and the CTA of rank 0 waits at most wait_ns
+ * nanoseconds for it (1 ns .. 1 s) before it gives up.  The CTAs that gave up
+ * record code 2 in the device fault word (qmv_device_fault) and write NaN to
+ * the outputs of their rows; every other output is the value
+ * qmv_mul_mat_vec_f32 computes.  The CTAs of rank 1 still receive rank 0's
+ * share and finish normally, so nothing waits without a bound and no store
+ * into a CTA arrives after it has exited.  Returns QMV_ERR_CONFIG, before
+ * launching, if the launch would not use clusters of CTAs (the exchange then
+ * does not exist); the argument errors of qmv_mul_mat_vec_f32 otherwise.  The
+ * pages have no counterpart: it tests the library's own fault reporting. */
+qmv_status qmv_debug_f32_withheld_share(int type, const void *W, int64_t M, int64_t K, const float *x,
+                                        int64_t ldx, int ncols, float *y, uint64_t wait_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMV_DEBUG_H */

@@ -9,6 +9,7 @@
 #include <tuple>
 
 #include "../../include/qmv.h"
+#include "../../include/qmv_debug.h"
 #include "gemv_tiles.cuh"
 #include "kernels.h"
 
@@ -59,6 +60,9 @@ constexpr int MAX_DEVICES = 64;
 constexpr size_t SMEM_RESERVE = 2048;  // static shared memory (MoE token lists) and alignment slack per CTA
 constexpr int F32_CLUSTER = 2;         // CTAs that share the quantization of fp32 activations (a TPC pair)
 constexpr int MAX_CLUSTER = 8;         // portable cluster size limit
+// MoE experts per call: the generic kernel gives every expert one grid row
+// plus one for the invalid ids, and gridDim.y is at most 65535
+constexpr int64_t MAX_EXPERTS = 65534;
 
 std::atomic<int> g_pdl{1};
 
@@ -688,7 +692,7 @@ size_t qmv_q8_1_bytes(int64_t K, int ncols)
     return static_cast<size_t>(ncols) * static_cast<size_t>(qmv_q8_1_padded_k(K) / QK8_1 * Q8_1_BYTES);
 }
 
-int qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *xq, void *stream)
+qmv_status qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *xq, void *stream)
 {
     if (!x || !xq) return QMV_ERR_NULL;
     if (K <= 0 || ncols <= 0 || ldx < K || K > (int64_t(1) << 28)) return QMV_ERR_SHAPE;
@@ -699,7 +703,7 @@ int qmv_quantize_q8_1(const float *x, int64_t K, int ncols, int64_t ldx, void *x
                                             static_cast<cudaStream_t>(stream), g_pdl.load() != 0));
 }
 
-int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t ldw, void *W, void *stream)
+qmv_status qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t ldw, void *W, void *stream)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (!w || !W) return QMV_ERR_NULL;
@@ -712,8 +716,8 @@ int qmv_quantize_weights(int type, const float *w, int64_t M, int64_t K, int64_t
                                                static_cast<cudaStream_t>(stream)));
 }
 
-int qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols, float *y,
-                    void *stream)
+qmv_status qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols, float *y,
+                           void *stream)
 {
     qmv_status s = check_common(type, W, M, K, xq, y);
     if (s != QMV_OK) return s;
@@ -729,8 +733,8 @@ int qmv_mul_mat_vec(int type, const void *W, int64_t M, int64_t K, const void *x
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_up, int64_t M, int64_t K,
-                                   const void *xq, int ncols, float *y, void *stream)
+qmv_status qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_up, int64_t M, int64_t K,
+                                          const void *xq, int ncols, float *y, void *stream)
 {
     qmv_status s = check_common(type, W_up, M, K, xq, y);
     if (s != QMV_OK) return s;
@@ -752,15 +756,15 @@ int qmv_mul_mat_vec_gate_up_swiglu(int type, const void *W_gate, const void *W_u
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const void *xq,
-                       const int32_t *ids, int n_tokens, int top_k, float *y, int32_t *dev_status, void *stream)
+qmv_status qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const void *xq,
+                              const int32_t *ids, int n_tokens, int top_k, float *y, int32_t *dev_status, void *stream)
 {
     qmv_status s = check_common(type, W, M, K, xq, y);
     if (s != QMV_OK) return s;
     if (!ids) return QMV_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(ids) % 4 || reinterpret_cast<uintptr_t>(dev_status) % 4) return QMV_ERR_ALIGN;
     if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
-    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
+    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > MAX_EXPERTS) return QMV_ERR_SHAPE;
     if ((s = check_gemv_ranges(type, M, K, &W, 1, n_expert, xq, nullptr, 0, n_tokens, y,
                                uint64_t(n_tokens) * top_k * M)) != QMV_OK)
         return s;
@@ -782,8 +786,8 @@ int qmv_mul_mat_vec_id(int type, const void *W, int64_t n_expert, int64_t M, int
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const float *x, int64_t ldx, int ncols,
-                        float *y, void *stream)
+qmv_status qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const float *x, int64_t ldx, int ncols,
+                               float *y, void *stream)
 {
     qmv_status s = check_common(type, W, M, K, x, y);
     if (s != QMV_OK) return s;
@@ -802,8 +806,32 @@ int qmv_mul_mat_vec_f32(int type, const void *W, int64_t M, int64_t K, const flo
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void *W_up, int64_t M, int64_t K,
-                                       const float *x, int64_t ldx, int ncols, float *y, void *stream)
+qmv_status qmv_debug_f32_withheld_share(int type, const void *W, int64_t M, int64_t K, const float *x, int64_t ldx,
+                                        int ncols, float *y, uint64_t wait_ns, void *stream)
+{
+    qmv_status s = check_common(type, W, M, K, x, y);
+    if (s != QMV_OK) return s;
+    if (ncols < 1 || ncols > 8) return QMV_ERR_NCOLS;
+    if (wait_ns < 1 || wait_ns > WAIT_LIMIT_NS) return QMV_ERR_SHAPE;
+    if ((s = check_f32(type, W, nullptr, K, ldx)) != QMV_OK) return s;
+    if ((s = check_gemv_ranges(type, M, K, &W, 1, 1, nullptr, x, ldx, ncols, y, uint64_t(ncols) * M)) != QMV_OK)
+        return s;
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W, M, K, nullptr, ncols);
+    p.xf = x;
+    p.ldx = ldx;
+    p.y = y;
+    Launch L;
+    if ((s = plan_f32(type, MODE_PLAIN, dev, p, ncols, 1, L)) != QMV_OK) return s;
+    if (L.cluster < 2 || L.fn == gemv_tiles_mma_fn_q4_K(MODE_PLAIN)) return QMV_ERR_CONFIG;
+    L.p.withhold = 1;
+    L.p.withhold_wait_ns = wait_ns;
+    return launch(L, static_cast<cudaStream_t>(stream));
+}
+
+qmv_status qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void *W_up, int64_t M, int64_t K,
+                                              const float *x, int64_t ldx, int ncols, float *y, void *stream)
 {
     qmv_status s = check_common(type, W_up, M, K, x, y);
     if (s != QMV_OK) return s;
@@ -828,16 +856,16 @@ int qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void 
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const float *x,
-                           int64_t ldx, const int32_t *ids, int n_tokens, int top_k, float *y, int32_t *dev_status,
-                           void *stream)
+qmv_status qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M, int64_t K, const float *x,
+                                  int64_t ldx, const int32_t *ids, int n_tokens, int top_k, float *y, int32_t *dev_status,
+                                  void *stream)
 {
     qmv_status s = check_common(type, W, M, K, x, y);
     if (s != QMV_OK) return s;
     if (!ids) return QMV_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(ids) % 4 || reinterpret_cast<uintptr_t>(dev_status) % 4) return QMV_ERR_ALIGN;
     if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
-    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
+    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > MAX_EXPERTS) return QMV_ERR_SHAPE;
     if ((s = check_f32(type, W, nullptr, K, ldx)) != QMV_OK) return s;
     if ((s = check_gemv_ranges(type, M, K, &W, 1, n_expert, nullptr, x, ldx, n_tokens, y,
                                uint64_t(n_tokens) * top_k * M)) != QMV_OK)
@@ -862,9 +890,9 @@ int qmv_mul_mat_vec_id_f32(int type, const void *W, int64_t n_expert, int64_t M,
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K, const void *xq,
-                          const float *x, int64_t ldx, int ncols, const float *bias, const float *gate_bias, float *y,
-                          void *stream)
+qmv_status qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K, const void *xq,
+                                 const float *x, int64_t ldx, int ncols, const float *bias, const float *gate_bias, float *y,
+                                 void *stream)
 {
     if (!xq && !x) return QMV_ERR_NULL;
     if (xq && x) return QMV_ERR_SHAPE;
@@ -898,10 +926,10 @@ int qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate, int64_
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int64_t n_expert, int64_t M, int64_t K,
-                             const void *xq, const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k,
-                             float *y, const void *W_shared_up, const void *W_shared_gate, float *y_shared,
-                             int32_t *dev_status, void *stream)
+qmv_status qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int64_t n_expert, int64_t M, int64_t K,
+                                    const void *xq, const float *x, int64_t ldx, const int32_t *ids, int n_tokens, int top_k,
+                                    float *y, const void *W_shared_up, const void *W_shared_gate, float *y_shared,
+                                    int32_t *dev_status, void *stream)
 {
     if (!xq && !x) return QMV_ERR_NULL;
     if (xq && x) return QMV_ERR_SHAPE;
@@ -916,7 +944,7 @@ int qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int
         reinterpret_cast<uintptr_t>(y_shared) % 4)
         return QMV_ERR_ALIGN;
     if (n_tokens < 1 || n_tokens > 8) return QMV_ERR_NCOLS;
-    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > 65535) return QMV_ERR_SHAPE;
+    if (top_k < 1 || top_k > 32 || n_expert < 1 || n_expert > MAX_EXPERTS) return QMV_ERR_SHAPE;
     if ((s = check_f32(type, W_up, W_gate, K, x ? ldx : K)) != QMV_OK) return s;
     if ((s = check_f32(type, W_shared_up, W_shared_gate, K, x ? ldx : K)) != QMV_OK) return s;
     {
@@ -956,8 +984,8 @@ int qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
-int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols, int32_t *out,
-                            void *stream)
+qmv_status qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const void *xq, int ncols, int32_t *out,
+                                   void *stream)
 {
     qmv_status s = check_common(type, W, M, K, xq, out);
     if (s != QMV_OK) return s;
@@ -978,7 +1006,7 @@ int qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K, const
     return launch(L, st);
 }
 
-int qmv_device_fault(unsigned int *code)
+qmv_status qmv_device_fault(unsigned int *code)
 {
     if (!code) return QMV_ERR_NULL;
     DevInfo dev;
@@ -991,7 +1019,7 @@ int qmv_device_fault(unsigned int *code)
     return QMV_OK;
 }
 
-int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share, int cluster)
+qmv_status qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_per_sm, int smem_share, int cluster)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (threads < 0 || threads > TILE_MAX_THREADS || threads % 32 || slice_units < 0 || stages < 0 || stages > 16 ||
@@ -1007,7 +1035,7 @@ int qmv_set_tuning(int type, int threads, int slice_units, int stages, int ctas_
     return QMV_OK;
 }
 
-int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles)
+qmv_status qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (dec_warps < 0 || dec_warps > TILE_MAX_THREADS / 32 || pre_tiles < 0 || pre_tiles > TILE_MAX_STAGES)
@@ -1018,7 +1046,7 @@ int qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles)
     return QMV_OK;
 }
 
-int qmv_read_bandwidth_probe(const void *buf, size_t bytes, unsigned int *sink, void *stream)
+qmv_status qmv_read_bandwidth_probe(const void *buf, size_t bytes, unsigned int *sink, void *stream)
 {
     if (!buf || !sink) return QMV_ERR_NULL;
     if (bytes == 0 || bytes % 16) return QMV_ERR_SHAPE;
@@ -1032,7 +1060,7 @@ int qmv_read_bandwidth_probe(const void *buf, size_t bytes, unsigned int *sink, 
                                          static_cast<cudaStream_t>(stream)));
 }
 
-int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, int fp32_input, qmv_launch_info *info)
+qmv_status qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, int fp32_input, qmv_launch_info *info)
 {
     if (!info) return QMV_ERR_NULL;
     *info = qmv_launch_info{};
@@ -1071,7 +1099,7 @@ int qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int ncols, in
     return QMV_OK;
 }
 
-int qmv_set_early_warps(int type, int early_warps)
+qmv_status qmv_set_early_warps(int type, int early_warps)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (early_warps < 0 || early_warps > TILE_MAX_THREADS / 32) return QMV_ERR_SHAPE;
@@ -1079,7 +1107,7 @@ int qmv_set_early_warps(int type, int early_warps)
     return QMV_OK;
 }
 
-int qmv_set_mma_min_cols(int type, int min_cols)
+qmv_status qmv_set_mma_min_cols(int type, int min_cols)
 {
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (min_cols < 0 || min_cols > 9) return QMV_ERR_SHAPE;
@@ -1087,13 +1115,13 @@ int qmv_set_mma_min_cols(int type, int min_cols)
     return QMV_OK;
 }
 
-int qmv_set_pdl(int enable)
+qmv_status qmv_set_pdl(int enable)
 {
     g_pdl = enable ? 1 : 0;
     return QMV_OK;
 }
 
-int qmv_set_checked(int enable)
+qmv_status qmv_set_checked(int enable)
 {
     g_checked = enable ? 1 : 0;
     return QMV_OK;

@@ -170,7 +170,7 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
                             if (i < nw) asm volatile("st.shared.u32 [%0], %1;" ::"r"(sc + off[i]), "r"(val[i]) : "memory");
                     }
                     for (uint32_t q = 0; q < ncta; ++q) {
-                        if (q == crank) continue;
+                        if (q == crank || (p.withhold && crank == 1)) continue;
                         const uint32_t bq = mapa_shared(xbar, q);
                         st_async_v2(mapa_shared(dq, q), w0, w1, bq);
                         if (j == 0) {
@@ -488,7 +488,18 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         // a partner stores here is counted, so none is still in flight after
         // the wait and no CTA can exit while a partner writes to it)
         __syncthreads();
-        if (!mbar_wait_bounded(xbar, 0) && threadIdx.x == 0 && p.fault) atomicOr(p.fault, FAULT_CLUSTER_STAGING);
+        const unsigned long long lim = (p.withhold && crank == 0) ? p.withhold_wait_ns : WAIT_LIMIT_NS;
+        if (__syncthreads_or(!mbar_wait_bounded(xbar, 0, lim))) {
+            // A partner's share never arrived: nothing is computed.  NaN marks
+            // every output of this CTA's rows invalid, the fault word tells the
+            // host, and the CTA leaves once its own weight copies have landed.
+            if (threadIdx.x == 0 && p.fault) atomicOr(p.fault, FAULT_CLUSTER_STAGING);
+            const int64_t r_end = min64(p.M, (g_begin + my_groups) * RW);
+            for (int64_t r = g_begin * RW + lane; r < r_end; r += 32)
+                for (int c = 0; c < p.ncols; ++c) p.y[(size_t)c * p.ldy + r] = __int_as_float(0x7fc00000);
+            cp_async_wait(0);
+            return;
+        }
     } else {
         __syncthreads();
     }

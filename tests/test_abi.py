@@ -27,7 +27,8 @@ def qlib():
 
 
 def _declared_symbols():
-    text = open(os.path.join(ROOT, "include", "qmv.h")).read()
+    inc = os.path.join(ROOT, "include")
+    text = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(qmv_[a-z0-9_]+)\s*\(", text)))
 
@@ -82,12 +83,20 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_mul_mat_vec_id(12, p, 8, 16, 256, p, p, 9, 2, p, nul, nul) == 4
     assert L.qmv_mul_mat_vec_id(12, p, 0, 16, 256, p, p, 4, 2, p, nul, nul) == 3
     assert L.qmv_mul_mat_vec_id(12, p, 8, 16, 256, p, p, 4, 33, p, nul, nul) == 3
+    assert L.qmv_mul_mat_vec_id(12, p, 65535, 16, 256, p, p, 4, 2, p, nul, nul) == 3  # grid rows: at most 65534
     # quantizers
     assert L.qmv_quantize_q8_1(nul, 256, 1, 256, p, nul) == 1
     assert L.qmv_quantize_q8_1(p, 256, 1, 100, p, nul) == 3
     assert L.qmv_quantize_weights(12, p, 4, 100, 100, p, nul) == 3
     assert L.qmv_quantize_weights(9, p, 4, 256, 256, p, nul) == 2
     assert L.qmv_debug_subblock_sums(14, p, 4, 256, p, 0, p, nul) == 4
+    # the withheld-share test entry: the fp32 call's checks, and a wait limit of 1 ns .. 1 s
+    wh = L.qmv_debug_f32_withheld_share
+    assert wh(12, p, 16, 4096, p, 4096, 1, p, 0, nul) == 3
+    assert wh(12, p, 16, 4096, p, 4096, 1, p, 1000000001, nul) == 3
+    assert wh(14, p, 16, 2304, p, 2304, 1, p, 1000, nul) == 3
+    assert wh(12, p, 16, 4096, p, 4096, 9, p, 1000, nul) == 4
+    assert wh(12, ctypes.c_void_p(0x1008), 16, 4096, p, 4096, 1, p, 1000, nul) == 5
     # fused fp32-input calls: the tile kernel's shapes (Q4_0/Q4_K: K % 256, Q6_K: K % 2048), 16-byte aligned W
     assert L.qmv_mul_mat_vec_f32(14, p, 16, 2304, p, 2304, 1, p, nul) == 3
     assert L.qmv_mul_mat_vec_f32(2, p, 16, 96, p, 96, 1, p, nul) == 3
@@ -208,13 +217,13 @@ def test_geometry_environment_override(qlib, spec, want):
 
 
 def test_header_is_plain_c99(tmp_path):
-    """include/qmv.h is a C header: it compiles as C99 with every warning an
+    """include/qmv.h and qmv_debug.h are C headers: they compile as C99 with every warning an
     error, and a C program declares and calls through it."""
     gcc = shutil.which("gcc")
     if gcc is None:
         pytest.skip("gcc not available")
     src = tmp_path / "use_header.c"
-    src.write_text('#include "qmv.h"\n'
+    src.write_text('#include "qmv.h"\n#include "qmv_debug.h"\n'
                    "int main(void) { qmv_launch_info info; (void)info;\n"
                    "  return qmv_status_str(QMV_OK) != 0 && qmv_version() > 0 ? 0 : 1; }\n")
     import subprocess
