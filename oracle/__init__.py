@@ -60,10 +60,12 @@ def lib():
         L.oracle_gemv_plain.argtypes = [ctypes.c_int, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
         L.oracle_gemv_formula.argtypes = [ctypes.c_int, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp]
         L.oracle_gemv_formula_mt.argtypes = [ctypes.c_int, _vp, _i64, _i64, _vp, _i64, _vp, _vp, ctypes.c_int]
+        L.oracle_gemv_int_f32.argtypes = [ctypes.c_int, _vp, _i64, _i64, _vp, _i64, _vp, ctypes.c_int]
         L.oracle_subblock_sums.argtypes = [ctypes.c_int, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
         for name in ("oracle_quantize_q8_1", "oracle_quantize_rows", "oracle_dequantize_rows",
                      "oracle_dequantize_q8_1", "oracle_dequantize_row_q4_K_f32", "oracle_gemv_plain",
-                     "oracle_gemv_formula", "oracle_gemv_formula_mt", "oracle_subblock_sums"):
+                     "oracle_gemv_formula", "oracle_gemv_formula_mt", "oracle_gemv_int_f32",
+                     "oracle_subblock_sums"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -204,6 +206,16 @@ def gemv_formula_mt(t: int, W: np.ndarray, M: int, K: int, xq: np.ndarray, ncols
     _check(lib().oracle_gemv_formula_mt(t, _p(W), M, K, _p(xq), ncols, _p(y), _p(l1), int(nthreads)),
            "gemv_formula_mt")
     return y, l1
+
+
+def gemv_int_f32(t: int, W: np.ndarray, M: int, K: int, xq: np.ndarray, ncols: int, nthreads: int = 1):
+    """The method's integer formula in fp32 over all rows (int32 block sums,
+    fp32 scaling), threaded by rows: y float32 [ncols][M].  A CPU baseline."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    y = np.empty((ncols, M), dtype=np.float32)
+    _check(lib().oracle_gemv_int_f32(t, _p(W), M, K, _p(xq), ncols, _p(y), int(nthreads)), "gemv_int_f32")
+    return y
 
 
 def subblock_sums(t: int, W: np.ndarray, M: int, K: int, xq: np.ndarray, ncols: int, rows=None):

@@ -503,6 +503,64 @@ static void formula_row(int type, const uint8_t *wrow, int64_t K, const uint8_t 
     if (l1o) *l1o = l1;
 }
 
+/* One row, one column, by the method's integer formula in fp32: exact int32
+ * block sums, then the block scaling of formula_row evaluated in fp32 (each
+ * product and sum rounded to fp32 in the order written), the way the method's
+ * kernels scale their dp4a sums ("mul_mat_vec_q" page, vec_dot_q4_0_q8_1_impl,
+ * vec_dot_q4_K_q8_1_impl_vmmq, the Q6_K vec_dot).  The CPU counterpart of the
+ * GPU arithmetic, timed as a second CPU baseline. */
+static float int_formula_row(int type, const uint8_t *wrow, int64_t K, const uint8_t *xqc)
+{
+    float y = 0.0f;
+    if (type == ORACLE_Q4_0) {
+        for (int64_t b = 0; b < K / QK4_0; ++b) {
+            const uint8_t *blk = wrow + b * Q4_0_BYTES;
+            const uint8_t *xb = xqc + b * Q8_1_BYTES;
+            int32_t sumi = 0;
+            for (int e = 0; e < 32; ++e) sumi += q4_0_code(blk, e) * (int8_t)xb[4 + e];
+            const float d4 = oracle_f16_to_f32(rd16(blk)), d8 = oracle_f16_to_f32(rd16(xb));
+            const float s = oracle_f16_to_f32(rd16(xb + 2));
+            const float scaled = d8 * (float)sumi, corr = 8.0f * s;
+            const float term = d4 * (scaled - corr);
+            y += term;
+        }
+    } else if (type == ORACLE_Q4_K) {
+        for (int64_t b = 0; b < K / QK_K; ++b) {
+            const uint8_t *blk = wrow + b * Q4_K_BYTES;
+            const float d = oracle_f16_to_f32(rd16(blk)), dmin = oracle_f16_to_f32(rd16(blk + 2));
+            for (int sb = 0; sb < 8; ++sb) {
+                const uint8_t *xb = xqc + (b * 8 + sb) * Q8_1_BYTES;
+                int32_t dot1 = 0, dot2 = 0;
+                for (int i = 0; i < 32; ++i) {
+                    const int qy = (int8_t)xb[4 + i];
+                    dot1 += q4_K_code(blk, 32 * sb + i) * qy;
+                    dot2 += qy;
+                }
+                int sc, m;
+                unpack_scale_min_q4_K(blk + 4, sb, &sc, &m);
+                const float d8 = oracle_f16_to_f32(rd16(xb));
+                const float t1 = (d * (float)sc) * (d8 * (float)dot1);
+                const float t2 = (dmin * (float)m) * (d8 * (float)dot2);
+                y += t1 - t2;
+            }
+        }
+    } else {
+        for (int64_t b = 0; b < K / QK_K; ++b) {
+            const uint8_t *blk = wrow + b * Q6_K_BYTES;
+            const float d = oracle_f16_to_f32(rd16(blk + 208));
+            for (int sb = 0; sb < 16; ++sb) {
+                const uint8_t *xb = xqc + (b * 8 + sb / 2) * Q8_1_BYTES;
+                int32_t sumi = 0;
+                for (int i = 0; i < 16; ++i)
+                    sumi += (q6_K_code(blk, 16 * sb + i) - 32) * (int8_t)xb[4 + 16 * (sb % 2) + i];
+                const float t = (d * (float)(int8_t)blk[192 + sb]) * (oracle_f16_to_f32(rd16(xb)) * (float)sumi);
+                y += t;
+            }
+        }
+    }
+    return y;
+}
+
 int oracle_gemv_formula(int type, const uint8_t *W, int64_t M, int64_t K, const uint8_t *xq,
                         int64_t ncols, const int64_t *rows, int64_t nrows, double *y, double *l1)
 {
@@ -528,6 +586,7 @@ typedef struct {
     const uint8_t *W, *xq;
     int64_t M, K, ncols, rb, xstride;
     double *y, *l1;
+    float *yf; /* set: the fp32 integer formula instead of the fp64 one */
     atomic_llong next;
 } mt_job;
 
@@ -541,11 +600,28 @@ static void *mt_worker(void *arg)
         if (r0 >= j->M) break;
         long long r1 = r0 + MT_CHUNK < j->M ? r0 + MT_CHUNK : j->M;
         for (long long r = r0; r < r1; ++r)
-            for (int64_t c = 0; c < j->ncols; ++c)
-                formula_row(j->type, j->W + r * j->rb, j->K, j->xq + c * j->xstride,
-                            &j->y[c * j->M + r], j->l1 ? &j->l1[c * j->M + r] : NULL);
+            for (int64_t c = 0; c < j->ncols; ++c) {
+                if (j->yf)
+                    j->yf[c * j->M + r] = int_formula_row(j->type, j->W + r * j->rb, j->K, j->xq + c * j->xstride);
+                else
+                    formula_row(j->type, j->W + r * j->rb, j->K, j->xq + c * j->xstride,
+                                &j->y[c * j->M + r], j->l1 ? &j->l1[c * j->M + r] : NULL);
+            }
     }
     return NULL;
+}
+
+static void run_mt(mt_job *job, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    atomic_init(&job->next, 0);
+    pthread_t th[512];
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[started], NULL, mt_worker, job) == 0) ++started;
+    mt_worker(job);
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
 }
 
 int oracle_gemv_formula_mt(int type, const uint8_t *W, int64_t M, int64_t K, const uint8_t *xq,
@@ -554,17 +630,21 @@ int oracle_gemv_formula_mt(int type, const uint8_t *W, int64_t M, int64_t K, con
     int rc = gemv_args_ok(type, W, M, K, xq, ncols, NULL, M);
     if (rc) return rc;
     if (!y) return -3;
-    if (nthreads < 1) nthreads = 1;
-    if (nthreads > 512) nthreads = 512;
     mt_job job = {type, W, xq, M, K, ncols, oracle_row_bytes(type, K),
-                  oracle_q8_1_padded_k(K) / QK8_1 * Q8_1_BYTES, y, l1, 0};
-    atomic_init(&job.next, 0);
-    pthread_t th[512];
-    int started = 0;
-    for (int t = 1; t < nthreads; ++t)
-        if (pthread_create(&th[started], NULL, mt_worker, &job) == 0) ++started;
-    mt_worker(&job);
-    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+                  oracle_q8_1_padded_k(K) / QK8_1 * Q8_1_BYTES, y, l1, NULL, 0};
+    run_mt(&job, nthreads);
+    return 0;
+}
+
+int oracle_gemv_int_f32(int type, const uint8_t *W, int64_t M, int64_t K, const uint8_t *xq,
+                        int64_t ncols, float *y, int nthreads)
+{
+    int rc = gemv_args_ok(type, W, M, K, xq, ncols, NULL, M);
+    if (rc) return rc;
+    if (!y) return -3;
+    mt_job job = {type, W, xq, M, K, ncols, oracle_row_bytes(type, K),
+                  oracle_q8_1_padded_k(K) / QK8_1 * Q8_1_BYTES, NULL, NULL, y, 0};
+    run_mt(&job, nthreads);
     return 0;
 }
 

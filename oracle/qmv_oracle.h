@@ -83,6 +83,11 @@ int oracle_gemv_formula(int type, const uint8_t *W, int64_t M, int64_t K, const 
  * that claim row chunks from a shared counter (timed CPU baseline). */
 int oracle_gemv_formula_mt(int type, const uint8_t *W, int64_t M, int64_t K, const uint8_t *xq,
                            int64_t ncols, double *y, double *l1, int nthreads);
+/* The method's integer formula in fp32 over all rows (int32 block sums, fp32
+ * block scaling): y [ncols][M] float; threaded like oracle_gemv_formula_mt.
+ * A CPU baseline, agreeing with oracle_gemv_formula within fp32 rounding. */
+int oracle_gemv_int_f32(int type, const uint8_t *W, int64_t M, int64_t K, const uint8_t *xq,
+                        int64_t ncols, float *y, int nthreads);
 
 /* Per-sub-block integer sums, [ncols][nrows][n] int32:
  *   Q4_0: n = K/32, sum over the block of q*qy with q the raw nibble 0..15;

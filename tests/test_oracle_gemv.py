@@ -222,3 +222,54 @@ def test_shared_expert_is_every_token_routed_to_one_matrix():
     Wd = oracle.dequantize_rows(oracle.Q4_K, Ws, K).astype(np.float64)
     xd = oracle.dequantize_q8_1(xq, K).astype(np.float64)
     assert np.allclose(ys, xd @ Wd.T, rtol=1e-12, atol=1e-12 * np.abs(l1).max())
+
+
+# ---- the fp32 integer-formula GEMV (the second CPU baseline) -------------------
+@pytest.mark.parametrize("t", TYPES)
+def test_int_f32_formula_within_fp32_rounding_of_the_fp64_formula(t):
+    M, K, nc = 24, 2048, 3
+    for W in (oracle.random_blocks(t, M, K, seed=71),
+              oracle.quantize_rows(t, synthetic.weights_f32(72, M, K))):
+        xq = _xq(73, nc, K, 0.01)
+        y64, l1 = oracle.gemv_formula(t, W, M, K, xq, nc)
+        y32 = oracle.gemv_int_f32(t, W, M, K, xq, nc).astype(np.float64)
+        # per row: K/16 scaled terms, each with at most four fp32 roundings,
+        # summed in fp32: |error| <= (4 + K/16) * 2^-24 * L1 (first order)
+        assert np.all(np.abs(y32 - y64) <= (4 + K / 16) * 2.0**-24 * l1 + 1e-30)
+
+
+def _integer_q8_1(seed, ncols, K):
+    """q8_1 blocks with d = 1 and codes in [-7, 7] (|sum| < 2048, so s = sum(q)
+    is an exact half): every block product is an exact small integer."""
+    nb = oracle.q8_1_padded_k(K) // 32
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = rng.integers(-7, 8, size=(ncols, nb, 32))
+    q[:, K // 32:, :] = 0
+    b = np.zeros((ncols, nb, 36), dtype=np.uint8)
+    b[..., 0:2] = [0x00, 0x3C]
+    sbits = oracle.f32_to_f16_bits(q.sum(axis=2).astype(np.float32))
+    b[..., 2] = sbits & 0xFF
+    b[..., 3] = sbits >> 8
+    b[..., 4:] = q.astype(np.int8).view(np.uint8)
+    return b.reshape(ncols, nb * 36)
+
+
+@pytest.mark.parametrize("t", TYPES)
+def test_int_f32_formula_exact_on_integer_cases(t):
+    # unit scales and integer activations: y is an integer below 2^24, which
+    # fp32 holds exactly, so both formulas must give the same value exactly
+    M, K, nc = 9, 1024, 2
+    W = _unit_scale_blocks(t, M, K, seed=74)
+    xq = _integer_q8_1(75, nc, K)
+    y64, _ = oracle.gemv_formula(t, W, M, K, xq, nc)
+    assert np.array_equal(y64, np.round(y64)) and np.all(np.abs(y64) < 2**24)
+    assert np.array_equal(oracle.gemv_int_f32(t, W, M, K, xq, nc).astype(np.float64), y64)
+
+
+@pytest.mark.parametrize("t", TYPES)
+def test_int_f32_threads_agree(t):
+    M, K, nc = 37, 512, 2
+    W = oracle.random_blocks(t, M, K, seed=76)
+    xq = _xq(77, nc, K)
+    y1 = oracle.gemv_int_f32(t, W, M, K, xq, nc, nthreads=1)
+    assert np.array_equal(oracle.gemv_int_f32(t, W, M, K, xq, nc, nthreads=5), y1)
