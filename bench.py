@@ -61,7 +61,7 @@ MMA_MIN_COLS = 9
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
 TRAFFIC = {"csrc_sha": "b53e6f5c2322b91f", "bytes_per_launch": 28530592,
-           "shape": "mean of the step's launch kinds qkv, o, gate+up, down (profiles/gemv_tiles_q4_K_down_fused.md)"}
+           "shape": "mean of the step's launch kinds qkv, o, gate+up, down"}
 
 
 def row_bytes(M, K):
@@ -189,12 +189,36 @@ def max_over_ranks(v, world, device=None):
 
 
 # ---- CPU oracle timing ----------------------------------------------------------
-def oracle_rate(min_seconds=2.0, rows_frac=1.0, nthreads=None):
-    """Weight GB/s of the CPU oracle on one layer's matrix mix: each distinct
-    shape (a row sample of it when rows_frac < 1) is timed, then weighted by
-    how often it occurs in a layer.  Returns (GB/s, threads, sample text)."""
-    import numpy as np
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
 
+    return platform.machine()
+
+
+_CPU_INPUTS = {}
+
+
+def oracle_rate(min_seconds=2.0, rows_frac=1.0, nthreads=None, kind="fp64"):
+    """Weight GB/s of a CPU GEMV on one layer's matrix mix: each distinct
+    shape (a row sample of it when rows_frac < 1) is timed, then weighted by
+    how often it occurs in a layer.  kind "fp64": the oracle's fp64 block
+    formula; "int_f32": the oracle's integer formula in fp32 (int32 block
+    sums, fp32 scaling).  Returns (GB/s, threads, sample text)."""
     import oracle
     import synthetic
 
@@ -204,11 +228,18 @@ def oracle_rate(min_seconds=2.0, rows_frac=1.0, nthreads=None):
     bytes_layer = 0.0
     for si, (name, (M, K)) in enumerate(SHAPES.items()):
         Ms = max(64, int(M * rows_frac))
-        W = oracle.quantize_rows(oracle.Q4_K, synthetic.weights_f32(31 + si, Ms, K))
-        xq = oracle.quantize_q8_1(synthetic.activations_f32(41 + si, 1, K, outlier_frac=0.01))
+        if (si, M) not in _CPU_INPUTS:  # quantized once, shared by every leg
+            _CPU_INPUTS[(si, M)] = (
+                oracle.quantize_rows(oracle.Q4_K, synthetic.weights_f32(31 + si, M, K)),
+                oracle.quantize_q8_1(synthetic.activations_f32(41 + si, 1, K, outlier_frac=0.01)))
+        W_all, xq = _CPU_INPUTS[(si, M)]
+        W = W_all[:Ms]
         reps, t0 = 0, time.perf_counter()
         while True:
-            oracle.gemv_formula_mt(oracle.Q4_K, W, Ms, K, xq, 1, nthreads)
+            if kind == "fp64":
+                oracle.gemv_formula_mt(oracle.Q4_K, W, Ms, K, xq, 1, nthreads)
+            else:
+                oracle.gemv_int_f32(oracle.Q4_K, W, Ms, K, xq, 1, nthreads)
             reps += 1
             el = time.perf_counter() - t0
             if el >= min_seconds / 3 and reps >= 2:
@@ -216,10 +247,25 @@ def oracle_rate(min_seconds=2.0, rows_frac=1.0, nthreads=None):
         per_row = el / reps / Ms
         t_layer += count[name] * M * per_row
         bytes_layer += count[name] * M * row_bytes(M, K)
-    sample = (f"oracle fp64 block-formula GEMV on {nthreads} host threads; one layer's matrix mix "
+    what = "fp64 block-formula" if kind == "fp64" else "fp32 integer-formula"
+    sample = (f"oracle {what} GEMV on {nthreads} host thread(s); one layer's matrix mix "
               f"(row fraction {rows_frac:g} of 4096x4096, 11008x4096, 4096x11008, each repeated >= "
               f"{min_seconds / 3:.1f} s) scaled by the layer's counts 4/2/1")
     return bytes_layer / t_layer / 1e9, nthreads, sample
+
+
+def cpu_baselines(seconds):
+    """The CPU legs: the oracle's fp64 formula and its fp32 integer formula,
+    each on all host cores and on one thread (about `seconds` of CPU work each)."""
+    gbs, cores, sample = oracle_rate(min_seconds=seconds)
+    one, _, _ = oracle_rate(min_seconds=seconds, rows_frac=0.25, nthreads=1)
+    gi, _, sample_i = oracle_rate(min_seconds=seconds, kind="int_f32")
+    gi1, _, _ = oracle_rate(min_seconds=seconds, rows_frac=0.25, nthreads=1, kind="int_f32")
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "one_thread_gbs": round(one, 4),
+            "int_f32": {"value": round(gi, 4), "one_thread_gbs": round(gi1, 4), "sample": sample_i},
+            "cpu_model": cpu_model(),
+            "note": "one-thread legs on a quarter of each matrix's rows; GB/s of Q4_K weights"}
 
 
 # ---- reference arm: the CPU oracle as it stands ------------------------------------------
@@ -319,13 +365,28 @@ def measure_ceilings(q, torch, stream, device, reps=10):
     return out
 
 
-def measure_configs(q, torch, stream, device, reps):
-    """Per-call time of the GEMV at each workload the benchmark is quoted on,
-    each launch chained over distinct weight copies (so consecutive calls do not
-    share L2) and timed with CUDA events as a graph of launches."""
-    import numpy as np
+def l2_bytes(torch, device):
+    return int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (126 << 20))
 
+
+def copies_for(torch, device, nbytes, floor=4):
+    """Distinct weight copies a chain rotates through so that it reads at least
+    three times the L2 size before any copy comes round again."""
+    need = 3 * l2_bytes(torch, device)
+    return max(floor, -(-need // nbytes))
+
+
+def measure_configs(q, torch, stream, device, reps, peak):
+    """Per-call time of the GEMV at each workload the benchmark is quoted on.
+    Each launch is chained over distinct weight copies totalling at least three
+    times the L2 size (so every call streams its weights from HBM) and timed
+    with CUDA events as a graph of launches; a cold single call after an L2
+    flush is timed beside it as a cross-check.  Returns (summary, detail):
+    summary name -> [us per call, weight GB/s, fraction of the peak]."""
     import synthetic
+
+    l2 = l2_bytes(torch, device)
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=device)
 
     def chain_time(calls):
         g = torch.cuda.CUDAGraph()
@@ -346,6 +407,21 @@ def measure_configs(q, torch, stream, device, reps):
             stream.synchronize()
         return e0.elapsed_time(e1) * 1e3 / (reps * len(calls))
 
+    def cold_time(call, trials=5):
+        """One call after writing 2x L2 of other data, events around the call alone (median)."""
+        ts = []
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(trials):
+                flush_buf.fill_(1)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                stream.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
     def weights(t, M, K, n, seed):
         with torch.cuda.stream(stream):
             ws = [q.quantize_weights(t, synthetic.device_normal_f32(seed + i, (M, K), 0.02, device), stream=stream)
@@ -357,99 +433,103 @@ def measure_configs(q, torch, stream, device, reps):
         x = torch.from_numpy(synthetic.activations_f32(seed, nc, K, outlier_frac=outl)).to(device)
         return q.quantize_q8_1(x, stream=stream)
 
-    out = {}
+    summary, detail = {}, {}
     y_flat = torch.empty(8 * 32000, dtype=torch.float32, device=device)
 
     def yv(nc, M):  # a contiguous [nc][M] output
         return y_flat[: nc * M].view(nc, M)
 
-    def plain(name, t, M, K, n, seed, ncols=1, outl=0.0):
+    def record(name, us, wbytes, n_copies, cold=None, **extra):
+        gbs = wbytes / us / 1e3
+        summary[name] = [round(us, 3), round(gbs, 1), round(gbs / peak, 4)]
+        detail[name] = {"us_per_call": round(us, 3), "weight_gbs": round(gbs, 1), "weight_bytes": wbytes,
+                        "distinct_weight_bytes": n_copies * wbytes, **extra}
+        if cold is not None:
+            detail[name]["cold_us"] = round(cold, 3)
+
+    def plain(name, t, M, K, seed, ncols=1, outl=0.0):
+        wb = M * q.row_bytes(t, K)
+        n = copies_for(torch, device, wb)
         ws = weights(t, M, K, n, seed)
         xq = xq_of(K, ncols, seed + 99, outl)
-        us = chain_time([lambda W=W: q.mul_mat_vec(t, W, M, K, xq, ncols, out=yv(ncols, M), stream=stream)
-                         for W in ws])
-        wb = ws[0].numel()
-        out[name] = {"us_per_call": round(us, 3), "weight_gbs": round(wb / us / 1e3, 1)}
+        calls = [lambda W=W: q.mul_mat_vec(t, W, M, K, xq, ncols, out=yv(ncols, M), stream=stream) for W in ws]
+        record(name, chain_time(calls), wb, n, cold_time(calls[0]))
         del ws
         torch.cuda.empty_cache()
 
-    plain("q4_0 4096x4096", q.Q4_0, 4096, 4096, 8, 3_000_000)
-    plain("q6_K 32000x4096", q.Q6_K, 32000, 4096, 4, 3_000_100)
-    plain("q6_K 4096x14336", q.Q6_K, 4096, 14336, 8, 3_000_200)
-    ws = weights(q.Q4_K, 14336, 4096, 8, 3_000_300)
-    sweep = {}
+    plain("q4_0 4096x4096", q.Q4_0, 4096, 4096, 3_000_000)
+    plain("q6_K 32000x4096", q.Q6_K, 32000, 4096, 3_000_100)
+    plain("q6_K 4096x14336", q.Q6_K, 4096, 14336, 3_000_200)
+    M, K = 14336, 4096
+    wb = M * q.row_bytes(q.Q4_K, K)
+    n14 = max(12, copies_for(torch, device, wb))
+    ws = weights(q.Q4_K, M, K, n14, 3_000_300)
     for nc in range(1, 9):
-        xq = xq_of(4096, nc, 3_000_400 + nc)
-        calls = [lambda W=W: q.mul_mat_vec(q.Q4_K, W, 14336, 4096, xq, nc, out=yv(nc, 14336), stream=stream)
-                 for W in ws]
-        # both decodes at every column count (the crossover), then the default choice
-        both = {}
-        for tag, min_cols in (("dp4a", 9), ("mma", 1)):
-            q.set_mma_min_cols(q.Q4_K, min_cols)
-            both[tag + "_us"] = round(chain_time(calls), 3)
-        q.set_mma_min_cols(q.Q4_K, 0)
+        xq = xq_of(K, nc, 3_000_400 + nc)
+        calls = [lambda W=W: q.mul_mat_vec(q.Q4_K, W, M, K, xq, nc, out=yv(nc, M), stream=stream) for W in ws]
+        # the default decode, then the opt-in tensor-core decode at the same column count
         us = chain_time(calls)
-        sweep[str(nc)] = {"us_per_call": round(us, 3), "weight_gbs": round(ws[0].numel() / us / 1e3, 1),
-                          "decode": "mma" if nc >= MMA_MIN_COLS else "dp4a", **both}
-    out["q4_K 14336x4096 ncols 1..8"] = sweep
+        cold = cold_time(calls[0]) if nc == 1 else None
+        q.set_mma_min_cols(q.Q4_K, 1)
+        us_mma = chain_time(calls)
+        q.set_mma_min_cols(q.Q4_K, 0)
+        record(f"q4_K 14336x4096 nc{nc}", us, wb, n14, cold, mma_us=round(us_mma, 3))
     # the same sweep for Q6_K (4096x14336, the down projection of an 8B-class FFN)
-    ws6 = weights(q.Q6_K, 4096, 14336, 6, 3_000_450)
-    sweep6 = {}
+    M6, K6 = 4096, 14336
+    wb6 = M6 * q.row_bytes(q.Q6_K, K6)
+    n6 = copies_for(torch, device, wb6)
+    ws6 = weights(q.Q6_K, M6, K6, n6, 3_000_450)
     for nc in range(1, 9):
-        xq = xq_of(14336, nc, 3_000_460 + nc)
-        us = chain_time([lambda W=W: q.mul_mat_vec(q.Q6_K, W, 4096, 14336, xq, nc, out=yv(nc, 4096), stream=stream)
-                         for W in ws6])
-        sweep6[str(nc)] = {"us_per_call": round(us, 3), "weight_gbs": round(ws6[0].numel() / us / 1e3, 1)}
-    out["q6_K 4096x14336 ncols 1..8"] = sweep6
+        xq = xq_of(K6, nc, 3_000_460 + nc)
+        calls = [lambda W=W: q.mul_mat_vec(q.Q6_K, W, M6, K6, xq, nc, out=yv(nc, M6), stream=stream) for W in ws6]
+        record(f"q6_K 4096x14336 nc{nc}", chain_time(calls), wb6, n6)
     del ws6
     torch.cuda.empty_cache()
-    # fused gate/up, two 14336x4096 matrices per call
-    xq = xq_of(4096, 1, 3_000_500)
-    pairs = [(ws[2 * i], ws[2 * i + 1]) for i in range(4)]
-    us = chain_time([lambda g=g, u=u: q.mul_mat_vec_gate_up_swiglu(q.Q4_K, g, u, 14336, 4096, xq, 1,
-                                                                    out=yv(1, 14336), stream=stream) for g, u in pairs])
-    out["q4_K gate+up 2x14336x4096 swiglu"] = {"us_per_call": round(us, 3),
-                                               "weight_gbs": round(2 * ws[0].numel() / us / 1e3, 1)}
+    # fused gate/up, two 14336x4096 matrices per call (pairs of the copies above)
+    xq = xq_of(K, 1, 3_000_500)
+    pairs = [(ws[2 * i], ws[2 * i + 1]) for i in range(n14 // 2)]
+    calls = [lambda g=g, u=u: q.mul_mat_vec_gate_up_swiglu(q.Q4_K, g, u, M, K, xq, 1, out=yv(1, M), stream=stream)
+             for g, u in pairs]
+    record("q4_K gate+up 2x14336x4096", chain_time(calls), 2 * wb, len(pairs), cold_time(calls[0]))
     # the same with the fused epilogue's up and gate biases
-    bu = torch.from_numpy(synthetic.activations_f32(3_000_510, 1, 14336)[0]).to(device)
-    bg = torch.from_numpy(synthetic.activations_f32(3_000_511, 1, 14336)[0]).to(device)
-    us = chain_time([lambda g=g, u=u: q.mul_mat_vec_fused(q.Q4_K, u, 14336, 4096, xq=xq, W_gate=g, bias=bu,
-                                                          gate_bias=bg, out=yv(1, 14336), stream=stream)
-                     for g, u in pairs])
-    out["q4_K gate+up 2x14336x4096 swiglu + up/gate biases"] = {
-        "us_per_call": round(us, 3), "weight_gbs": round(2 * ws[0].numel() / us / 1e3, 1)}
-    # MoE: 8 experts of 14336x4096, 4 tokens, top-2 drawn without replacement
-    E = torch.stack(ws).view(8, -1)
+    bu = torch.from_numpy(synthetic.activations_f32(3_000_510, 1, M)[0]).to(device)
+    bg = torch.from_numpy(synthetic.activations_f32(3_000_511, 1, M)[0]).to(device)
+    calls = [lambda g=g, u=u: q.mul_mat_vec_fused(q.Q4_K, u, M, K, xq=xq, W_gate=g, bias=bu, gate_bias=bg,
+                                                  out=yv(1, M), stream=stream) for g, u in pairs]
+    record("q4_K gate+up 2x14336x4096 +biases", chain_time(calls), 2 * wb, len(pairs))
+    del ws
+    torch.cuda.empty_cache()
+    # MoE: 8 experts of 14336x4096, 4 tokens, top-2 drawn without replacement;
+    # the chain rotates among distinct expert sets
     ids = synthetic.moe_ids(3_000_600, 4, 2, 8)
     n_touched = len(set(ids.reshape(-1).tolist()))
     idd = torch.from_numpy(ids).to(device)
-    xq4 = xq_of(4096, 4, 3_000_700)
-    ym = torch.empty((4, 2, 14336), dtype=torch.float32, device=device)
-    us = chain_time([lambda: q.mul_mat_vec_id(q.Q4_K, E, 8, 14336, 4096, xq4, idd, out=ym, stream=stream)] * 4)
-    out["q4_K moe 8x14336x4096 4 tokens top-2"] = {
-        "us_per_call": round(us, 3), "experts_touched": n_touched,
-        "weight_gbs": round(n_touched * ws[0].numel() / us / 1e3, 1),
-        "note": "the same call repeated; the touched experts (%d x 33 MB) exceed L2" % n_touched}
+    xq4 = xq_of(K, 4, 3_000_700)
+    ym = torch.empty((4, 2, M), dtype=torch.float32, device=device)
+    ysh = torch.empty((4, M), dtype=torch.float32, device=device)
+    n_sets = max(2, copies_for(torch, device, n_touched * wb, floor=2))
+    sets = [torch.stack(weights(q.Q4_K, M, K, 8, 3_001_000 + 10 * i)).view(8, -1) for i in range(n_sets)]
+    calls = [lambda E=E: q.mul_mat_vec_id(q.Q4_K, E, 8, M, K, xq4, idd, out=ym, stream=stream) for E in sets]
+    record("q4_K moe 8x14336x4096 4tok top-2", chain_time(calls), n_touched * wb, n_sets, cold_time(calls[0]),
+           experts_touched=n_touched)
     # the same routing plus a shared expert (every token), one launch
-    w_sh = weights(q.Q4_K, 14336, 4096, 1, 3_000_800)[0]
-    ysh = torch.empty((4, 14336), dtype=torch.float32, device=device)
-    us = chain_time([lambda: q.mul_mat_vec_id_fused(q.Q4_K, E, 8, 14336, 4096, idd, xq=xq4, W_shared=w_sh, out=ym,
-                                                    out_shared=ysh, stream=stream)] * 4)
-    out["q4_K moe 8x14336x4096 4 tokens top-2 + shared expert 14336x4096"] = {
-        "us_per_call": round(us, 3), "experts_touched": n_touched + 1,
-        "weight_gbs": round((n_touched + 1) * ws[0].numel() / us / 1e3, 1)}
+    shared = [weights(q.Q4_K, M, K, 1, 3_002_000 + i)[0] for i in range(n_sets)]
+    calls = [lambda E=E, S=S: q.mul_mat_vec_id_fused(q.Q4_K, E, 8, M, K, idd, xq=xq4, W_shared=S, out=ym,
+                                                     out_shared=ysh, stream=stream) for E, S in zip(sets, shared)]
+    record("q4_K moe +shared expert", chain_time(calls), (n_touched + 1) * wb, n_sets,
+           experts_touched=n_touched + 1)
     # the gated form: experts' gate matrices beside the up ones, the shared expert gated too
-    Eg = torch.stack(weights(q.Q4_K, 14336, 4096, 8, 3_000_900)).view(8, -1)
-    w_shg = weights(q.Q4_K, 14336, 4096, 1, 3_000_950)[0]
-    us = chain_time([lambda: q.mul_mat_vec_id_fused(q.Q4_K, E, 8, 14336, 4096, idd, xq=xq4, W_gate=Eg,
-                                                    W_shared=w_sh, W_shared_gate=w_shg, out=ym, out_shared=ysh,
-                                                    stream=stream)] * 4)
-    out["q4_K moe gate/up 8x2x14336x4096 4 tokens top-2 + shared gate/up expert"] = {
-        "us_per_call": round(us, 3), "experts_touched": n_touched + 1,
-        "weight_gbs": round(2 * (n_touched + 1) * ws[0].numel() / us / 1e3, 1)}
-    del ws, E, w_sh, Eg, w_shg
+    gsets = [torch.stack(weights(q.Q4_K, M, K, 8, 3_003_000 + 10 * i)).view(8, -1) for i in range(n_sets)]
+    gshared = [weights(q.Q4_K, M, K, 1, 3_004_000 + i)[0] for i in range(n_sets)]
+    calls = [lambda E=E, G=G, S=S, SG=SG: q.mul_mat_vec_id_fused(q.Q4_K, E, 8, M, K, idd, xq=xq4, W_gate=G,
+                                                                 W_shared=S, W_shared_gate=SG, out=ym, out_shared=ysh,
+                                                                 stream=stream)
+             for E, G, S, SG in zip(sets, gsets, shared, gshared)]
+    record("q4_K moe gate/up +shared gate/up", chain_time(calls), 2 * (n_touched + 1) * wb, n_sets,
+           experts_touched=n_touched + 1)
+    del sets, shared, gsets, gshared, flush_buf
     torch.cuda.empty_cache()
-    return out
+    return summary, detail
 
 
 def run_gpu(args):
@@ -552,7 +632,10 @@ def run_gpu(args):
     # q8_1-input GEMV chains at the three Llama-7B shapes (the pages' per-call figure)
     xq4 = q.quantize_q8_1(xs[0][0], stream=stream)
     xq11 = q.quantize_q8_1(acts[0], stream=stream)
-    shape_w = {"4096x4096": [weights[l]["o"][0] for l in range(N_LAYERS)],
+    # 4096x4096: every o matrix and the q, k and v slices of every stacked qkv
+    # (128 distinct matrices, 1.2 GB); every chain reads far more than 3x L2
+    qkv_slices = [weights[l]["qkv"][0][i * D_MODEL:(i + 1) * D_MODEL] for l in range(N_LAYERS) for i in range(3)]
+    shape_w = {"4096x4096": [weights[l]["o"][0] for l in range(N_LAYERS)] + qkv_slices,
                "11008x4096": [w for l in range(N_LAYERS) for w in weights[l]["gate_up"]],
                "4096x11008": [weights[l]["down"][0] for l in range(N_LAYERS)]}
     y_shape = torch.empty((1, D_FF), dtype=torch.float32, device=device)
@@ -568,7 +651,8 @@ def run_gpu(args):
     # ---- timed region: the step ----------------------------------------------------
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk, torch.cuda.stream(stream):
+    clk = ClockSampler(local).__enter__()  # sampled until every GPU measurement below is done
+    with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             graph.replay()
         stream.synchronize()
@@ -622,7 +706,15 @@ def run_gpu(args):
     achieved = tot_bytes / tot_time / 1e3  # GB/s
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["csrc_sha"] == csrc_sha() else None
 
-    configs = measure_configs(q, torch, stream, device, reps) if not args.no_configs else None
+    summary = {f"step {k}": [v["us_per_call"], v["weight_gbs"], round(v["weight_gbs"] / peak, 4)]
+               for k, v in kinds.items()}
+    summary.update({f"q4_K {k}": [v["us_per_call"], v["weight_gbs"], round(v["weight_gbs"] / peak, 4)]
+                    for k, v in per_shape.items()})
+    detail = {"step_kernels": kinds, "per_shape": per_shape}
+    if not args.no_configs:
+        cs, cd = measure_configs(q, torch, stream, device, reps, peak)
+        summary.update(cs)
+        detail["configs"] = cd
 
     # ---- end to end: host buffers, copies inside the timed region ---------------------
     # Every step copies its inputs host->device and its outputs device->host.
@@ -682,12 +774,12 @@ def run_gpu(args):
         raise RuntimeError("device fault word set during the benchmark")
 
     ceilings = None if args.no_configs else measure_ceilings(q, torch, stream, device)
+    clk.__exit__()
     if rank != 0:
         return 0
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        gbs, cores, sample = oracle_rate(min_seconds=args.cpu_seconds)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = cpu_baselines(args.cpu_seconds)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -702,10 +794,9 @@ def run_gpu(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "gemv_tiles_kernel<Q4_K, ncols=1, fp32 input> (the step's 128 launches by kind)",
                      "peak_kind": f"{peak_kind} HBM copy bandwidth"},
-        "step_kernels": kinds,
-        "per_shape": per_shape,
-        "configs": configs,
         "hbm_frac_of_measured": round(value / peak, 4),
+        "summary": summary,
+        "summary_fields": ["us per call", "weight GB/s", f"fraction of the {peak_kind} {peak} GB/s"],
         "ceilings": ceilings,
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5),
@@ -716,6 +807,9 @@ def run_gpu(args):
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
+    # the per-launch details (decode variants, cold single calls, copies chained)
+    # on a line of their own ahead of the result line, which stays compact
+    print("detail: " + json.dumps(detail), flush=True)
     print(json.dumps(line), flush=True)
     return 0
 
