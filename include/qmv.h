@@ -290,16 +290,6 @@ qmv_status qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
  * every setting.  Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above. */
 qmv_status qmv_set_early_warps(int type, int early_warps);
 
-/* Tiles each decoding warp of the streaming GEMV of `type` asks L2 to fetch
- * from HBM before it waits for the previous kernel on the stream, beyond the
- * tiles it copies into shared memory then (0..16; 0 = none, the default).
- * The data goes to L2 only, so nothing returns to the SM ahead of the
- * activation loads that follow the wait, while HBM keeps streaming across the
- * kernel boundary; the warp's later copies of those tiles hit in L2.  For
- * sweeps; results are identical for every setting.  Returns QMV_ERR_TYPE /
- * QMV_ERR_SHAPE as above. */
-qmv_status qmv_set_l2_prefetch(int type, int tiles);
-
 /* Column count from which the plain GEMV of `type` (qmv_mul_mat_vec, its
  * fp32-input and fused forms) decodes with the tensor cores instead of the
  * per-column dp4a: 8-row tiles multiplied by all columns at once with
@@ -348,9 +338,9 @@ qmv_status qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int nc
 /* Environment override of the geometry knobs above, for tuning runs:
  * QMV_GEOM="type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K
  * and keys threads, slice_units, stages, ctas_per_sm, smem_share, cluster,
- * dec_warps, pre_tiles, early_warps, l2_tiles and mma_min_cols (the
- * arguments of qmv_set_tuning, qmv_set_stream_tuning, qmv_set_early_warps,
- * qmv_set_l2_prefetch and qmv_set_mma_min_cols, same ranges).  It is read
+ * dec_warps, pre_tiles, early_warps and mma_min_cols (the arguments of
+ * qmv_set_tuning, qmv_set_stream_tuning, qmv_set_early_warps and
+ * qmv_set_mma_min_cols, same ranges).  It is read
  * once, before the first GEMV-family call is planned, and applied through
  * those setters; later setter calls override it.  A malformed spec or an
  * out-of-range value makes every GEMV-family call return QMV_ERR_CONFIG

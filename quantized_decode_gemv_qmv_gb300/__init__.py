@@ -31,7 +31,7 @@ EXPORTS = (
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv", "qmv_read_bandwidth_probe",
-    "qmv_set_early_warps", "qmv_set_l2_prefetch", "qmv_debug_f32_withheld_share",
+    "qmv_set_early_warps", "qmv_debug_f32_withheld_share",
 )
 
 
@@ -95,7 +95,6 @@ def lib():
         L.qmv_set_checked.argtypes = [_int]
         L.qmv_set_mma_min_cols.argtypes = [_int, _int]
         L.qmv_set_early_warps.argtypes = [_int, _int]
-        L.qmv_set_l2_prefetch.argtypes = [_int, _int]
         L.qmv_read_bandwidth_probe.argtypes = [_vp, ctypes.c_size_t, _vp, _vp]
         L.qmv_describe_gemv.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.POINTER(LaunchInfo)]
         L.qmv_debug_f32_withheld_share.argtypes = [_int, _vp, _i64, _i64, _vp, _i64, _int, _vp, ctypes.c_uint64, _vp]
@@ -105,8 +104,7 @@ def lib():
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
                      "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
-                     "qmv_read_bandwidth_probe", "qmv_set_early_warps", "qmv_set_l2_prefetch",
-                     "qmv_debug_f32_withheld_share"):
+                     "qmv_read_bandwidth_probe", "qmv_set_early_warps", "qmv_debug_f32_withheld_share"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -499,11 +497,6 @@ def describe_gemv(qtype: int, M: int, K: int, ncols: int = 1, gate_up: bool = Fa
 def set_early_warps(qtype: int, early_warps: int = 0):
     """Decoding warps that request tiles before the dependency wait (0: all)."""
     _check("qmv_set_early_warps", lib().qmv_set_early_warps(qtype, early_warps))
-
-
-def set_l2_prefetch(qtype: int, tiles: int = 0):
-    """Tiles per decoding warp fetched into L2 only before the dependency wait (0: none)."""
-    _check("qmv_set_l2_prefetch", lib().qmv_set_l2_prefetch(qtype, tiles))
 
 
 def set_mma_min_cols(qtype: int, min_cols: int = 0):

@@ -63,7 +63,6 @@ constexpr int MAX_CLUSTER = 8;         // portable cluster size limit
 // MoE experts per call: the generic kernel gives every expert one grid row
 // plus one for the invalid ids, and gridDim.y is at most 65535
 constexpr int64_t MAX_EXPERTS = 65534;
-constexpr int MAX_L2_TILES = 16;  // qmv_set_l2_prefetch: at most this many tiles per warp
 
 std::atomic<int> g_pdl{1};
 
@@ -72,7 +71,6 @@ struct Tuning {
     std::atomic<int> dec_warps{0}, pre_tiles{0};
     std::atomic<int> mma_min_cols{0};  // 0: MMA_MIN_COLS; 9: never
     std::atomic<int> early_warps{0};   // 0: every decoding warp requests its early tiles
-    std::atomic<int> l2_tiles{0};      // tiles per warp fetched into L2 only before the dependency wait
 };
 Tuning g_tuning[3];
 
@@ -128,14 +126,14 @@ bool apply_geom_entry(const std::string &entry)
     const int type = tname == "q4_0" ? FMT_Q4_0 : tname == "q4_K" ? FMT_Q4_K : tname == "q6_K" ? FMT_Q6_K : -1;
     if (type < 0) return false;
     const Tuning &cur = g_tuning[tidx(type)];
-    constexpr int NK = 11;
+    constexpr int NK = 10;
     int v[NK] = {cur.threads.load(),     cur.slice_units.load(), cur.stages.load(),
                  cur.ctas_per_sm.load(), cur.smem_share.load(),  cur.cluster.load(),
                  cur.dec_warps.load(),   cur.pre_tiles.load(),   cur.mma_min_cols.load(),
-                 cur.early_warps.load(), cur.l2_tiles.load()};
+                 cur.early_warps.load()};
     static const char *const keys[NK] = {"threads",   "slice_units", "stages",       "ctas_per_sm", "smem_share",
                                          "cluster",   "dec_warps",   "pre_tiles",    "mma_min_cols",
-                                         "early_warps", "l2_tiles"};
+                                         "early_warps"};
     size_t pos = colon + 1;
     while (pos <= entry.size()) {
         size_t comma = entry.find(',', pos);
@@ -150,7 +148,7 @@ bool apply_geom_entry(const std::string &entry)
     }
     return qmv_set_tuning(type, v[0], v[1], v[2], v[3], v[4], v[5]) == QMV_OK &&
            qmv_set_stream_tuning(type, v[6], v[7]) == QMV_OK && qmv_set_mma_min_cols(type, v[8]) == QMV_OK &&
-           qmv_set_early_warps(type, v[9]) == QMV_OK && qmv_set_l2_prefetch(type, v[10]) == QMV_OK;
+           qmv_set_early_warps(type, v[9]) == QMV_OK;
 }
 
 qmv_status geom_env()
@@ -458,7 +456,6 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     p.pre_tiles = tu.pre_tiles.load() > 0 ? std::min(stages, tu.pre_tiles.load())
                                           : (tiles_per_warp <= stages ? stages : 1);
     p.early_warps = tu.early_warps.load() > 0 ? tu.early_warps.load() : wpc;
-    p.l2_tiles = tu.l2_tiles.load();
     p.act_bytes = static_cast<uint32_t>(act);
     p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
     L.fn = fn;
@@ -1107,14 +1104,6 @@ qmv_status qmv_set_early_warps(int type, int early_warps)
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (early_warps < 0 || early_warps > TILE_MAX_THREADS / 32) return QMV_ERR_SHAPE;
     g_tuning[tidx(type)].early_warps = early_warps;
-    return QMV_OK;
-}
-
-qmv_status qmv_set_l2_prefetch(int type, int tiles)
-{
-    if (!weight_type(type)) return QMV_ERR_TYPE;
-    if (tiles < 0 || tiles > MAX_L2_TILES) return QMV_ERR_SHAPE;
-    g_tuning[tidx(type)].l2_tiles = tiles;
     return QMV_OK;
 }
 

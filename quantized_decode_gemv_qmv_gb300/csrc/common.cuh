@@ -202,13 +202,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
-// Asks L2 to fetch [src, src + bytes) from HBM without copying it anywhere
-// (16-byte aligned address, size a multiple of 16).
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;

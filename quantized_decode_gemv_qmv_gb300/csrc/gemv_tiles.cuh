@@ -469,24 +469,6 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 
     if (warp < p.early_warps)
         while (issued < total && issued < p.pre_tiles) issue_tile();  // weights first
-    if constexpr (!IS_MOE) {
-        // the warp's next tiles into L2 only: HBM keeps streaming across the
-        // boundary without copies that return to this SM ahead of the
-        // activation loads (RW lanes per tile, one row segment each)
-        if (p.l2_tiles > 0 && warp < nwarps) {
-            const int64_t per_g = static_cast<int64_t>(n_kt) * NM;
-            const int64_t t_end = min64(total, issued + p.l2_tiles);
-            for (int64_t j = issued + lane / RW; j < t_end; j += 32 / RW) {
-                const int64_t grp = g_begin + j / per_g;
-                const int rem = static_cast<int>(j - (j / per_g) * per_g);
-                const int kt = rem / NM;
-                const int64_t row = grp * RW + lane % RW;
-                if (row < p.M)
-                    prefetch_l2(((NM == 2 && rem % NM) ? W1 : W0) + row * rb + static_cast<int64_t>(kt) * (UW * UNIT),
-                                static_cast<uint32_t>(min(UW, U - kt * UW) * UNIT));
-            }
-        }
-    }
     if constexpr (!IS_MOE) pdl_wait();
     if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
     if (!MMA && ncta > 1 && threadIdx.x == 0)

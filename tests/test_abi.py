@@ -151,8 +151,6 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_set_mma_min_cols(12, 0) == 0
     assert L.qmv_set_early_warps(12, 13) == 3 and L.qmv_set_early_warps(12, -1) == 3
     assert L.qmv_set_early_warps(2, 0) == 0 and L.qmv_set_early_warps(9, 0) == 2
-    assert L.qmv_set_l2_prefetch(12, 17) == 3 and L.qmv_set_l2_prefetch(12, -1) == 3
-    assert L.qmv_set_l2_prefetch(9, 0) == 2 and L.qmv_set_l2_prefetch(14, 0) == 0
     rp = L.qmv_read_bandwidth_probe
     assert rp(nul, 16, p, nul) == 1 and rp(p, 16, nul, nul) == 1
     assert rp(p, 0, p, nul) == 3 and rp(p, 17, p, nul) == 3
@@ -194,7 +192,6 @@ print('rc', L.qmv_mul_mat_vec(12, p, 16, 256, p, 1, p, ctypes.c_void_p(0)))
     ("q4_K:stages=x", 10),                                # not a number
     ("q5_K:stages=2", 10),                                # unknown type
     ("q4_K:warps=4", 10),                                 # unknown key
-    ("q4_K:l2_tiles=17", 10),                             # out of range (at most 16)
     ("q4_K", 10),                                         # no key list
 ])
 def test_geometry_environment_override(qlib, spec, want):
