@@ -22,7 +22,8 @@ with both decodes, the fused gate/up, the MoE variants); and bandwidth
 ceilings (device copy, torch reduction, the library's read probe).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-  python bench.py --kernel-only SHAPE|KIND|moe [--ncols N] [--mma-min-cols N]   (profiler captures)
+  python bench.py --kernel-only SHAPE|KIND|moe|q6_K:MxK|q4_0:MxK [--ncols N] [--mma-min-cols N]   (profiler captures)
+  python bench.py --trace all|NAME   (per-CTA timeline of chained launches: release, staging, tail)
 """
 from __future__ import annotations
 
@@ -832,6 +833,21 @@ def run_kernel_only(args):
     kinds = {name: (M, K, nmat) for name, M, K, nmat in STEP}
     shapes = dict(SHAPES, **{"14336x4096": (14336, 4096)})
     nc = args.ncols
+    qt = Q4_K
+    if args.kernel_only.startswith("q6_K:") or args.kernel_only.startswith("q4_0:"):
+        # another format at a config shape, q8_1 input (e.g. q6_K:4096x14336)
+        fmt, shape = args.kernel_only.split(":", 1)
+        qt = q.Q6_K if fmt == "q6_K" else q.Q4_0
+        M, K = (int(v) for v in shape.split("x"))
+        Ws = [q.quantize_weights(qt, synthetic.device_normal_f32(7 + 2 * i, (M, K), 0.02, "cuda")) for i in range(4)]
+        xq = q.quantize_q8_1(torch.from_numpy(synthetic.activations_f32(9, nc, K)).cuda())
+        y = torch.empty((nc, M), dtype=torch.float32, device="cuda")
+        for i in range(args.launches):
+            q.mul_mat_vec(qt, Ws[i % len(Ws)], M, K, xq, nc, out=y)
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel_only": args.kernel_only, "launches": args.launches,
+                          "weight_bytes_per_launch": int(Ws[0].numel())}))
+        return 0
     if args.kernel_only == "moe":
         # the configs' MoE call: 8 experts of 14336x4096, 4 tokens top-2 (the same seeded routing)
         M, K = 14336, 4096
@@ -872,6 +888,99 @@ def run_kernel_only(args):
     return 0
 
 
+def run_trace(args):
+    """Timeline of chained GEMV launches (per-CTA timestamps, qmv_debug_trace):
+    for each workload, a CUDA graph of N launches over distinct weight copies
+    (the benchmark's chained per-call setting) is replayed with the timeline on,
+    and every launch k >= 1 is measured against the one before it: the PDL
+    release (previous launch's last CTA done -> first wait return), the
+    activation staging (wait return -> staged, median over CTAs), the decode
+    tail (median staged -> last CTA done), the spread of CTA finish times and
+    the launch period (last CTA done to last CTA done)."""
+    import numpy as np
+    import torch
+
+    import synthetic
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import quantized_decode_gemv_qmv_gb300 as q
+
+    torch.cuda.set_device(0)
+    q.set_pdl(True)
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream()
+    work = {  # name: (type, M, K, matrices, fp32 input)
+        "q4_K 4096x4096 q8_1": (q.Q4_K, 4096, 4096, 1, False),
+        "q4_K 14336x4096 q8_1": (q.Q4_K, 14336, 4096, 1, False),
+        "q6_K 4096x14336 q8_1": (q.Q6_K, 4096, 14336, 1, False),
+        "step qkv 12288x4096 fp32": (q.Q4_K, 12288, 4096, 1, True),
+        "step o 4096x4096 fp32": (q.Q4_K, 4096, 4096, 1, True),
+        "step gate+up 2x11008x4096 fp32": (q.Q4_K, 11008, 4096, 2, True),
+        "step down 4096x11008 fp32": (q.Q4_K, 4096, 11008, 1, True),
+    }
+    if args.trace != "all":
+        work = {k: v for k, v in work.items() if args.trace in k}
+    out = {}
+    for name, (t, M, K, nmat, f32) in work.items():
+        wb = nmat * M * q.row_bytes(t, K)
+        n = max(16, -(-3 * (126 << 20) // wb))
+        with torch.cuda.stream(s):
+            Ws = [[q.quantize_weights(t, synthetic.device_normal_f32(500 + 10 * i + m, (M, K), 0.02, dev), stream=s)
+                   for m in range(nmat)] for i in range(n)]
+        s.synchronize()
+        x = torch.from_numpy(synthetic.activations_f32(77, 1, K, outlier_frac=0.01)).to(dev)
+        xq = q.quantize_q8_1(x, stream=s)
+        y = torch.empty((1, M), dtype=torch.float32, device=dev)
+        buf = torch.zeros(n * q.TRACE_MAX_CTAS * 4, dtype=torch.int64, device=dev)
+
+        def chain():
+            for W in Ws:
+                if nmat == 2:
+                    q.mul_mat_vec_gate_up_swiglu_f32(t, W[1], W[0], M, K, x, out=y, stream=s)
+                elif f32:
+                    q.mul_mat_vec_f32(t, W[0], M, K, x, out=y, stream=s)
+                else:
+                    q.mul_mat_vec(t, W[0], M, K, xq, 1, out=y, stream=s)
+
+        with torch.cuda.stream(s):
+            chain()  # eager warm-up
+        s.synchronize()
+        q.debug_trace(buf, n)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            chain()
+        q.debug_trace(None)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                g.replay()
+            s.synchronize()
+            buf.zero_()
+            g.replay()
+        s.synchronize()
+        T = buf.view(n, q.TRACE_MAX_CTAS, 4).cpu().numpy().astype(np.float64)
+        rows = []
+        for k in range(1, n):
+            cur = T[k][T[k][:, 0] > 0]
+            prev = T[k - 1][T[k - 1][:, 0] > 0]
+            prev_done = prev[:, 3].max()
+            rows.append([cur[:, 1].min() - prev_done,                # release
+                         np.median(cur[:, 2] - cur[:, 1]),            # staging
+                         cur[:, 3].max() - np.median(cur[:, 2]),      # decode tail
+                         cur[:, 3].max() - np.median(cur[:, 3]),      # last CTA behind the median one
+                         cur[:, 0].min() - prev_done,                 # first CTA entry (negative: early)
+                         cur[:, 3].max() - prev_done])                # period
+        r = np.median(np.asarray(rows), axis=0) / 1e3
+        out[name] = {"release_us": round(r[0], 3), "staging_us": round(r[1], 3), "tail_us": round(r[2], 3),
+                     "last_cta_behind_median_us": round(r[3], 3), "first_entry_us": round(r[4], 3),
+                     "period_us": round(r[5], 3), "ideal_us": round(wb / 6668.5e3, 3), "launches": n - 1,
+                     "ctas": int((T[1][:, 0] > 0).sum())}
+        print(json.dumps({name: out[name]}), flush=True)
+        del Ws, buf
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -885,6 +994,8 @@ def main():
                     help="profiling aid: only GEMV launches of one shape, step kind, or the MoE call (moe)")
     ap.add_argument("--launches", type=int, default=8)
     ap.add_argument("--ncols", type=int, default=1, help="profiling aid: activation columns of a --kernel-only shape")
+    ap.add_argument("--trace", default=None,
+                    help="timeline of chained launches (per-CTA timestamps): 'all' or a substring of a workload name")
     ap.add_argument("--mma-min-cols", type=int, default=0,
                     help="profiling aid: columns from which --kernel-only uses the tensor-core decode (0: default)")
     args = ap.parse_args()
@@ -893,6 +1004,8 @@ def main():
         return run_reference(args)
     if args.kernel_only:
         return run_kernel_only(args)
+    if args.trace:
+        return run_trace(args)
     return run_gpu(args)
 
 

@@ -44,6 +44,24 @@ qmv_status qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K
 qmv_status qmv_debug_f32_withheld_share(int type, const void *W, int64_t M, int64_t K, const float *x,
                                         int64_t ldx, int ncols, float *y, uint64_t wait_ns, void *stream);
 
+/* Timeline of the streaming GEMV launches, for measuring where a launch's
+ * time goes.  While enabled, each of the next `slots` GEMV launches of the
+ * streaming tile kernel (any call of qmv.h that takes that kernel; the
+ * generic kernel and the quantizers are not traced) writes, per CTA b, four
+ * globaltimer readings (ns) into buf + (k*1024 + b)*4, k = the launch's index
+ * since this call: [0] the CTA's first instruction, [1] the return of the
+ * wait for the previous kernel on the stream (programmatic dependent launch),
+ * [2] its activations staged in shared memory, [3] the last of its warps done
+ * (an atomic max, so [3] must be zero beforehand).  buf: device memory of
+ * slots * 1024 * 4 * 8 bytes, 8-byte aligned; launches of more than 1024 CTAs
+ * and launches past the slots are not recorded.  Under CUDA graph capture the
+ * slot is fixed when the call is captured.  buf NULL or slots 0 disables it.
+ * Costs a few instructions per CTA when disabled.  Not thread-safe with
+ * concurrent launches from other host threads (the slot counter is shared).
+ * The pages have no counterpart: a measurement aid of this library.
+ * Returns QMV_ERR_SHAPE for slots < 0, QMV_ERR_ALIGN for a misaligned buf. */
+qmv_status qmv_debug_trace(unsigned long long *buf, int64_t slots);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ EXPORTS = (
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv", "qmv_read_bandwidth_probe",
-    "qmv_set_early_warps", "qmv_debug_f32_withheld_share",
+    "qmv_set_early_warps", "qmv_debug_f32_withheld_share", "qmv_debug_trace",
 )
 
 
@@ -98,13 +98,15 @@ def lib():
         L.qmv_read_bandwidth_probe.argtypes = [_vp, ctypes.c_size_t, _vp, _vp]
         L.qmv_describe_gemv.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.POINTER(LaunchInfo)]
         L.qmv_debug_f32_withheld_share.argtypes = [_int, _vp, _i64, _i64, _vp, _i64, _int, _vp, ctypes.c_uint64, _vp]
+        L.qmv_debug_trace.argtypes = [_vp, _i64]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
                      "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_mul_mat_vec_fused",
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
                      "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
-                     "qmv_read_bandwidth_probe", "qmv_set_early_warps", "qmv_debug_f32_withheld_share"):
+                     "qmv_read_bandwidth_probe", "qmv_set_early_warps", "qmv_debug_f32_withheld_share",
+                     "qmv_debug_trace"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -456,6 +458,23 @@ def debug_f32_withheld_share(qtype: int, W, M: int, K: int, x, wait_ns: int, out
     _call("qmv_debug_f32_withheld_share", dev, stream, qtype, _ptr(W), M, K, _ptr(x2), ldx, ncols, _ptr(out),
           ctypes.c_uint64(wait_ns))
     return out
+
+
+TRACE_MAX_CTAS = 1024
+
+
+def debug_trace(buf=None, slots: int = 0):
+    """Diagnostics: per-CTA timestamps of the next `slots` streaming GEMV
+    launches into buf (int64 CUDA tensor of slots*1024*4, zeroed); None stops
+    (see include/qmv_debug.h, qmv_debug_trace)."""
+    import torch
+
+    if buf is None:
+        _check("qmv_debug_trace", lib().qmv_debug_trace(None, 0))
+        return
+    _tensor(buf, "buf", torch.int64, slots * TRACE_MAX_CTAS * 4 * 8)
+    _device_of((("buf", buf),))
+    _check("qmv_debug_trace", lib().qmv_debug_trace(_ptr(buf), slots))
 
 
 def device_fault() -> int:

@@ -66,6 +66,12 @@ constexpr int64_t MAX_EXPERTS = 65534;
 
 std::atomic<int> g_pdl{1};
 
+// Diagnostic timeline (qmv_debug_trace): the next g_trace_slots tile-kernel
+// launches each get a slot of TRACE_MAX_CTAS x 4 timestamps.
+constexpr int TRACE_MAX_CTAS = 1024;
+std::atomic<unsigned long long *> g_trace_buf{nullptr};
+std::atomic<int64_t> g_trace_slots{0}, g_trace_next{0};
+
 struct Tuning {
     std::atomic<int> threads{0}, slice_units{0}, stages{0}, ctas_per_sm{0}, smem_share{0}, cluster{0};
     std::atomic<int> dec_warps{0}, pre_tiles{0};
@@ -544,6 +550,11 @@ qmv_status launch(const Launch &L, cudaStream_t st)
     cfg.attrs = attr;
     cfg.numAttrs = n_attr;
     GemvParams p = L.p;
+    unsigned long long *tb = g_trace_buf.load();
+    if (tb && L.stream && L.grid.x <= static_cast<unsigned>(TRACE_MAX_CTAS)) {
+        const int64_t k = g_trace_next.fetch_add(1);
+        if (k < g_trace_slots.load()) p.trace = tb + k * TRACE_MAX_CTAS * 4;
+    }
     void *args[1] = {&p};
     cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, args);
     return cuda_status(e);
@@ -1112,6 +1123,17 @@ qmv_status qmv_set_mma_min_cols(int type, int min_cols)
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (min_cols < 0 || min_cols > 9) return QMV_ERR_SHAPE;
     g_tuning[tidx(type)].mma_min_cols = min_cols;
+    return QMV_OK;
+}
+
+qmv_status qmv_debug_trace(unsigned long long *buf, int64_t slots)
+{
+    if (slots < 0) return QMV_ERR_SHAPE;
+    if (buf && reinterpret_cast<uintptr_t>(buf) % 8) return QMV_ERR_ALIGN;
+    g_trace_buf = nullptr;
+    g_trace_slots = buf ? slots : 0;
+    g_trace_next = 0;
+    g_trace_buf = slots ? buf : nullptr;
     return QMV_OK;
 }
 

@@ -39,6 +39,7 @@ struct GemvParams {
     int early_warps;     // tile kernel: warps that make those early requests (the first ones; >= dec_warps: all)
     uint32_t act_bytes;  // tile kernel: shared bytes of the activation area
     uint32_t raw_off;    // tile kernel: offset of the raw q8_1 copy inside the activation area (0: none)
+    unsigned long long *trace;  // diagnostics: per-CTA timestamps [entry, waited, staged, done] (nullable)
     int withhold;        // test only: the rank-1 CTA of each fp32-staging cluster keeps its share to itself
     unsigned long long withhold_wait_ns;  // test only: how long the rank-0 CTA then waits for that share
 };

@@ -282,6 +282,10 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     const int stages = p.stages;
 
     pdl_launch_dependents();
+    // optional timeline (qmv_debug_trace): entry, after the dependency wait,
+    // activations staged, last warp done
+    unsigned long long *const trace = p.trace ? p.trace + 4 * blockIdx.x : nullptr;
+    if (trace && threadIdx.x == 0) trace[0] = global_timer_ns();
     // fp32 input in a cluster: the CTAs share the quantization (see
     // stage_tile_activations); this arrive lets the others know this CTA runs
     uint32_t crank = 0, ncta = 1;
@@ -470,6 +474,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     if (warp < p.early_warps)
         while (issued < total && issued < p.pre_tiles) issue_tile();  // weights first
     if constexpr (!IS_MOE) pdl_wait();
+    if (trace && threadIdx.x == 0) trace[1] = global_timer_ns();
     if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
     if (!MMA && ncta > 1 && threadIdx.x == 0)
         mbar_arrive_expect_tx(xbar, cluster_share_bytes<F>(p.ncols * p.units_per_row * 8, crank, ncta));
@@ -504,6 +509,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         __syncthreads();
     }
 
+    if (trace && threadIdx.x == 0) trace[2] = global_timer_ns();
     while (issued < total && issued < stages) issue_tile();  // the rest of the ring
 
     const uint32_t act_qs = smem_u32(smem);
@@ -646,6 +652,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         }
         if (++cbuf == stages) cbuf = 0;
     }
+    if (trace && lane == 0) atomicMax(trace + 3, global_timer_ns());
 }
 
 // Kernel table of the tile path for one format (instantiated only in that
