@@ -38,9 +38,9 @@
  *     wait on the previous grid.  The one spin-wait is bounded: the fp32-input
  *     plain and gate/up calls, whose clusters of CTAs share the quantization
  *     of the activations, wait on an mbarrier for the partners' shares for at
- *     most one second; past that the kernel records code 2 in the sticky
- *     device fault word (qmv_device_fault), writes NaN to the outputs of that
- *     CTA's rows and returns instead of hanging.
+ *     most one second; past that each warp that gave up records code 2 in
+ *     the sticky device fault word (qmv_device_fault), writes NaN to the
+ *     outputs of its rows and returns instead of hanging.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -74,7 +74,8 @@ typedef enum {
     QMV_ERR_DEVICE_FAULT = 8, /* a kernel's bounded wait ran out (see qmv_device_fault) */
     QMV_ERR_RANGE = 9,        /* checked mode: an argument's byte range is not inside one device
                                  allocation (see qmv_set_checked) */
-    QMV_ERR_CONFIG = 10       /* the QMV_GEOM environment override is malformed or out of range */
+    QMV_ERR_CONFIG = 10       /* the QMV_GEOM environment override is malformed or out of range;
+                                 or a test entry of qmv_debug.h has no launch of the form it needs */
 } qmv_status;
 
 /* Human-readable name of a status code (static storage). */
@@ -242,7 +243,7 @@ qmv_status qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_ga
 /* Reads and clears the sticky device fault word of the current device: 0 if
  * no kernel's bounded wait has run out since the last call, else the OR of
  * nonzero codes (2: a cluster partner's share of the staged fp32 activations
- * did not arrive within the wait limit).  A CTA whose wait ran out computes
+ * did not arrive within the wait limit).  A warp whose wait ran out computes
  * nothing: it writes NaN to every output of its rows and returns, so a bad
  * result cannot pass for a good one.  Callers of the fp32-input plain and
  * gate/up calls (and of qmv_mul_mat_vec_fused with fp32 x) should read this

@@ -1,10 +1,16 @@
 /*
- * libqmv test-only entry points: exact integer intermediates of the GEMV and a
- * way to make the library's one bounded wait run out on purpose.  Not part of
- * the compute API; they exist so that tests can check the kernels bit for bit
- * and exercise the fault path.  Conventions (ownership, asynchronous
+ * libqmv test-only entry points: exact integer intermediates of the GEMV, a
+ * way to make the library's one bounded wait run out on purpose, and a
+ * per-CTA timeline of launches.  Not part of the compute API; they exist so
+ * that tests can check the kernels bit for bit, exercise the fault path and
+ * measure where a launch's time goes.  Conventions (ownership, asynchronous
  * execution on `stream`, host validation before any launch, status codes)
  * are those of qmv.h.
+ *
+ * The last two run instrumented twins of the streaming tile kernel: the same
+ * code plus the timeline stores and the withheld share, which the ordinary
+ * kernels do not carry.  Twins exist for the plain GEMV of one or two columns
+ * and the fused gate/up GEMV of one column (4-row tiles, dp4a decode).
  */
 #ifndef QMV_DEBUG_H
 #define QMV_DEBUG_H
@@ -32,31 +38,32 @@ qmv_status qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K
  * the bounded wait of its activation exchange runs out: in every cluster of
  * CTAs that share the quantization of x, the CTA of rank 1 withholds its
  * share from the others, and the CTA of rank 0 waits at most wait_ns
- * nanoseconds for it (1 ns .. 1 s) before it gives up.  The CTAs that gave up
- * record code 2 in the device fault word (qmv_device_fault) and write NaN to
- * the outputs of their rows; every other output is the value
+ * nanoseconds for it (1 ns .. 1 s) before its warps give up.  Warps that gave
+ * up record code 2 in the device fault word (qmv_device_fault) and write NaN
+ * to the outputs of their rows; every other output is the value
  * qmv_mul_mat_vec_f32 computes.  The CTAs of rank 1 still receive rank 0's
  * share and finish normally, so nothing waits without a bound and no store
  * into a CTA arrives after it has exited.  Returns QMV_ERR_CONFIG, before
  * launching, if the launch would not use clusters of CTAs (the exchange then
- * does not exist); the argument errors of qmv_mul_mat_vec_f32 otherwise.  The
+ * does not exist) or without an instrumented twin (ncols > 2); the argument
+ * errors of qmv_mul_mat_vec_f32 otherwise.  The
  * pages have no counterpart: it tests the library's own fault reporting. */
 qmv_status qmv_debug_f32_withheld_share(int type, const void *W, int64_t M, int64_t K, const float *x,
                                         int64_t ldx, int ncols, float *y, uint64_t wait_ns, void *stream);
 
 /* Timeline of the streaming GEMV launches, for measuring where a launch's
- * time goes.  While enabled, each of the next `slots` GEMV launches of the
- * streaming tile kernel (any call of qmv.h that takes that kernel; the
- * generic kernel and the quantizers are not traced) writes, per CTA b, four
- * globaltimer readings (ns) into buf + (k*1024 + b)*4, k = the launch's index
- * since this call: [0] the CTA's first instruction, [1] the return of the
+ * time goes.  While enabled, each of the next `slots` launches that have an
+ * instrumented twin (any call of qmv.h whose launch takes one; other launches
+ * are not recorded and take no slot) runs the twin, which writes, per CTA b,
+ * four globaltimer readings (ns) into buf + (k*1024 + b)*4, k = the launch's
+ * index since this call: [0] the CTA's first instruction, [1] the return of the
  * wait for the previous kernel on the stream (programmatic dependent launch),
  * [2] its activations staged in shared memory, [3] the last of its warps done
  * (an atomic max, so [3] must be zero beforehand).  buf: device memory of
  * slots * 1024 * 4 * 8 bytes, 8-byte aligned; launches of more than 1024 CTAs
  * and launches past the slots are not recorded.  Under CUDA graph capture the
  * slot is fixed when the call is captured.  buf NULL or slots 0 disables it.
- * Costs a few instructions per CTA when disabled.  Not thread-safe with
+ * Costs nothing when disabled.  Not thread-safe with
  * concurrent launches from other host threads (the slot counter is shared).
  * The pages have no counterpart: a measurement aid of this library.
  * Returns QMV_ERR_SHAPE for slots < 0, QMV_ERR_ALIGN for a misaligned buf. */

@@ -449,7 +449,7 @@ def debug_f32_withheld_share(qtype: int, W, M: int, K: int, x, wait_ns: int, out
     """Test only: mul_mat_vec_f32 with one CTA of every cluster withholding its
     share of the quantized activations, so that its partner's bounded wait
     (wait_ns) runs out; that partner's rows come back NaN and the device fault
-    word gets code 2 (see include/qmv_debug.h)."""
+    word gets code 2 (see include/qmv_debug.h).  One or two columns."""
     x2, ldx = _x2d(x, K)
     ncols = x2.shape[0]
     _weights(W, "W", qtype, M, K)
@@ -464,9 +464,10 @@ TRACE_MAX_CTAS = 1024
 
 
 def debug_trace(buf=None, slots: int = 0):
-    """Diagnostics: per-CTA timestamps of the next `slots` streaming GEMV
-    launches into buf (int64 CUDA tensor of slots*1024*4, zeroed); None stops
-    (see include/qmv_debug.h, qmv_debug_trace)."""
+    """Diagnostics: per-CTA timestamps of the next `slots` GEMV launches that
+    have an instrumented twin (plain, 1-2 columns; gate/up, 1 column) into buf
+    (int64 CUDA tensor of slots*1024*4, zeroed); None stops (see
+    include/qmv_debug.h, qmv_debug_trace)."""
     import torch
 
     if buf is None:

@@ -19,6 +19,9 @@ const void *gemv_tiles_fn_q4_0(int mode, int nc, int rw);
 const void *gemv_tiles_fn_q4_K(int mode, int nc, int rw);
 const void *gemv_tiles_mma_fn_q4_K(int mode);
 const void *gemv_tiles_fn_q6_K(int mode, int nc, int rw);
+const void *gemv_tiles_probe_fn_q4_0(int mode, int nc);
+const void *gemv_tiles_probe_fn_q4_K(int mode, int nc);
+const void *gemv_tiles_probe_fn_q6_K(int mode, int nc);
 const void *gemv_generic_fn_q4_0(int mode);
 const void *gemv_generic_fn_q4_K(int mode);
 const void *gemv_generic_fn_q6_K(int mode);
@@ -29,6 +32,18 @@ const void *gemv_tiles_fn(int type, int mode, int nc, int rw)
     case FMT_Q4_0: return gemv_tiles_fn_q4_0(mode, nc, rw);
     case FMT_Q4_K: return gemv_tiles_fn_q4_K(mode, nc, rw);
     case FMT_Q6_K: return gemv_tiles_fn_q6_K(mode, nc, rw);
+    default: return nullptr;
+    }
+}
+
+// The instrumented twin of the tile kernel gemv_tiles_fn(type, mode, nc, 4)
+// (timeline and withheld share of qmv_debug.h); nullptr where none exists.
+const void *gemv_tiles_probe_fn(int type, int mode, int nc)
+{
+    switch (type) {
+    case FMT_Q4_0: return gemv_tiles_probe_fn_q4_0(mode, nc);
+    case FMT_Q4_K: return gemv_tiles_probe_fn_q4_K(mode, nc);
+    case FMT_Q6_K: return gemv_tiles_probe_fn_q6_K(mode, nc);
     default: return nullptr;
     }
 }
@@ -66,8 +81,9 @@ constexpr int64_t MAX_EXPERTS = 65534;
 
 std::atomic<int> g_pdl{1};
 
-// Diagnostic timeline (qmv_debug_trace): the next g_trace_slots tile-kernel
-// launches each get a slot of TRACE_MAX_CTAS x 4 timestamps.
+// Diagnostic timeline (qmv_debug_trace): the next g_trace_slots launches that
+// have an instrumented twin run it, each with a slot of TRACE_MAX_CTAS x 4
+// timestamps.
 constexpr int TRACE_MAX_CTAS = 1024;
 std::atomic<unsigned long long *> g_trace_buf{nullptr};
 std::atomic<int64_t> g_trace_slots{0}, g_trace_next{0};
@@ -284,6 +300,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Launch {
     const void *fn = nullptr;
+    const void *probe = nullptr;  // fn's instrumented twin (qmv_debug.h), if it has one
     bool stream = false;
     int rw = 0;       // tile kernel: weight rows per warp tile
     int cluster = 1;  // CTAs per cluster (1: no cluster dimension)
@@ -465,6 +482,7 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     p.act_bytes = static_cast<uint32_t>(act);
     p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
     L.fn = fn;
+    L.probe = (!mma && rw == 4) ? gemv_tiles_probe_fn(type, mode, nc_t) : nullptr;
     L.stream = true;
     L.rw = rw;
     L.cluster = cl;
@@ -550,13 +568,21 @@ qmv_status launch(const Launch &L, cudaStream_t st)
     cfg.attrs = attr;
     cfg.numAttrs = n_attr;
     GemvParams p = L.p;
+    const void *fn = L.fn;
     unsigned long long *tb = g_trace_buf.load();
-    if (tb && L.stream && L.grid.x <= static_cast<unsigned>(TRACE_MAX_CTAS)) {
+    if (tb && L.probe && L.grid.x <= static_cast<unsigned>(TRACE_MAX_CTAS)) {
         const int64_t k = g_trace_next.fetch_add(1);
-        if (k < g_trace_slots.load()) p.trace = tb + k * TRACE_MAX_CTAS * 4;
+        if (k < g_trace_slots.load()) {
+            DevInfo dev;
+            qmv_status s = device_info(dev);
+            if (s == QMV_OK) s = ensure_smem_attr(dev, L.probe);
+            if (s != QMV_OK) return s;
+            p.trace = tb + k * TRACE_MAX_CTAS * 4;
+            fn = L.probe;
+        }
     }
     void *args[1] = {&p};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, args);
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     return cuda_status(e);
 }
 
@@ -835,7 +861,10 @@ qmv_status qmv_debug_f32_withheld_share(int type, const void *W, int64_t M, int6
     p.y = y;
     Launch L;
     if ((s = plan_f32(type, MODE_PLAIN, dev, p, ncols, 1, L)) != QMV_OK) return s;
-    if (L.cluster < 2 || L.fn == gemv_tiles_mma_fn_q4_K(MODE_PLAIN)) return QMV_ERR_CONFIG;
+    if (L.cluster < 2 || !L.probe) return QMV_ERR_CONFIG;
+    if ((s = ensure_smem_attr(dev, L.probe)) != QMV_OK) return s;
+    L.fn = L.probe;
+    L.probe = nullptr;  // not traced: the timeline is of the ordinary launches
     L.p.withhold = 1;
     L.p.withhold_wait_ns = wait_ns;
     return launch(L, static_cast<cudaStream_t>(stream));

@@ -9,6 +9,8 @@ namespace qmv {
 
 const void *gemv_tiles_fn_q4_K(int mode, int nc, int rw) { return tiles_kernel_fn<FMT_Q4_K>(mode, nc, rw); }
 
+const void *gemv_tiles_probe_fn_q4_K(int mode, int nc) { return tiles_probe_kernel_fn<FMT_Q4_K>(mode, nc); }
+
 const void *gemv_tiles_mma_fn_q4_K(int mode) { return tiles_mma_kernel_fn<FMT_Q4_K>(mode); }
 
 const void *gemv_generic_fn_q4_K(int mode)

@@ -8,6 +8,8 @@ namespace qmv {
 
 const void *gemv_tiles_fn_q6_K(int mode, int nc, int rw) { return tiles_kernel_fn<FMT_Q6_K>(mode, nc, rw); }
 
+const void *gemv_tiles_probe_fn_q6_K(int mode, int nc) { return tiles_probe_kernel_fn<FMT_Q6_K>(mode, nc); }
+
 const void *gemv_generic_fn_q6_K(int mode)
 {
     constexpr int F = FMT_Q6_K;

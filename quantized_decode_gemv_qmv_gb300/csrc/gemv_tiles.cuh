@@ -99,8 +99,9 @@ inline int tile_bytes_rt(int type, int rw, bool tc = false)
 // stores each result into the shared memory of every CTA of the cluster
 // (distributed shared memory), so the work is not repeated in every CTA; the
 // caller has made sure every CTA of the cluster is running, and completes the
-// exchange with a cluster barrier.
-template <int F, int NC, typename ColFn>
+// exchange with a cluster barrier.  WITHHOLD (instrumented kernels only):
+// when p.withhold is set, the CTA of rank 1 keeps its share to itself.
+template <int F, int NC, bool WITHHOLD, typename ColFn>
 __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint8_t *smem, int n_active, ColFn src_col,
                                                        uint32_t crank, uint32_t ncta, uint32_t xbar)
 {
@@ -170,7 +171,7 @@ __device__ __forceinline__ void stage_tile_activations(const GemvParams &p, uint
                             if (i < nw) asm volatile("st.shared.u32 [%0], %1;" ::"r"(sc + off[i]), "r"(val[i]) : "memory");
                     }
                     for (uint32_t q = 0; q < ncta; ++q) {
-                        if (q == crank || (p.withhold && crank == 1)) continue;
+                        if (q == crank || (WITHHOLD && p.withhold && crank == 1)) continue;
                         const uint32_t bq = mapa_shared(xbar, q);
                         st_async_v2(mapa_shared(dq, q), w0, w1, bq);
                         if (j == 0) {
@@ -251,7 +252,24 @@ __device__ __forceinline__ uint32_t cluster_share_bytes(int n_all, uint32_t cran
     return static_cast<uint32_t>((n_all - (blk1 - blk0)) * per_block);
 }
 
-template <int F, int NC, int MODE, int RW, bool TC = false>
+// A warp whose activations never arrived: code 2 in the fault word, and NaN in
+// every output of its rows r0 .. r_end-1, so a bad result cannot pass for a
+// good one.  Out of line, so that the code the warp runs when the activations
+// do arrive stays as short as without it (inline, it made the step's launches
+// about 0.5 % slower on GB300).
+static __device__ __noinline__ void give_up_rows(float *y, int64_t ldy, int ncols, int64_t r0, int64_t r_end, int lane,
+                                                 unsigned int *fault)
+{
+    if (lane == 0 && fault) atomicOr(fault, FAULT_CLUSTER_STAGING);
+    for (int64_t r = r0 + lane; r < r_end; r += 32)
+        for (int c = 0; c < ncols; ++c) y[(size_t)c * ldy + r] = __int_as_float(0x7fc00000);
+}
+
+// PROBE: the instrumented twin of a kernel (qmv_debug.h): the same code plus
+// the timeline stores (p.trace) and the withheld share (p.withhold).  The
+// ordinary kernels carry neither: the instructions would sit on the path from
+// the dependency wait to the first decode, which every launch pays.
+template <int F, int NC, int MODE, int RW, bool TC = false, bool PROBE = false>
 __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEBUG) ? 2 : 1)
     gemv_tiles_kernel(const GemvParams p)
 {
@@ -284,7 +302,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     pdl_launch_dependents();
     // optional timeline (qmv_debug_trace): entry, after the dependency wait,
     // activations staged, last warp done
-    unsigned long long *const trace = p.trace ? p.trace + 4 * blockIdx.x : nullptr;
+    unsigned long long *const trace = (PROBE && p.trace) ? p.trace + 4 * blockIdx.x : nullptr;
     if (trace && threadIdx.x == 0) trace[0] = global_timer_ns();
     // fp32 input in a cluster: the CTAs share the quantization (see
     // stage_tile_activations); this arrive lets the others know this CTA runs
@@ -479,11 +497,11 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     if (!MMA && ncta > 1 && threadIdx.x == 0)
         mbar_arrive_expect_tx(xbar, cluster_share_bytes<F>(p.ncols * p.units_per_row * 8, crank, ncta));
     if constexpr (IS_MOE)
-        stage_tile_activations<F, NC>(p, smem, n_active, [&](int c) { return s_tok[c]; }, 0u, 1u, 0u);
+        stage_tile_activations<F, NC, PROBE>(p, smem, n_active, [&](int c) { return s_tok[c]; }, 0u, 1u, 0u);
     else if constexpr (MMA)
         stage_mma_activations(p, smem, n_active, [](int c) { return c; }, crank, ncta);
     else
-        stage_tile_activations<F, NC>(p, smem, n_active, [](int c) { return c; }, crank, ncta, xbar);
+        stage_tile_activations<F, NC, PROBE>(p, smem, n_active, [](int c) { return c; }, crank, ncta, xbar);
     if (ncta > 1 && MMA) {
         cluster_arrive();  // this CTA's share is stored everywhere ...
         cluster_wait();    // ... and every share is here; no remote access after this point
@@ -493,15 +511,13 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         // a partner stores here is counted, so none is still in flight after
         // the wait and no CTA can exit while a partner writes to it)
         __syncthreads();
-        const unsigned long long lim = (p.withhold && crank == 0) ? p.withhold_wait_ns : WAIT_LIMIT_NS;
-        if (__syncthreads_or(!mbar_wait_bounded(xbar, 0, lim))) {
-            // A partner's share never arrived: nothing is computed.  NaN marks
-            // every output of this CTA's rows invalid, the fault word tells the
-            // host, and the CTA leaves once its own weight copies have landed.
-            if (threadIdx.x == 0 && p.fault) atomicOr(p.fault, FAULT_CLUSTER_STAGING);
-            const int64_t r_end = min64(p.M, (g_begin + my_groups) * RW);
-            for (int64_t r = g_begin * RW + lane; r < r_end; r += 32)
-                for (int c = 0; c < p.ncols; ++c) p.y[(size_t)c * p.ldy + r] = __int_as_float(0x7fc00000);
+        const unsigned long long lim = (PROBE && p.withhold && crank == 0) ? p.withhold_wait_ns : WAIT_LIMIT_NS;
+        if (__builtin_expect(__any_sync(0xffffffffu, !mbar_wait_bounded(xbar, 0, lim)), 0)) {
+            // A partner's share never arrived: this warp computes nothing
+            // (give_up_rows), and leaves once its own weight copies have
+            // landed.  Each warp decides for itself, so a share that lands
+            // just at the limit leaves every row either right or NaN.
+            give_up_rows(p.y, p.ldy, p.ncols, g_begin * RW, min64(p.M, (g_begin + my_groups) * RW), lane, p.fault);
             cp_async_wait(0);
             return;
         }
@@ -665,6 +681,17 @@ const void *tiles_mma_kernel_fn(int mode)
     if constexpr (F == FMT_Q4_K)
         if (mode == MODE_PLAIN)
             return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, MMA_COLS, MODE_PLAIN, MMA_RW, true>);
+    return nullptr;
+}
+
+// The instrumented twins (PROBE) exist for the plain GEMV of one or two
+// columns and the fused gate/up GEMV of one column, 4-row tiles, dp4a decode.
+template <int F>
+const void *tiles_probe_kernel_fn(int mode, int nc)
+{
+    if (mode == MODE_PLAIN && nc == 1) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_PLAIN, 4, false, true>);
+    if (mode == MODE_PLAIN && nc == 2) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 2, MODE_PLAIN, 4, false, true>);
+    if (mode == MODE_GATE && nc == 1) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_GATE, 4, false, true>);
     return nullptr;
 }
 

@@ -4,7 +4,7 @@ The fp32-input GEMV shares the quantization of x among the CTAs of a cluster;
 each CTA waits, with a time limit, for its partners' shares.  The test-only
 entry qmv_debug_f32_withheld_share has the rank-1 CTA of every cluster keep
 its share, so the rank-0 CTA's wait (1 ms here) runs out.  Checked: the call
-returns; the device fault word reads code 2; the rows of the CTAs that gave up
+returns; the device fault word reads code 2; the rows of the warps that gave up
 are NaN in every column, and every other output is bit for bit the ordinary
 call's; the next ordinary call finds the fault word clear, matches the oracle
 and leaves the word clear.  No kernel hangs or faults: the withholding CTA still
@@ -53,7 +53,7 @@ def host(t):
     return t.cpu().numpy()
 
 
-@pytest.mark.parametrize("t,M,K,ncols", [(oracle.Q4_K, 4096, 4096, 1), (oracle.Q4_K, 1003, 2048, 3),
+@pytest.mark.parametrize("t,M,K,ncols", [(oracle.Q4_K, 4096, 4096, 1), (oracle.Q4_K, 1003, 2048, 2),
                                          (oracle.Q6_K, 517, 4096, 2), (oracle.Q4_0, 700, 1024, 1)])
 def test_withheld_share_runs_the_wait_out(q, t, M, K, ncols):
     W = oracle.quantize_rows(t, synthetic.weights_f32(2200 + M, M, K))
@@ -79,3 +79,15 @@ def test_withheld_share_runs_the_wait_out(q, t, M, K, ncols):
     xq = oracle.quantize_q8_1(x)
     y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq, ncols)
     assert np.all(np.abs(y2.astype(np.float64) - y_ref) <= TOL * l1)
+
+
+def test_withheld_share_needs_an_instrumented_kernel(q):
+    """Three columns have no instrumented twin: refused before any launch."""
+    t, M, K = oracle.Q4_K, 512, 2048
+    W = oracle.quantize_rows(t, synthetic.weights_f32(2300, M, K))
+    x = synthetic.activations_f32(2301, 3, K)
+    y = dev(np.full((3, M), 7.0, np.float32))
+    with pytest.raises(q.QmvError) as e:
+        q.debug_f32_withheld_share(t, dev(W), M, K, dev(x), 1_000_000, out=y)
+    assert e.value.status == 10
+    assert np.all(host(y) == 7.0) and q.device_fault() == 0
