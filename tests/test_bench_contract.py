@@ -28,3 +28,18 @@ def test_reference_arm_json_line():
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert d["vs_baseline"] is None
+
+
+def test_traffic_figure_belongs_to_the_current_kernel_sources():
+    """The bench line's roofline.traffic is a DRAM byte count taken with ncu
+    from the kernels as they are; it is keyed to a hash of the kernel sources.
+    A kernel edit without a new capture would silently null the figure, so a
+    stale key fails here: re-run the DRAM metrics pass over the step's four
+    launch kinds and update bench.TRAFFIC."""
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    assert bench.TRAFFIC["csrc_sha"] == bench.csrc_sha(), (bench.TRAFFIC["csrc_sha"], bench.csrc_sha())
+    assert bench.TRAFFIC["bytes_per_launch"] > 0
