@@ -61,7 +61,7 @@ MMA_MIN_COLS = 9
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "086c80bd64dcf129", "bytes_per_launch": 28535456,
+TRAFFIC = {"csrc_sha": "98b95de6f5bcff67", "bytes_per_launch": 28534560,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down"}
 
 
@@ -894,9 +894,11 @@ def run_trace(args):
     (the benchmark's chained per-call setting) is replayed with the timeline on,
     and every launch k >= 1 is measured against the one before it: the PDL
     release (previous launch's last CTA done -> first wait return), the
-    activation staging (wait return -> staged, median over CTAs), the decode
-    tail (median staged -> last CTA done), the spread of CTA finish times and
-    the launch period (last CTA done to last CTA done)."""
+    activation staging (wait return -> staged, median over CTAs) and its
+    parts (wait return -> first activation loads returned -> own part of the
+    staging done -> all activations in shared memory), the decode tail
+    (median staged -> last CTA done), the spread of CTA finish times and the
+    launch period (last CTA done to last CTA done)."""
     import numpy as np
     import torch
 
@@ -932,7 +934,8 @@ def run_trace(args):
         x = torch.from_numpy(synthetic.activations_f32(77, 1, K, outlier_frac=0.01)).to(dev)
         xq = q.quantize_q8_1(x, stream=s)
         y = torch.empty((1, M), dtype=torch.float32, device=dev)
-        buf = torch.zeros(n * q.TRACE_MAX_CTAS * 4, dtype=torch.int64, device=dev)
+        W_ = q.TRACE_WORDS
+        buf = torch.zeros(n * q.TRACE_MAX_CTAS * W_, dtype=torch.int64, device=dev)
 
         def chain():
             for W in Ws:
@@ -958,22 +961,30 @@ def run_trace(args):
             buf.zero_()
             g.replay()
         s.synchronize()
-        T = buf.view(n, q.TRACE_MAX_CTAS, 4).cpu().numpy().astype(np.float64)
+        T = buf.view(n, q.TRACE_MAX_CTAS, W_).cpu().numpy().astype(np.float64)
         rows = []
         for k in range(1, n):
             cur = T[k][T[k][:, 0] > 0]
             prev = T[k - 1][T[k - 1][:, 0] > 0]
-            prev_done = prev[:, 3].max()
+            prev_done = prev[:, 5].max()
             rows.append([cur[:, 1].min() - prev_done,                # release
-                         np.median(cur[:, 2] - cur[:, 1]),            # staging
-                         cur[:, 3].max() - np.median(cur[:, 2]),      # decode tail
-                         cur[:, 3].max() - np.median(cur[:, 3]),      # last CTA behind the median one
+                         np.median(cur[:, 4] - cur[:, 1]),            # staging
+                         np.median(cur[:, 2] - cur[:, 1]),            #   wait -> first loads returned
+                         np.median(cur[:, 3] - cur[:, 2]),            #   first loads -> own part done
+                         np.median(cur[:, 4] - cur[:, 3]),            #   own part -> all activations in
+                         cur[:, 5].max() - np.median(cur[:, 4]),      # decode tail
+                         cur[:, 5].max() - np.median(cur[:, 5]),      # last CTA behind the median one
                          cur[:, 0].min() - prev_done,                 # first CTA entry (negative: early)
-                         cur[:, 3].max() - prev_done])                # period
+                         cur[:, 5].max() - prev_done])                # period
         r = np.median(np.asarray(rows), axis=0) / 1e3
-        out[name] = {"release_us": round(r[0], 3), "staging_us": round(r[1], 3), "tail_us": round(r[2], 3),
-                     "last_cta_behind_median_us": round(r[3], 3), "first_entry_us": round(r[4], 3),
-                     "period_us": round(r[5], 3), "ideal_us": round(wb / 6668.5e3, 3), "launches": n - 1,
+        # the staging parts need stamps [2] and [3], which only the coalesced
+        # staging paths write (not the per-unit q8_1 staging)
+        parts = bool(np.all(T[1:, :, 2][T[1:, :, 0] > 0] > 0))
+        part = (lambda v: round(v, 3)) if parts else (lambda v: None)
+        out[name] = {"release_us": round(r[0], 3), "staging_us": round(r[1], 3), "first_loads_us": part(r[2]),
+                     "own_part_us": part(r[3]), "complete_us": part(r[4]), "tail_us": round(r[5], 3),
+                     "last_cta_behind_median_us": round(r[6], 3), "first_entry_us": round(r[7], 3),
+                     "period_us": round(r[8], 3), "ideal_us": round(wb / 6668.5e3, 3), "launches": n - 1,
                      "ctas": int((T[1][:, 0] > 0).sum())}
         print(json.dumps({name: out[name]}), flush=True)
         del Ws, buf

@@ -291,6 +291,19 @@ qmv_status qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
  * every setting.  Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above. */
 qmv_status qmv_set_early_warps(int type, int early_warps);
 
+/* Delay, in ns, between the start of a CTA and its early weight requests, for
+ * launches of `type` in which every warp requests all of its tiles before the
+ * dependency wait and the next kernel's CTA fits beside this one on the SM
+ * (the 4096x4096 class of shapes).  Such a CTA typically starts just as the
+ * kernel beside it passes its own dependency wait; holding the requests back
+ * lets that kernel's activation loads reach the memory system first, while
+ * the tiles still land long before this launch needs them.  ns: 1..100000
+ * sets the delay, 0 restores the built-in default (400 ns, measured on
+ * GB300), -1 turns it off.  Results are identical for every setting.
+ * Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above.  (A tuning entry point of
+ * this library; the pages have no counterpart.) */
+qmv_status qmv_set_early_delay(int type, int ns);
+
 /* Column count from which the plain GEMV of `type` (qmv_mul_mat_vec, its
  * fp32-input and fused forms) decodes with the tensor cores instead of the
  * per-column dp4a: 8-row tiles multiplied by all columns at once with
@@ -339,9 +352,9 @@ qmv_status qmv_describe_gemv(int type, int gate_up, int64_t M, int64_t K, int nc
 /* Environment override of the geometry knobs above, for tuning runs:
  * QMV_GEOM="type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K
  * and keys threads, slice_units, stages, ctas_per_sm, smem_share, cluster,
- * dec_warps, pre_tiles, early_warps and mma_min_cols (the arguments of
- * qmv_set_tuning, qmv_set_stream_tuning, qmv_set_early_warps and
- * qmv_set_mma_min_cols, same ranges).  It is read
+ * dec_warps, pre_tiles, early_warps, early_delay_ns and mma_min_cols (the
+ * arguments of qmv_set_tuning, qmv_set_stream_tuning, qmv_set_early_warps,
+ * qmv_set_early_delay and qmv_set_mma_min_cols, same ranges).  It is read
  * once, before the first GEMV-family call is planned, and applied through
  * those setters; later setter calls override it.  A malformed spec or an
  * out-of-range value makes every GEMV-family call return QMV_ERR_CONFIG

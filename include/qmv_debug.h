@@ -55,12 +55,16 @@ qmv_status qmv_debug_f32_withheld_share(int type, const void *W, int64_t M, int6
  * time goes.  While enabled, each of the next `slots` launches that have an
  * instrumented twin (any call of qmv.h whose launch takes one; other launches
  * are not recorded and take no slot) runs the twin, which writes, per CTA b,
- * four globaltimer readings (ns) into buf + (k*1024 + b)*4, k = the launch's
+ * six globaltimer readings (ns) into buf + (k*1024 + b)*6, k = the launch's
  * index since this call: [0] the CTA's first instruction, [1] the return of the
  * wait for the previous kernel on the stream (programmatic dependent launch),
- * [2] its activations staged in shared memory, [3] the last of its warps done
- * (an atomic max, so [3] must be zero beforehand).  buf: device memory of
- * slots * 1024 * 4 * 8 bytes, 8-byte aligned; launches of more than 1024 CTAs
+ * [2] its first activation loads returned (thread 0), [3] its own part of the
+ * staging done (thread 0: fp32 input, its share quantized and sent to the
+ * cluster; q8_1 input, the blocks repacked), [4] all activations in its shared
+ * memory (after the CTA barrier and the partners' shares), [5] the last of its
+ * warps done (an atomic max, so [5] must be zero beforehand).  [2] and [3]
+ * stay zero where q8_1 input is not 16-byte aligned (another staging path).
+ * buf: device memory of slots * 1024 * 6 * 8 bytes, 8-byte aligned; launches of more than 1024 CTAs
  * and launches past the slots are not recorded.  Under CUDA graph capture the
  * slot is fixed when the call is captured.  buf NULL or slots 0 disables it.
  * Costs nothing when disabled.  Not thread-safe with

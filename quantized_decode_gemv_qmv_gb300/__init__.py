@@ -31,7 +31,7 @@ EXPORTS = (
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv", "qmv_read_bandwidth_probe",
-    "qmv_set_early_warps", "qmv_debug_f32_withheld_share", "qmv_debug_trace",
+    "qmv_set_early_warps", "qmv_set_early_delay", "qmv_debug_f32_withheld_share", "qmv_debug_trace",
 )
 
 
@@ -95,6 +95,7 @@ def lib():
         L.qmv_set_checked.argtypes = [_int]
         L.qmv_set_mma_min_cols.argtypes = [_int, _int]
         L.qmv_set_early_warps.argtypes = [_int, _int]
+        L.qmv_set_early_delay.argtypes = [_int, _int]
         L.qmv_read_bandwidth_probe.argtypes = [_vp, ctypes.c_size_t, _vp, _vp]
         L.qmv_describe_gemv.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.POINTER(LaunchInfo)]
         L.qmv_debug_f32_withheld_share.argtypes = [_int, _vp, _i64, _i64, _vp, _i64, _int, _vp, ctypes.c_uint64, _vp]
@@ -105,7 +106,7 @@ def lib():
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
                      "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
-                     "qmv_read_bandwidth_probe", "qmv_set_early_warps", "qmv_debug_f32_withheld_share",
+                     "qmv_read_bandwidth_probe", "qmv_set_early_warps", "qmv_set_early_delay", "qmv_debug_f32_withheld_share",
                      "qmv_debug_trace"):
             getattr(L, name).restype = _int
         _lib = L
@@ -461,19 +462,20 @@ def debug_f32_withheld_share(qtype: int, W, M: int, K: int, x, wait_ns: int, out
 
 
 TRACE_MAX_CTAS = 1024
+TRACE_WORDS = 6  # stamps per CTA: entry, wait returned, first loads, own staging, staged, done
 
 
 def debug_trace(buf=None, slots: int = 0):
     """Diagnostics: per-CTA timestamps of the next `slots` GEMV launches that
     have an instrumented twin (plain, 1-2 columns; gate/up, 1 column) into buf
-    (int64 CUDA tensor of slots*1024*4, zeroed); None stops (see
+    (int64 CUDA tensor of slots*1024*6, zeroed); None stops (see
     include/qmv_debug.h, qmv_debug_trace)."""
     import torch
 
     if buf is None:
         _check("qmv_debug_trace", lib().qmv_debug_trace(None, 0))
         return
-    _tensor(buf, "buf", torch.int64, slots * TRACE_MAX_CTAS * 4 * 8)
+    _tensor(buf, "buf", torch.int64, slots * TRACE_MAX_CTAS * TRACE_WORDS * 8)
     _device_of((("buf", buf),))
     _check("qmv_debug_trace", lib().qmv_debug_trace(_ptr(buf), slots))
 
@@ -517,6 +519,12 @@ def describe_gemv(qtype: int, M: int, K: int, ncols: int = 1, gate_up: bool = Fa
 def set_early_warps(qtype: int, early_warps: int = 0):
     """Decoding warps that request tiles before the dependency wait (0: all)."""
     _check("qmv_set_early_warps", lib().qmv_set_early_warps(qtype, early_warps))
+
+
+def set_early_delay(qtype: int, ns: int = 0):
+    """Delay in ns of the early weight requests of launches that request their
+    whole matrix early (0: the default, -1: none; see include/qmv.h)."""
+    _check("qmv_set_early_delay", lib().qmv_set_early_delay(qtype, ns))
 
 
 def set_mma_min_cols(qtype: int, min_cols: int = 0):

@@ -78,12 +78,15 @@ constexpr int MAX_CLUSTER = 8;         // portable cluster size limit
 // MoE experts per call: the generic kernel gives every expert one grid row
 // plus one for the invalid ids, and gridDim.y is at most 65535
 constexpr int64_t MAX_EXPERTS = 65534;
+// Delay of the early weight requests of launches that request their whole
+// matrix early (plan_tiles).
+constexpr int EARLY_DELAY_NS = 400;
 
 std::atomic<int> g_pdl{1};
 
 // Diagnostic timeline (qmv_debug_trace): the next g_trace_slots launches that
-// have an instrumented twin run it, each with a slot of TRACE_MAX_CTAS x 4
-// timestamps.
+// have an instrumented twin run it, each with a slot of TRACE_MAX_CTAS x
+// TRACE_WORDS timestamps.
 constexpr int TRACE_MAX_CTAS = 1024;
 std::atomic<unsigned long long *> g_trace_buf{nullptr};
 std::atomic<int64_t> g_trace_slots{0}, g_trace_next{0};
@@ -93,6 +96,7 @@ struct Tuning {
     std::atomic<int> dec_warps{0}, pre_tiles{0};
     std::atomic<int> mma_min_cols{0};  // 0: MMA_MIN_COLS; 9: never
     std::atomic<int> early_warps{0};   // 0: every decoding warp requests its early tiles
+    std::atomic<int> early_delay_ns{0};  // 0: EARLY_DELAY_NS; -1: no delay
 };
 Tuning g_tuning[3];
 
@@ -103,6 +107,7 @@ std::map<std::tuple<int, const void *, int, size_t>, int> g_occupancy;  // (dev,
 std::map<std::tuple<int, const void *, int, size_t, int>, int> g_clusters;  // (..., cluster size) -> resident clusters
 std::map<std::pair<int, const void *>, bool> g_smem_attr;
 int g_num_sms[MAX_DEVICES];
+int g_clock_khz[MAX_DEVICES];
 int g_smem_optin[MAX_DEVICES];
 int g_smem_sm[MAX_DEVICES];
 int g_smem_resv[MAX_DEVICES];
@@ -114,6 +119,7 @@ qmv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_E
 struct DevInfo {
     int dev;
     int num_sms;
+    int clock_khz;      // peak SM clock
     size_t smem_limit;  // dynamic shared memory a CTA may use
     size_t smem_per_sm; // shared memory of one SM
     size_t smem_resv;   // shared memory the hardware reserves per CTA
@@ -124,7 +130,8 @@ struct DevInfo {
 // "type:key=value,key=value;type:..." with type q4_0, q4_K or q6_K and keys
 // threads, slice_units, stages, ctas_per_sm, smem_share, cluster (as for
 // qmv_set_tuning), dec_warps, pre_tiles (qmv_set_stream_tuning),
-// early_warps (qmv_set_early_warps) and mma_min_cols (qmv_set_mma_min_cols).
+// early_warps (qmv_set_early_warps), early_delay_ns (qmv_set_early_delay) and
+// mma_min_cols (qmv_set_mma_min_cols).
 // Read once, before the first GEMV call is planned; values go through the
 // setters' range checks.
 std::once_flag g_geom_once;
@@ -148,14 +155,14 @@ bool apply_geom_entry(const std::string &entry)
     const int type = tname == "q4_0" ? FMT_Q4_0 : tname == "q4_K" ? FMT_Q4_K : tname == "q6_K" ? FMT_Q6_K : -1;
     if (type < 0) return false;
     const Tuning &cur = g_tuning[tidx(type)];
-    constexpr int NK = 10;
+    constexpr int NK = 11;
     int v[NK] = {cur.threads.load(),     cur.slice_units.load(), cur.stages.load(),
                  cur.ctas_per_sm.load(), cur.smem_share.load(),  cur.cluster.load(),
                  cur.dec_warps.load(),   cur.pre_tiles.load(),   cur.mma_min_cols.load(),
-                 cur.early_warps.load()};
+                 cur.early_warps.load(), cur.early_delay_ns.load()};
     static const char *const keys[NK] = {"threads",   "slice_units", "stages",       "ctas_per_sm", "smem_share",
                                          "cluster",   "dec_warps",   "pre_tiles",    "mma_min_cols",
-                                         "early_warps"};
+                                         "early_warps", "early_delay_ns"};
     size_t pos = colon + 1;
     while (pos <= entry.size()) {
         size_t comma = entry.find(',', pos);
@@ -170,7 +177,7 @@ bool apply_geom_entry(const std::string &entry)
     }
     return qmv_set_tuning(type, v[0], v[1], v[2], v[3], v[4], v[5]) == QMV_OK &&
            qmv_set_stream_tuning(type, v[6], v[7]) == QMV_OK && qmv_set_mma_min_cols(type, v[8]) == QMV_OK &&
-           qmv_set_early_warps(type, v[9]) == QMV_OK;
+           qmv_set_early_warps(type, v[9]) == QMV_OK && qmv_set_early_delay(type, v[10]) == QMV_OK;
 }
 
 qmv_status geom_env()
@@ -213,12 +220,16 @@ qmv_status device_info(DevInfo &d)
         int resv = 0;
         if (cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, d.dev) != cudaSuccess) resv = 1024;
         g_smem_resv[d.dev] = resv;
+        int khz = 0;
+        if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, d.dev) != cudaSuccess || khz <= 0) khz = 2000000;
+        g_clock_khz[d.dev] = khz;
         void *f = nullptr;
         if (cudaGetSymbolAddress(&f, g_fault_word) != cudaSuccess) return QMV_ERR_CUDA;
         g_fault_ptr[d.dev] = static_cast<unsigned int *>(f);
         g_num_sms[d.dev] = n;
     }
     d.num_sms = g_num_sms[d.dev];
+    d.clock_khz = g_clock_khz[d.dev];
     d.smem_limit = static_cast<size_t>(g_smem_optin[d.dev]) - SMEM_RESERVE;
     d.smem_per_sm = static_cast<size_t>(g_smem_sm[d.dev]);
     d.smem_resv = static_cast<size_t>(g_smem_resv[d.dev]);
@@ -479,6 +490,18 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     p.pre_tiles = tu.pre_tiles.load() > 0 ? std::min(stages, tu.pre_tiles.load())
                                           : (tiles_per_warp <= stages ? stages : 1);
     p.early_warps = tu.early_warps.load() > 0 ? tu.early_warps.load() : wpc;
+    // Where every warp requests all of its tiles early and the next kernel's
+    // CTA can sit beside this one, those requests wait EARLY_DELAY_NS after the
+    // CTA starts (see the kernel).  Measured on GB300: 4096x4096 Q4_K chained
+    // 3.59 -> 3.00 us per call, the step's o launch 4.61 -> 4.29 us, no launch
+    // slower; the same delay on launches that stream more than their rings hold
+    // made 14336x4096 and the Q6_K 4096x14336 launch 1-2 % slower.
+    p.early_delay = 0;
+    if (!is_moe && tiles_per_warp <= p.pre_tiles && tu.early_delay_ns.load() >= 0 &&
+        occupancy(dev.dev, fn, cta_warps * 32, smem) >= 2) {
+        const int ns = tu.early_delay_ns.load() > 0 ? tu.early_delay_ns.load() : EARLY_DELAY_NS;
+        p.early_delay = static_cast<int>(static_cast<int64_t>(ns) * dev.clock_khz / 1000000);
+    }
     p.act_bytes = static_cast<uint32_t>(act);
     p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
     L.fn = fn;
@@ -577,7 +600,7 @@ qmv_status launch(const Launch &L, cudaStream_t st)
             qmv_status s = device_info(dev);
             if (s == QMV_OK) s = ensure_smem_attr(dev, L.probe);
             if (s != QMV_OK) return s;
-            p.trace = tb + k * TRACE_MAX_CTAS * 4;
+            p.trace = tb + k * TRACE_MAX_CTAS * TRACE_WORDS;
             fn = L.probe;
         }
     }
@@ -1144,6 +1167,14 @@ qmv_status qmv_set_early_warps(int type, int early_warps)
     if (!weight_type(type)) return QMV_ERR_TYPE;
     if (early_warps < 0 || early_warps > TILE_MAX_THREADS / 32) return QMV_ERR_SHAPE;
     g_tuning[tidx(type)].early_warps = early_warps;
+    return QMV_OK;
+}
+
+qmv_status qmv_set_early_delay(int type, int ns)
+{
+    if (!weight_type(type)) return QMV_ERR_TYPE;
+    if (ns < -1 || ns > 100000) return QMV_ERR_SHAPE;
+    g_tuning[tidx(type)].early_delay_ns = ns;
     return QMV_OK;
 }
 

@@ -37,6 +37,7 @@ struct GemvParams {
     int dec_warps;       // tile kernel: warps that stream and decode (the first ones; the rest only stage)
     int pre_tiles;       // tile kernel: tiles per warp requested before the dependency wait (1..stages)
     int early_warps;     // tile kernel: warps that make those early requests (the first ones; >= dec_warps: all)
+    int early_delay;     // tile kernel: SM clock cycles from the CTA's start to its early requests (0: none)
     uint32_t act_bytes;  // tile kernel: shared bytes of the activation area
     uint32_t raw_off;    // tile kernel: offset of the raw q8_1 copy inside the activation area (0: none)
     unsigned long long *trace;  // diagnostics: per-CTA timestamps [entry, waited, staged, done] (nullable)

@@ -151,6 +151,9 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.qmv_set_mma_min_cols(12, 0) == 0
     assert L.qmv_set_early_warps(12, 13) == 3 and L.qmv_set_early_warps(12, -1) == 3
     assert L.qmv_set_early_warps(2, 0) == 0 and L.qmv_set_early_warps(9, 0) == 2
+    assert L.qmv_set_early_delay(12, -2) == 3 and L.qmv_set_early_delay(12, 100001) == 3
+    assert L.qmv_set_early_delay(9, 0) == 2 and L.qmv_set_early_delay(12, -1) == 0
+    assert L.qmv_set_early_delay(12, 0) == 0
     assert L.qmv_debug_trace(p, -1) == 3 and L.qmv_debug_trace(ctypes.c_void_p(0x1004), 1) == 5
     assert L.qmv_debug_trace(nul, 0) == 0
     rp = L.qmv_read_bandwidth_probe

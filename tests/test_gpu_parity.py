@@ -254,6 +254,28 @@ def test_stream_tuning_variants_agree(q, t):
         q.set_stream_tuning(t)
 
 
+
+@pytest.mark.parametrize("t", [oracle.Q4_0, oracle.Q4_K])
+def test_early_delay_changes_nothing(q, t):
+    # a 4096x4096 launch requests its whole matrix before the dependency wait,
+    # which the planner holds back by a short delay; no delay, the default and
+    # a long one give bitwise-equal results, q8_1 and fp32 input alike
+    M, K = 4096, 4096
+    W = weights(t, M, K, 720 + t)
+    x = synthetic.activations_f32(721, 1, K)
+    xq = oracle.quantize_q8_1(x)
+    y_ref, l1 = oracle.gemv_formula(t, W, M, K, xq, 1)
+    Wd, xd, xfd = dev(W), dev(xq), dev(x)
+    y0 = host(q.mul_mat_vec(t, Wd, M, K, xd, 1))
+    assert_close_l1(y0, y_ref, l1, f"type {t} default delay")
+    try:
+        for ns in (-1, 5000, 0):
+            q.set_early_delay(t, ns)
+            assert np.array_equal(host(q.mul_mat_vec(t, Wd, M, K, xd, 1)), y0), f"type {t} delay {ns}"
+            assert np.array_equal(host(q.mul_mat_vec_f32(t, Wd, M, K, xfd)), y0), f"type {t} delay {ns} fp32"
+    finally:
+        q.set_early_delay(t, 0)
+
 # ---- fused gate/up + SwiGLU ------------------------------------------------------
 def _swiglu_tol(g, u, l1g, l1u):
     sig = 1.0 / (1.0 + np.exp(-g))

@@ -1,11 +1,12 @@
 """The launch timeline (qmv_debug_trace) and its instrumented kernels.
 
 While the timeline is on, launches that have an instrumented twin run it and
-write four timestamps per CTA; other launches are not recorded and take no
+write six timestamps per CTA; other launches are not recorded and take no
 slot.  Checked: a traced launch's outputs are bit for bit the ordinary
-launch's; every CTA of a recorded launch has its four stamps in order (entry,
-dependency wait returned, activations staged, last warp done) and no CTA past
-the grid has any; a launch without a twin leaves its slot free; nothing is
+launch's; every CTA of a recorded launch has its six stamps in order (entry,
+dependency wait returned, first activation loads returned, its own part of the
+staging done, all activations in shared memory, last warp done) and no CTA
+past the grid has any; a launch without a twin leaves its slot free; nothing is
 written past the enabled slots; with programmatic dependent launch, a
 dependent launch's wait returns no earlier than its predecessor's last CTA
 finished.
@@ -18,7 +19,7 @@ import synthetic
 
 pytestmark = pytest.mark.gpu
 
-SLOT = 1024 * 4  # int64 words per slot: 1024 CTAs x 4 stamps
+SLOT = 1024 * 6  # int64 words per slot: 1024 CTAs x 6 stamps
 CLOCK_SLACK_NS = 1000  # globaltimer ticks and SM-to-SM skew, generously
 
 
@@ -55,8 +56,8 @@ def host(t):
 
 
 def stamps(buf, k, grid):
-    """Slot k as [grid][4], and whether every CTA past the grid is blank."""
-    s = host(buf)[k * SLOT:(k + 1) * SLOT].reshape(1024, 4)
+    """Slot k as [grid][6], and whether every CTA past the grid is blank."""
+    s = host(buf)[k * SLOT:(k + 1) * SLOT].reshape(1024, 6)
     return s[:grid], not s[grid:].any()
 
 
@@ -96,11 +97,11 @@ def test_timeline_of_instrumented_launches(q):
     s1, blank1 = stamps(buf, 1, gg)
     assert blank0 and blank1
     for s_ in (s0, s1):
-        assert np.all(s_ > 0), "every CTA of a recorded launch writes all four stamps"
-        assert np.all(np.diff(s_, axis=1) >= 0), "entry <= wait returned <= staged <= done"
+        assert np.all(s_ > 0), "every CTA of a recorded launch writes all six stamps"
+        assert np.all(np.diff(s_, axis=1) >= 0), "entry <= wait <= loads <= own part <= staged <= done"
     assert not host(buf)[2 * SLOT:].any(), "nothing is written past the enabled slots"
     # the gate/up launch depends on the plain one: its wait returns after the plain one's last CTA
-    assert s1[:, 1].min() >= s0[:, 3].max() - CLOCK_SLACK_NS
+    assert s1[:, 1].min() >= s0[:, 5].max() - CLOCK_SLACK_NS
 
 
 def test_launch_without_twin_takes_no_slot(q):
