@@ -61,7 +61,7 @@ MMA_MIN_COLS = 9
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "7d6d111ec55a31c9", "bytes_per_launch": 28537600,
+TRAFFIC = {"csrc_sha": "561cc2d271c9dde9", "bytes_per_launch": 28537984,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down"}
 
 
@@ -498,7 +498,26 @@ def measure_configs(q, torch, stream, device, reps, peak):
     calls = [lambda g=g, u=u: q.mul_mat_vec_fused(q.Q4_K, u, M, K, xq=xq, W_gate=g, bias=bu, gate_bias=bg,
                                                   out=yv(1, M), stream=stream) for g, u in pairs]
     record("q4_K gate+up 2x14336x4096 +biases", chain_time(calls), 2 * wb, len(pairs))
-    del ws
+    # an 8B-class FFN: gate+up 2x14336x4096 then down 4096x14336, the SwiGLU
+    # output handed over as fp32 (down quantizes it while staging) or as the
+    # q8_1 blocks the gate+up launch writes (qmv_mul_mat_vec_fused_q8_1)
+    downs = weights(q.Q4_K, K, M, len(pairs), 3_000_520)
+    wbd = K * q.row_bytes(q.Q4_K, M)
+    y14 = torch.empty((1, M), dtype=torch.float32, device=device)
+    yq14 = torch.empty((1, q.q8_1_bytes(M)), dtype=torch.uint8, device=device)
+    y4 = torch.empty((1, K), dtype=torch.float32, device=device)
+    calls = []
+    for (g, u), D in zip(pairs, downs):
+        calls += [lambda g=g, u=u: q.mul_mat_vec_fused(q.Q4_K, u, M, K, xq=xq, W_gate=g, out=y14, stream=stream),
+                  lambda D=D: q.mul_mat_vec_f32(q.Q4_K, D, K, M, y14, out=y4, stream=stream)]
+    record("q4_K ffn 14336: gate+up, down; fp32 hand-off", 2 * chain_time(calls), 2 * wb + wbd, len(pairs))
+    calls = []
+    for (g, u), D in zip(pairs, downs):
+        calls += [lambda g=g, u=u: q.mul_mat_vec_fused_q8_1(q.Q4_K, u, M, K, xq=xq, W_gate=g, want_y=False,
+                                                            out_q8_1=yq14, stream=stream),
+                  lambda D=D: q.mul_mat_vec(q.Q4_K, D, K, M, yq14, 1, out=y4, stream=stream)]
+    record("q4_K ffn 14336: gate+up, down; q8_1 hand-off", 2 * chain_time(calls), 2 * wb + wbd, len(pairs))
+    del ws, downs
     torch.cuda.empty_cache()
     # MoE: 8 experts of 14336x4096, 4 tokens, top-2 drawn without replacement;
     # the chain rotates among distinct expert sets

@@ -232,6 +232,26 @@ qmv_status qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate,
                                  const void *xq, const float *x, int64_t ldx, int ncols, const float *bias,
                                  const float *gate_bias, float *y, void *stream);
 
+/* qmv_mul_mat_vec_fused_q8_1: qmv_mul_mat_vec_fused of one column (ncols
+ * must be 1) whose result is also written as q8_1 blocks, ready to be the
+ * activations of the next GEMV: yq receives qmv_q8_1_bytes(M, 1) bytes, the
+ * blocks qmv_quantize_q8_1 would write for y with K = M (the 512-padding
+ * included, as zero blocks), bit for bit.  The pages quantize each
+ * activation vector in a pass of its own before the GEMV (mul_mat_vec_q
+ * page, section "激活的量化"); here the producing GEMV does it in its
+ * epilogue: every CTA owns whole 32-row blocks of y, keeps their values in
+ * shared memory and quantizes them once its warps are done, so the consumer
+ * reads 36 bytes per 32 values instead of 128 and needs no quantize pass.
+ * y (fp32 [M]) is optional: NULL writes only yq; otherwise y equals
+ * qmv_mul_mat_vec_fused's bit for bit.  yq must be 4-byte aligned; the other
+ * arguments, shapes and errors are those of qmv_mul_mat_vec_fused
+ * (QMV_ERR_NULL for yq NULL, QMV_ERR_NCOLS for ncols != 1).  A warp whose
+ * wait for its cluster partner's share of x ran out (qmv_device_fault, code
+ * 2) leaves NaN in its rows of y and a NaN scale in their blocks. */
+qmv_status qmv_mul_mat_vec_fused_q8_1(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K,
+                                      const void *xq, const float *x, int64_t ldx, int ncols, const float *bias,
+                                      const float *gate_bias, float *y, void *yq, void *stream);
+
 qmv_status qmv_mul_mat_vec_id_fused(int type, const void *W_up, const void *W_gate, int64_t n_expert,
                                     int64_t M, int64_t K, const void *xq, const float *x, int64_t ldx,
                                     const int32_t *ids, int n_tokens, int top_k, float *y,

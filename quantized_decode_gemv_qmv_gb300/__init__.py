@@ -28,7 +28,7 @@ EXPORTS = (
     "qmv_status_str", "qmv_version", "qmv_row_bytes", "qmv_q8_1_padded_k", "qmv_q8_1_bytes",
     "qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec", "qmv_mul_mat_vec_gate_up_swiglu",
     "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32", "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32",
-    "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_id_fused",
+    "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_fused_q8_1", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv", "qmv_read_bandwidth_probe",
     "qmv_set_early_warps", "qmv_set_early_delay", "qmv_debug_f32_withheld_share", "qmv_debug_trace",
@@ -85,6 +85,8 @@ def lib():
         L.qmv_mul_mat_vec_id_f32.argtypes = [_int, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _int, _vp, _vp,
                                              _vp]
         L.qmv_mul_mat_vec_fused.argtypes = [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _vp]
+        L.qmv_mul_mat_vec_fused_q8_1.argtypes = [_int, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _int, _vp, _vp, _vp, _vp,
+                                                 _vp]
         L.qmv_mul_mat_vec_id_fused.argtypes = [_int, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int,
                                                _vp, _vp, _vp, _vp, _vp, _vp]
         L.qmv_debug_subblock_sums.argtypes = [_int, _vp, _i64, _i64, _vp, _int, _vp, _vp]
@@ -103,6 +105,7 @@ def lib():
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
                      "qmv_mul_mat_vec_gate_up_swiglu_f32", "qmv_mul_mat_vec_id_f32", "qmv_mul_mat_vec_fused",
+                     "qmv_mul_mat_vec_fused_q8_1",
                      "qmv_mul_mat_vec_id_fused", "qmv_debug_subblock_sums",
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
                      "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
@@ -403,6 +406,36 @@ def mul_mat_vec_fused(qtype: int, W_up, M: int, K: int, xq=None, x=None, W_gate=
     _call("qmv_mul_mat_vec_fused", dev, stream, qtype, _ptr(W_up), _ptr(W_gate), M, K, pq, px, ldx, ncols,
           _ptr(bias), _ptr(gate_bias), _ptr(out))
     return out
+
+
+def mul_mat_vec_fused_q8_1(qtype: int, W_up, M: int, K: int, xq=None, x=None, W_gate=None, bias=None,
+                           gate_bias=None, out=None, out_q8_1=None, want_y=True, stream=None):
+    """mul_mat_vec_fused of one column whose result is also written as q8_1
+    blocks (uint8 [q8_1_bytes(M)], the next GEMV's activations): returns
+    (y [1][M] or None when want_y is False and out is None, yq)."""
+    import torch
+
+    act, pq, px, ldx, ncols = _activations(xq, x, K)
+    if ncols != 1:
+        raise ValueError("mul_mat_vec_fused_q8_1 takes one activation column")
+    _weights(W_up, "W_up", qtype, M, K)
+    if W_gate is not None:
+        _weights(W_gate, "W_gate", qtype, M, K)
+    for name, b in (("bias", bias), ("gate_bias", gate_bias)):
+        if b is not None:
+            _tensor(b, name, torch.float32, 4 * M)
+    if out is not None or want_y:
+        out = _out(out, "out", (1, M), W_up.device, 4 * M)
+    nq = _q8_1_bytes(M, 1)
+    if out_q8_1 is None:
+        out_q8_1 = torch.empty((1, nq), dtype=torch.uint8, device=W_up.device)
+    else:
+        _tensor(out_q8_1, "out_q8_1", torch.uint8, nq)
+    dev = _device_of((("W_up", W_up), ("W_gate", W_gate), act, ("bias", bias), ("gate_bias", gate_bias),
+                      ("out", out), ("out_q8_1", out_q8_1)), stream)
+    _call("qmv_mul_mat_vec_fused_q8_1", dev, stream, qtype, _ptr(W_up), _ptr(W_gate), M, K, pq, px, ldx, 1,
+          _ptr(bias), _ptr(gate_bias), _ptr(out), _ptr(out_q8_1))
+    return out, out_q8_1
 
 
 def mul_mat_vec_id_fused(qtype: int, W, n_expert: int, M: int, K: int, ids, xq=None, x=None, W_gate=None,

@@ -22,6 +22,9 @@ const void *gemv_tiles_fn_q6_K(int mode, int nc, int rw);
 const void *gemv_tiles_probe_fn_q4_0(int mode, int nc);
 const void *gemv_tiles_probe_fn_q4_K(int mode, int nc);
 const void *gemv_tiles_probe_fn_q6_K(int mode, int nc);
+const void *gemv_tiles_yq_fn_q4_0(int mode, bool probe);
+const void *gemv_tiles_yq_fn_q4_K(int mode, bool probe);
+const void *gemv_tiles_yq_fn_q6_K(int mode, bool probe);
 const void *gemv_generic_fn_q4_0(int mode);
 const void *gemv_generic_fn_q4_K(int mode);
 const void *gemv_generic_fn_q6_K(int mode);
@@ -44,6 +47,18 @@ const void *gemv_tiles_probe_fn(int type, int mode, int nc)
     case FMT_Q4_0: return gemv_tiles_probe_fn_q4_0(mode, nc);
     case FMT_Q4_K: return gemv_tiles_probe_fn_q4_K(mode, nc);
     case FMT_Q6_K: return gemv_tiles_probe_fn_q6_K(mode, nc);
+    default: return nullptr;
+    }
+}
+
+// The tile kernel of the plain or gate/up GEMV of one column that also writes
+// y as q8_1 blocks (qmv_mul_mat_vec_fused_q8_1), or its instrumented twin.
+const void *gemv_tiles_yq_fn(int type, int mode, bool probe)
+{
+    switch (type) {
+    case FMT_Q4_0: return gemv_tiles_yq_fn_q4_0(mode, probe);
+    case FMT_Q4_K: return gemv_tiles_yq_fn_q4_K(mode, probe);
+    case FMT_Q6_K: return gemv_tiles_yq_fn_q6_K(mode, probe);
     default: return nullptr;
     }
 }
@@ -352,11 +367,14 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     // mma_min columns on; the same choice for q8_1 and fp32 input, so the two
     // stay bit-identical
     const int mma_min = tu.mma_min_cols.load() > 0 ? tu.mma_min_cols.load() : MMA_MIN_COLS;
-    const bool mma = allow_mma && type == FMT_Q4_K && mode == MODE_PLAIN && nc_t >= mma_min;
+    const bool yq = p.yq != nullptr;  // y also as q8_1 blocks: one column, 4-row tiles, dp4a decode
+    const bool mma = !yq && allow_mma && type == FMT_Q4_K && mode == MODE_PLAIN && nc_t >= mma_min;
     int rw = 4;
     if (mma) rw = MMA_RW;
-    else if (tu.slice_units.load()) rw = 32 / std::max(4, std::min(16, pow2_at_least(tu.slice_units.load())));
-    const void *fn = mma ? gemv_tiles_mma_fn_q4_K(mode) : gemv_tiles_fn(type, mode, nc_t, rw);
+    else if (tu.slice_units.load() && !yq) rw = 32 / std::max(4, std::min(16, pow2_at_least(tu.slice_units.load())));
+    const void *fn = yq    ? gemv_tiles_yq_fn(type, mode, false)
+                     : mma ? gemv_tiles_mma_fn_q4_K(mode)
+                           : gemv_tiles_fn(type, mode, nc_t, rw);
     if (!fn && rw != 4 && !mma) {
         rw = 4;
         fn = gemv_tiles_fn(type, mode, nc_t, rw);
@@ -385,6 +403,18 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     const int64_t G = (p.M + rw - 1) / rw;
     int64_t gx = std::min(max_ctas, G);
     int64_t groups_per_cta = (G + gx - 1) / gx;
+    // q8_1 output: every CTA owns whole 32-row blocks of y and keeps their fp32
+    // values in shared memory until it quantizes them
+    const int64_t n_yblk = (p.M + 31) / 32;
+    size_t ybuf = 0;
+    if (yq) {
+        const int64_t blk_per_cta = (n_yblk + gx - 1) / gx;
+        groups_per_cta = blk_per_cta * (32 / rw);
+        p.ybuf_rows = static_cast<int>(blk_per_cta * 32);
+        p.yq_nb_pad = static_cast<int>((p.M + ROW_PAD - 1) / ROW_PAD * ROW_PAD / QK8_1);
+        p.yq_col_bytes = static_cast<int64_t>(p.yq_nb_pad) * Q8_1_BYTES;
+        ybuf = align_up(static_cast<size_t>(nc_t) * p.ybuf_rows * 4, 16);
+    }
     const bool is_moe = mode == MODE_MOE || mode == MODE_MOE_GATE;
     if (is_moe) {
         // the kernel shares the grid among the experts the ids pick (at most
@@ -403,7 +433,9 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     // bit-identical results).
     const size_t st_smem = static_smem(fn);
     const size_t fn_limit = std::min(dev.smem_limit, dev.smem_limit + SMEM_RESERVE - st_smem);
-    auto need = [&](int w, int st, size_t act) { return act + static_cast<size_t>(w) * (st * tb + warp_extra) + 128; };
+    auto need = [&](int w, int st, size_t act) {
+        return act + ybuf + static_cast<size_t>(w) * (st * tb + warp_extra) + 128;
+    };
     auto fit = [&](size_t budget, int &w, int &st) {
         w = max_wpc;
         st = stages;
@@ -453,8 +485,10 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     // fp32 input is quantized straight into the packed layout
     size_t act = packed;
     if (p.xf == nullptr && !mma && need(max_wpc, stages, packed + raw) <= budget) act = packed + raw;
+    const size_t act_staged = act;  // the q8_1 output's row buffer follows the staged activations
+    act += ybuf;
     const int wpc = max_wpc;
-    const size_t smem = need(wpc, stages, act);
+    const size_t smem = need(wpc, stages, act_staged);  // need() adds the row buffer
     if (ensure_smem_attr(dev, fn) != QMV_OK) return TilePlan::Error;
     if (occupancy(dev.dev, fn, cta_warps * 32, smem) <= 0) return TilePlan::Error;
     // fp32 input: clusters of CTAs share the quantization of the activations
@@ -503,9 +537,10 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
         p.early_delay = static_cast<int>(static_cast<int64_t>(ns) * dev.clock_khz / 1000000);
     }
     p.act_bytes = static_cast<uint32_t>(act);
-    p.raw_off = act > packed ? static_cast<uint32_t>(packed) : 0u;
+    p.raw_off = act_staged > packed ? static_cast<uint32_t>(packed) : 0u;
+    p.ybuf_off = static_cast<uint32_t>(act_staged);
     L.fn = fn;
-    L.probe = (!mma && rw == 4) ? gemv_tiles_probe_fn(type, mode, nc_t) : nullptr;
+    L.probe = yq ? gemv_tiles_yq_fn(type, mode, true) : (!mma && rw == 4) ? gemv_tiles_probe_fn(type, mode, nc_t) : nullptr;
     L.stream = true;
     L.rw = rw;
     L.cluster = cl;
@@ -984,6 +1019,47 @@ qmv_status qmv_mul_mat_vec_fused(int type, const void *W_up, const void *W_gate,
     p.bias = bias;
     p.gate_bias = gate_bias;
     p.y = y;
+    Launch L;
+    if ((s = plan_f32(type, W_gate ? MODE_GATE : MODE_PLAIN, dev, p, ncols, 1, L)) != QMV_OK) return s;
+    return launch(L, static_cast<cudaStream_t>(stream));
+}
+
+qmv_status qmv_mul_mat_vec_fused_q8_1(int type, const void *W_up, const void *W_gate, int64_t M, int64_t K,
+                                      const void *xq, const float *x, int64_t ldx, int ncols, const float *bias,
+                                      const float *gate_bias, float *y, void *yq, void *stream)
+{
+    if (!xq && !x) return QMV_ERR_NULL;
+    if (xq && x) return QMV_ERR_SHAPE;
+    if (!yq) return QMV_ERR_NULL;
+    qmv_status s = check_common(type, W_up, M, K, xq ? xq : static_cast<const void *>(x), y ? y : yq);
+    if (s != QMV_OK) return s;
+    if (reinterpret_cast<uintptr_t>(yq) % 4) return QMV_ERR_ALIGN;
+    if (gate_bias && !W_gate) return QMV_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(bias) % 4 || reinterpret_cast<uintptr_t>(gate_bias) % 4) return QMV_ERR_ALIGN;
+    if (ncols != 1) return QMV_ERR_NCOLS;
+    if (M > (int64_t(1) << 31)) return QMV_ERR_SHAPE;
+    if ((s = check_f32(type, W_up, W_gate, K, x ? ldx : K)) != QMV_OK) return s;
+    {
+        const void *Ws[2] = {W_up, W_gate};
+        if ((s = check_gemv_ranges(type, M, K, Ws, W_gate ? 2 : 1, 1, xq, x, ldx, ncols, y, y ? uint64_t(M) : 0u)) !=
+            QMV_OK)
+            return s;
+    }
+    QMV_RANGE(bias, uint64_t(M) * 4u);
+    QMV_RANGE(gate_bias, uint64_t(M) * 4u);
+    QMV_RANGE(yq, qmv_q8_1_bytes(M, 1));
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W_up, M, K, xq, ncols);
+    if (x) {
+        p.xf = x;
+        p.ldx = ldx;
+    }
+    p.W2 = static_cast<const uint8_t *>(W_gate);
+    p.bias = bias;
+    p.gate_bias = gate_bias;
+    p.y = y;
+    p.yq = static_cast<uint8_t *>(yq);
     Launch L;
     if ((s = plan_f32(type, W_gate ? MODE_GATE : MODE_PLAIN, dev, p, ncols, 1, L)) != QMV_OK) return s;
     return launch(L, static_cast<cudaStream_t>(stream));

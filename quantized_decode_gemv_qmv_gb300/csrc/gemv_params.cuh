@@ -15,7 +15,8 @@ struct GemvParams {
     const uint8_t *xq;   // q8_1 activations, column c at xq + c*xq_col_bytes
     const float *xf;     // fp32 activations quantized in place (tile kernel), column c at xf + c*ldx; or null
     int64_t ldx;
-    float *y;            // PLAIN/GATE: y[c*ldy + r]; MOE: y[(t*top_k + k)*M + r]
+    float *y;            // PLAIN/GATE: y[c*ldy + r] (nullable when yq is set); MOE: y[(t*top_k + k)*M + r]
+    uint8_t *yq;         // PLAIN/GATE (tile kernel): y quantized to q8_1 as well, column c at yq + c*yq_col_bytes (nullable)
     int32_t *dbg;        // DEBUG: per-sub-block int sums
     const int32_t *ids;  // MOE: [n_tokens][top_k]
     int32_t *status;     // MOE: number of invalid ids (nullable)
@@ -28,6 +29,7 @@ struct GemvParams {
     int64_t row_bytes;
     int64_t xq_col_bytes;
     int64_t expert_bytes;
+    int64_t yq_col_bytes;  // yq: bytes per column (yq_nb_pad blocks of 36 bytes)
     int64_t n_groups;    // tile kernel: ceil(M / rows per tile)
     int K;
     int ncols;           // active columns (PLAIN/GATE/DEBUG)
@@ -40,6 +42,9 @@ struct GemvParams {
     int early_delay;     // tile kernel: SM clock cycles from the CTA's start to its early requests (0: none)
     uint32_t act_bytes;  // tile kernel: shared bytes of the activation area
     uint32_t raw_off;    // tile kernel: offset of the raw q8_1 copy inside the activation area (0: none)
+    uint32_t ybuf_off;   // yq: offset of the CTA's fp32 rows of y inside the activation area
+    int ybuf_rows;       // yq: rows of that buffer per column (whole 32-row blocks)
+    int yq_nb_pad;       // yq: blocks per column, the 512-padding included
     unsigned long long *trace;  // diagnostics: per-CTA timestamps [entry, waited, staged, done] (nullable)
     int withhold;        // test only: the rank-1 CTA of each fp32-staging cluster keeps its share to itself
     unsigned long long withhold_wait_ns;  // test only: how long the rank-0 CTA then waits for that share

@@ -10,6 +10,8 @@ const void *gemv_tiles_fn_q4_0(int mode, int nc, int rw) { return tiles_kernel_f
 
 const void *gemv_tiles_probe_fn_q4_0(int mode, int nc) { return tiles_probe_kernel_fn<FMT_Q4_0>(mode, nc); }
 
+const void *gemv_tiles_yq_fn_q4_0(int mode, bool probe) { return tiles_yq_kernel_fn<FMT_Q4_0>(mode, probe); }
+
 const void *gemv_generic_fn_q4_0(int mode)
 {
     constexpr int F = FMT_Q4_0;

@@ -11,6 +11,8 @@ const void *gemv_tiles_fn_q4_K(int mode, int nc, int rw) { return tiles_kernel_f
 
 const void *gemv_tiles_probe_fn_q4_K(int mode, int nc) { return tiles_probe_kernel_fn<FMT_Q4_K>(mode, nc); }
 
+const void *gemv_tiles_yq_fn_q4_K(int mode, bool probe) { return tiles_yq_kernel_fn<FMT_Q4_K>(mode, probe); }
+
 const void *gemv_tiles_mma_fn_q4_K(int mode) { return tiles_mma_kernel_fn<FMT_Q4_K>(mode); }
 
 const void *gemv_generic_fn_q4_K(int mode)

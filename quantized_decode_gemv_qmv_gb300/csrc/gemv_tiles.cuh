@@ -45,10 +45,8 @@ constexpr int MOE_MAX_SLOTS = 256;  // n_tokens * top_k <= 8 * 32
 constexpr int MOE_COL_WEIGHT = 6;   // MoE grid split: an expert's work ~ 6 + the tokens (columns) it serves
 
 // Tile geometry for format F and RW rows per tile: UW = 32/RW units per tile
-// row (one per lane), the row segment SEG 16-byte pieces long.  Copies:
-// Q4_0 / Q4_K tiles row-wise (LPR = 32/RW lanes per row, NJ instructions
-// each, copy_row_pieces); Q6_K tiles as one run of pieces over the warp
-// (PER_LANE instructions per lane).  Rows are padded in shared memory (stride SS):
+// row (one per lane), the row segment SEG 16-byte pieces long, copied
+// row-wise (LPR = 32/RW lanes per row, NJ instructions each, copy_row_pieces).  Rows are padded in shared memory (stride SS):
 //   Q4_0 / Q4_K (144-byte units): SS/16 = 8/RW mod 8, so the 8 lanes of a
 //     128-bit read phase (RW rows of 8/RW units) hit distinct bank quads;
 //   Q6_K (210-byte units, RW = 4): SS = 1,696 bytes = 32 mod 128, which spreads
@@ -65,8 +63,6 @@ struct TileGeom {
     static_assert((UW * UNIT) % 16 == 0, "a tile row segment must be whole 16-byte pieces");
     static_assert(F != FMT_Q6_K || RW == 4, "Q6_K tiles are 4 rows x 8 super-blocks");
     static constexpr int SEG = UW * UNIT / 16;
-    static constexpr int PIECES = RW * SEG;
-    static constexpr int PER_LANE = (PIECES + 31) / 32;
     static constexpr int LPR = 32 / RW;                // row-wise copy: lanes per tile row
     static constexpr int NJ = (SEG + LPR - 1) / LPR;   // row-wise copy: instructions per lane
     static constexpr int SS = F == FMT_Q6_K ? UW * UNIT + 16
@@ -267,16 +263,59 @@ __device__ __forceinline__ uint32_t cluster_share_bytes(int n_all, uint32_t cran
 }
 
 // A warp whose activations never arrived: code 2 in the fault word, and NaN in
-// every output of its rows r0 .. r_end-1, so a bad result cannot pass for a
-// good one.  Out of line, so that the code the warp runs when the activations
-// do arrive stays as short as without it (inline, it made the step's launches
-// about 0.5 % slower on GB300).
+// every output of its rows r0 .. r_end-1 (y if given, and the CTA's buffer of
+// rows for the q8_1 output, whose blocks then carry a NaN scale), so a bad
+// result cannot pass for a good one.  Out of line, so that the code the warp
+// runs when the activations do arrive stays as short as without it (inline,
+// it made the step's launches about 0.5 % slower on GB300).
 static __device__ __noinline__ void give_up_rows(float *y, int64_t ldy, int ncols, int64_t r0, int64_t r_end, int lane,
-                                                 unsigned int *fault)
+                                                 unsigned int *fault, float *ybuf, int ybuf_rows, int64_t yrow0)
 {
     if (lane == 0 && fault) atomicOr(fault, FAULT_CLUSTER_STAGING);
     for (int64_t r = r0 + lane; r < r_end; r += 32)
-        for (int c = 0; c < ncols; ++c) y[(size_t)c * ldy + r] = __int_as_float(0x7fc00000);
+        for (int c = 0; c < ncols; ++c) {
+            if (y) y[(size_t)c * ldy + r] = __int_as_float(0x7fc00000);
+            if (ybuf) ybuf[c * ybuf_rows + (r - yrow0)] = __int_as_float(0x7fc00000);
+        }
+}
+
+// The q8_1 output (p.yq): after the CTA barrier, the CTA's fp32 rows in ybuf
+// (whole 32-row blocks from row yrow0, column c at ybuf + c*ybuf_rows) are
+// quantized with the arithmetic of the standalone quantizer (q8_1.cuh), 4
+// lanes per block, rows at and past M as zeros; the CTA holding the last block
+// also writes the padding blocks (all zero bytes, the quantization of zeros).
+// Every thread of the CTA takes part (the group reductions shuffle over whole
+// warps).
+__device__ __forceinline__ void store_rows_q8_1(const GemvParams &p, const float *ybuf, int64_t b0, int64_t b1,
+                                                int64_t n_blk)
+{
+    const int nb_cta = static_cast<int>(b1 - b0);
+    const int n_out = nb_cta + (b1 == n_blk && b1 > b0 ? p.yq_nb_pad - static_cast<int>(n_blk) : 0);
+    const int tasks = n_out * p.ncols * 4;
+    const int rounds = (tasks + blockDim.x - 1) / blockDim.x;
+    for (int rd = 0; rd < rounds; ++rd) {
+        const int t = rd * blockDim.x + threadIdx.x;
+        const bool ok = t < tasks;
+        const int tt = ok ? t : 0;
+        const int c = tt / (n_out * 4);
+        const int rem = tt - c * n_out * 4;
+        const int b = rem >> 2, j = rem & 3;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t row = (b0 + b) * 32 + 8 * j + i;
+            v[i] = (ok && b < nb_cta && row < p.M) ? ybuf[c * p.ybuf_rows + static_cast<int>(row - b0 * 32)] : 0.f;
+        }
+        uint32_t w0, w1, ds;
+        int sum, part;
+        q8_1_block_group4(v, w0, w1, ds, sum, part);
+        if (ok) {
+            uint32_t *o = reinterpret_cast<uint32_t *>(p.yq + (size_t)c * p.yq_col_bytes + (size_t)(b0 + b) * Q8_1_BYTES);
+            o[1 + 2 * j] = w0;
+            o[2 + 2 * j] = w1;
+            if (j == 0) o[0] = ds;
+        }
+    }
 }
 
 // One tile row's copy: lane kq of the row's LPR lanes copies its 16-byte
@@ -284,18 +323,17 @@ static __device__ __noinline__ void give_up_rows(float *y, int64_t ldy, int ncol
 // both the row segment and its shared copy), so a lane's addresses are one
 // base plus constant offsets and the copy costs one instruction per piece.
 // Only pieces below lim are copied (a partial last k-tile).  Each instruction
-// moves 16 LPR contiguous bytes of every row of the tile.  Used for the
-// 144-byte units of Q4_0 / Q4_K (on GB300 the step 1.020 -> 1.002 ms, the MoE
-// calls 5 % faster); Q6_K keeps the contiguous per-warp copy, since row-wise
-// its 32000x4096 launch was 2 % slower.
+// moves 16 LPR contiguous bytes of every row of the tile.  On GB300, against a
+// per-piece division of one run of pieces over the warp: Q4_0 / Q4_K (144-byte
+// units) the step 1.020 -> 1.002 ms and the MoE calls 5 % faster; Q6_K (with
+// each lane's first piece rotated to a line boundary) 4096x14336 11.40 -> 10.96
+// us and 5-8 columns 4-5 % faster, its 32000x4096 launch 2.6 % slower.
 template <int LPR, int SEG, int... J>
 __device__ __forceinline__ void copy_row_pieces(uint32_t dst, const uint8_t *src, int kq, int lim,
                                                 std::integer_sequence<int, J...>)
 {
-    constexpr int NJ = static_cast<int>(sizeof...(J));
     if (lim >= SEG)
-        ((((SEG % LPR) == 0 || J < NJ - 1 || kq + LPR * J < SEG) ? cp_async16_at<16 * LPR * J>(dst, src) : void()),
-         ...);
+        ((((J + 1) * LPR <= SEG || kq + LPR * J < SEG) ? cp_async16_at<16 * LPR * J>(dst, src) : void()), ...);
     else
         ((kq + LPR * J < lim ? cp_async16_at<16 * LPR * J>(dst, src) : void()), ...);
 }
@@ -304,7 +342,7 @@ __device__ __forceinline__ void copy_row_pieces(uint32_t dst, const uint8_t *src
 // the timeline stores (p.trace) and the withheld share (p.withhold).  The
 // ordinary kernels carry neither: the instructions would sit on the path from
 // the dependency wait to the first decode, which every launch pays.
-template <int F, int NC, int MODE, int RW, bool TC = false, bool PROBE = false>
+template <int F, int NC, int MODE, int RW, bool TC = false, bool PROBE = false, bool YQ = false>
 __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEBUG) ? 2 : 1)
     gemv_tiles_kernel(const GemvParams p)
 {
@@ -324,6 +362,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     constexpr int NM = (MODE == MODE_GATE || MODE == MODE_MOE_GATE) ? 2 : 1;  // matrices (up, gate)
     constexpr bool MMA = TC;  // tensor-core decode (gemv_mma.cuh): Q4_K, plain, up to 8 columns
     static_assert(!MMA || (F == FMT_Q4_K && MODE == MODE_PLAIN && NC == MMA_COLS), "tensor-core tiles: Q4_K plain");
+    static_assert(!YQ || (!MMA && (MODE == MODE_PLAIN || MODE == MODE_GATE)), "q8_1 output: plain or gate/up, dp4a");
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = p.dec_warps;  // warps that stream and decode; the others only help staging
@@ -505,11 +544,26 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 
     // every warp (of the grid; MoE: of the expert's CTAs) owns a contiguous,
     // balanced range of row groups (whole groups: a row's partial sums never
-    // leave the warp)
-    const int64_t gwarp = cta_index * nwarps + warp;
-    const int64_t wtot = cta_count * nwarps;
-    const int64_t g_begin = warp < nwarps ? (gwarp * p.n_groups) / wtot : 0;
-    const int64_t my_groups = warp < nwarps ? ((gwarp + 1) * p.n_groups) / wtot - g_begin : 0;
+    // leave the warp).  With the q8_1 output (PLAIN/GATE), every CTA owns whole
+    // 32-row blocks of y (blocks yb0 .. yb1-1 from row yrow0), its warps a
+    // balanced share of their row groups.
+    int64_t g_begin, my_groups, yb0 = 0, yb1 = 0, yrow0 = 0;
+    const int64_t n_yblk = (p.M + 31) / 32;
+    if constexpr (YQ) {
+        yb0 = cta_index * n_yblk / cta_count;
+        yb1 = (cta_index + 1) * n_yblk / cta_count;
+        yrow0 = yb0 * 32;
+        const int64_t cg0 = yb0 * (32 / RW);
+        const int64_t ng = min64(yb1 * (32 / RW), p.n_groups) - cg0;
+        g_begin = warp < nwarps ? cg0 + (warp * ng) / nwarps : 0;
+        my_groups = warp < nwarps ? cg0 + ((warp + 1) * ng) / nwarps - g_begin : 0;
+    } else {
+        const int64_t gwarp = cta_index * nwarps + warp;
+        const int64_t wtot = cta_count * nwarps;
+        g_begin = warp < nwarps ? (gwarp * p.n_groups) / wtot : 0;
+        my_groups = warp < nwarps ? ((gwarp + 1) * p.n_groups) / wtot - g_begin : 0;
+    }
+    float *const ybuf = reinterpret_cast<float *>(smem + p.ybuf_off);  // YQ only
     const int64_t total = my_groups * n_kt * NM;
 
     // this warp's ring of tile buffers (tensor-core decode: then its row-factor scratch)
@@ -528,14 +582,13 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         const int64_t rows_left = p.M - grow;
         const int lim = min(UW, U - ld_kt * UW) * UNIT / 16;  // valid pieces per tile row
         if constexpr (F == FMT_Q6_K) {
-            const uint32_t dst = ring + static_cast<uint32_t>(ld_buf * TB);
-#pragma unroll
-            for (int j = 0; j < G::PER_LANE; ++j) {
-                const int i = 32 * j + lane;
-                const int seg = i / SEG;
-                const int off = i - seg * SEG;
-                if (i < G::PIECES && off < lim && seg < rows_left)
-                    cp_async16(dst + seg * SS + off * 16, base + seg * rb + off * 16);
+            // each lane's first piece rotated so that every instruction covers
+            // one aligned 128-byte line of each row (1,680-byte row segments)
+            if (cr < rows_left) {
+                const uint8_t *rowp = base + cr * rb;
+                const int k0 = (ck - static_cast<int>(reinterpret_cast<uintptr_t>(rowp) >> 4)) & (G::LPR - 1);
+                copy_row_pieces<G::LPR, SEG>(ring + static_cast<uint32_t>(ld_buf * TB + cr * SS + k0 * 16),
+                                             rowp + k0 * 16, k0, lim, std::make_integer_sequence<int, G::NJ>{});
             }
         } else if (cr < rows_left) {
             copy_row_pieces<G::LPR, SEG>(ring + static_cast<uint32_t>(ld_buf * TB + cr * SS + ck * 16),
@@ -589,9 +642,15 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
             // A partner's share never arrived: this warp computes nothing
             // (give_up_rows), and leaves once its own weight copies have
             // landed.  Each warp decides for itself, so a share that lands
-            // just at the limit leaves every row either right or NaN.
-            give_up_rows(p.y, p.ldy, p.ncols, g_begin * RW, min64(p.M, (g_begin + my_groups) * RW), lane, p.fault);
+            // just at the limit leaves every row either right or NaN.  With
+            // the q8_1 output the warp stays for the CTA's final quantization.
+            give_up_rows(p.y, p.ldy, p.ncols, g_begin * RW, min64(p.M, (g_begin + my_groups) * RW), lane, p.fault,
+                         YQ ? ybuf : nullptr, p.ybuf_rows, yrow0);
             cp_async_wait(0);
+            if constexpr (YQ) {
+                __syncthreads();  // the other warps' rows (they meet the barrier after their loop)
+                store_rows_q8_1(p, ybuf, yb0, yb1, n_yblk);
+            }
             return;
         }
     } else {
@@ -707,12 +766,17 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
                         if (c >= n_active) break;
-                        if constexpr (MODE == MODE_PLAIN) {
-                            p.y[(size_t)c * p.ldy + row] = p.bias ? acc[0][c] + b_up : acc[0][c];
-                        } else if constexpr (MODE == MODE_GATE) {
-                            const float up = p.bias ? acc[0][c] + b_up : acc[0][c];
-                            const float gate = p.gate_bias ? acc[NM - 1][c] + b_gate : acc[NM - 1][c];
-                            p.y[(size_t)c * p.ldy + row] = up * silu_f32(gate);
+                        if constexpr (MODE == MODE_PLAIN || MODE == MODE_GATE) {
+                            float out;
+                            if constexpr (MODE == MODE_PLAIN) {
+                                out = p.bias ? acc[0][c] + b_up : acc[0][c];
+                            } else {
+                                const float up = p.bias ? acc[0][c] + b_up : acc[0][c];
+                                const float gate = p.gate_bias ? acc[NM - 1][c] + b_gate : acc[NM - 1][c];
+                                out = up * silu_f32(gate);
+                            }
+                            if (!YQ || p.y) p.y[(size_t)c * p.ldy + row] = out;
+                            if constexpr (YQ) ybuf[c * p.ybuf_rows + static_cast<int>(row - yrow0)] = out;
                         } else {
                             const int tok = s_tok[c];
                             const float v = MODE == MODE_MOE_GATE ? acc[0][c] * silu_f32(acc[NM - 1][c]) : acc[0][c];
@@ -742,6 +806,10 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         if (++cbuf == stages) cbuf = 0;
     }
     if (trace && lane == 0) atomicMax(trace + 5, global_timer_ns());
+    if constexpr (YQ) {
+        __syncthreads();  // every row of the CTA's blocks is in ybuf
+        store_rows_q8_1(p, ybuf, yb0, yb1, n_yblk);
+    }
 }
 
 // Kernel table of the tile path for one format (instantiated only in that
@@ -765,6 +833,20 @@ const void *tiles_probe_kernel_fn(int mode, int nc)
     if (mode == MODE_PLAIN && nc == 1) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_PLAIN, 4, false, true>);
     if (mode == MODE_PLAIN && nc == 2) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 2, MODE_PLAIN, 4, false, true>);
     if (mode == MODE_GATE && nc == 1) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_GATE, 4, false, true>);
+    return nullptr;
+}
+
+// The q8_1-output variants (YQ): plain and gate/up GEMV of one column, 4-row
+// tiles, dp4a decode; probe: their instrumented twins.
+template <int F>
+const void *tiles_yq_kernel_fn(int mode, bool probe)
+{
+    if (mode == MODE_PLAIN)
+        return probe ? reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_PLAIN, 4, false, true, true>)
+                     : reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_PLAIN, 4, false, false, true>);
+    if (mode == MODE_GATE)
+        return probe ? reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_GATE, 4, false, true, true>)
+                     : reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_GATE, 4, false, false, true>);
     return nullptr;
 }
 

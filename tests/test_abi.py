@@ -119,6 +119,16 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert fm(12, p, nul, 16, 4096, p, nul, 0, 0, nul, nul, p, nul) == 4
     assert fm(12, p, ctypes.c_void_p(0x1008), 16, 4096, p, nul, 0, 1, nul, nul, p, nul) == 5
     assert fm(9, p, nul, 16, 4096, p, nul, 0, 1, nul, nul, p, nul) == 2
+    # the q8_1-output form: yq required and 4-byte aligned, y optional, one column
+    fq = L.qmv_mul_mat_vec_fused_q8_1  # (type, W_up, W_gate, M, K, xq, x, ldx, ncols, b, gb, y, yq, s)
+    assert fq(12, p, nul, 16, 4096, p, nul, 0, 1, nul, nul, p, nul, nul) == 1
+    assert fq(12, p, nul, 16, 4096, nul, nul, 0, 1, nul, nul, nul, p, nul) == 1
+    assert fq(12, p, nul, 16, 4096, p, p, 4096, 1, nul, nul, nul, p, nul) == 3
+    assert fq(12, p, nul, 16, 4096, p, nul, 0, 1, nul, nul, nul, ctypes.c_void_p(0x1002), nul) == 5
+    assert fq(12, p, nul, 16, 4096, p, nul, 0, 2, nul, nul, nul, p, nul) == 4
+    assert fq(12, p, nul, 16, 4096, p, nul, 0, 1, nul, p, nul, p, nul) == 3
+    assert fq(14, p, nul, 16, 2304, p, nul, 0, 1, nul, nul, nul, p, nul) == 3
+    assert fq(9, p, nul, 16, 4096, p, nul, 0, 1, nul, nul, nul, p, nul) == 2
     im = L.qmv_mul_mat_vec_id_fused   # (type, W, W_gate, E, M, K, xq, x, ldx, ids, T, k, y, Ws, Wsg, ys, st, s)
     assert im(12, p, nul, 8, 16, 4096, nul, nul, 0, p, 4, 2, p, nul, nul, nul, nul, nul) == 1
     assert im(12, p, nul, 8, 16, 4096, p, p, 4096, p, 4, 2, p, nul, nul, nul, nul, nul) == 3
