@@ -401,26 +401,33 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
             }
             cluster_arrive_relaxed();
         }
-        if (!MMA && p.xf != nullptr) {
-            // This CTA's share of x's 32-value blocks (the blocks it will
-            // quantize), fetched into L2 before the dependency wait, so that
-            // the staging loads after it hit L2 instead of queueing for HBM.
-            // Safe even when the previous kernel writes x: L2 is where this
-            // GPU's global memory is coherent, so its stores update the lines
-            // (only L1 could go stale, and the staging loads bypass L1).
-            // Measured on GB300 with activations not in L2: step launches
-            // 0.7-6 % faster.
-            const int nblk = U * 8;
-            const int n_all = p.ncols * nblk;
-            const int b0 = static_cast<int>(static_cast<int64_t>(crank) * n_all / ncta);
-            const int b1 = static_cast<int>(static_cast<int64_t>(crank + 1) * n_all / ncta);
-            for (int b = b0 + static_cast<int>(threadIdx.x); b < b1; b += blockDim.x) {
-                const int c = b / nblk;
-                const float *a = p.xf + (size_t)c * p.ldx + (size_t)(b - c * nblk) * 32;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+    // This CTA's share of x's 32-value blocks (fp32 input: the blocks it will
+    // quantize), fetched into L2 before the dependency wait, so that the
+    // staging loads after it hit L2 instead of queueing for HBM.  Safe even
+    // when the previous kernel writes x: L2 is where this GPU's global memory
+    // is coherent, so its stores update the lines (only L1 could go stale,
+    // and the staging loads bypass L1).  Issued at entry where the early
+    // weight requests are held back (p.early_delay), else right after those
+    // requests.  Measured on GB300 with activations not in L2: the step 1.030
+    // -> 1.004 ms with the prefetch at entry, and qkv, gate+up and down a
+    // further 1 % faster with it after their early requests (o 7 % slower).
+    auto prefetch_x = [&]() {
+        if constexpr ((MODE == MODE_PLAIN || MODE == MODE_GATE) && !MMA) {
+            if (p.xf != nullptr) {
+                const int nblk = U * 8;
+                const int n_all = p.ncols * nblk;
+                const int b0 = static_cast<int>(static_cast<int64_t>(crank) * n_all / ncta);
+                const int b1 = static_cast<int>(static_cast<int64_t>(crank + 1) * n_all / ncta);
+                for (int b = b0 + static_cast<int>(threadIdx.x); b < b1; b += blockDim.x) {
+                    const int c = b / nblk;
+                    const float *a = p.xf + (size_t)c * p.ldx + (size_t)(b - c * nblk) * 32;
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+                }
             }
         }
-    }
+    };
+    if (p.early_delay > 0) prefetch_x();
 
     int n_active = p.ncols;
     int64_t row_base = 0;    // MoE: first row of this CTA's expert
@@ -571,33 +578,53 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         smem_u32(smem + p.act_bytes) + static_cast<uint32_t>(min(warp, nwarps - 1) * (stages * TB + WARP_EXTRA));
 
     // ---- copies: tile (group, k-tile, matrix) -> ring buffer, one group per tile ----
+    // Q4_0 / Q4_K: the loader walks its tiles incrementally: ld_row is this
+    // lane's row of the current group (matrix 0), advanced by one group's rows
+    // at the end of each group; the gate matrix sits a fixed distance dW from
+    // it (the step's launches 0.9-1.6 % faster than with the tile's address
+    // computed from its indices).  Q6_K keeps that computation: incrementally
+    // its 4096x14336 launch was 7 % slower.
+    const int cr = lane / G::LPR, ck = lane % G::LPR;  // row-wise copy: this lane's tile row and first piece
+    const uint8_t *ld_row = W0 + (row_base + g_begin * RW + cr) * rb;
+    const int64_t dW = NM == 2 ? static_cast<int64_t>(W1 - W0) : 0;
+    int64_t ld_rows_left = p.M - g_begin * RW - cr;  // > 0: this lane's row exists
+    const int lim_last = (U - (n_kt - 1) * UW) * UNIT / 16;  // valid pieces per row of the last k-tile
     int64_t ld_g = g_begin;
     int ld_kt = 0, ld_m = 0, ld_buf = 0;
     int64_t issued = 0;
-    const int cr = lane / G::LPR, ck = lane % G::LPR;  // row-wise copy: this lane's tile row and first piece
     auto issue_tile = [&]() {
-        const uint8_t *W = (NM == 2 && ld_m) ? W1 : W0;
-        const int64_t grow = ld_g * RW;  // first row of the group inside the matrix
-        const uint8_t *base = W + (row_base + grow) * rb + static_cast<int64_t>(ld_kt) * (UW * UNIT);
-        const int64_t rows_left = p.M - grow;
-        const int lim = min(UW, U - ld_kt * UW) * UNIT / 16;  // valid pieces per tile row
         if constexpr (F == FMT_Q6_K) {
             // each lane's first piece rotated so that every instruction covers
             // one aligned 128-byte line of each row (1,680-byte row segments)
-            if (cr < rows_left) {
+            const uint8_t *W = (NM == 2 && ld_m) ? W1 : W0;
+            const int64_t grow = ld_g * RW;  // first row of the group inside the matrix
+            const uint8_t *base = W + (row_base + grow) * rb + static_cast<int64_t>(ld_kt) * (UW * UNIT);
+            const int lim = min(UW, U - ld_kt * UW) * UNIT / 16;  // valid pieces per tile row
+            if (cr < p.M - grow) {
                 const uint8_t *rowp = base + cr * rb;
                 const int k0 = (ck - static_cast<int>(reinterpret_cast<uintptr_t>(rowp) >> 4)) & (G::LPR - 1);
                 copy_row_pieces<G::LPR, SEG>(ring + static_cast<uint32_t>(ld_buf * TB + cr * SS + k0 * 16),
                                              rowp + k0 * 16, k0, lim, std::make_integer_sequence<int, G::NJ>{});
             }
-        } else if (cr < rows_left) {
-            copy_row_pieces<G::LPR, SEG>(ring + static_cast<uint32_t>(ld_buf * TB + cr * SS + ck * 16),
-                                         base + cr * rb + ck * 16, ck, lim, std::make_integer_sequence<int, G::NJ>{});
+        } else {
+            const uint8_t *rowp = ld_row + static_cast<int64_t>(ld_kt) * (UW * UNIT) + ((NM == 2 && ld_m) ? dW : 0);
+            const int lim = ld_kt == n_kt - 1 ? lim_last : SEG;
+            if (ld_rows_left > 0)
+                copy_row_pieces<G::LPR, SEG>(ring + static_cast<uint32_t>(ld_buf * TB + cr * SS + ck * 16),
+                                             rowp + ck * 16, ck, lim, std::make_integer_sequence<int, G::NJ>{});
         }
         cp_async_commit();
         if (++ld_m == NM) {
             ld_m = 0;
-            if (++ld_kt == n_kt) { ld_kt = 0; ++ld_g; }
+            if (++ld_kt == n_kt) {
+                ld_kt = 0;
+                if constexpr (F == FMT_Q6_K) {
+                    ++ld_g;
+                } else {
+                    ld_row += RW * rb;
+                    ld_rows_left -= RW;
+                }
+            }
         }
         if (++ld_buf == stages) ld_buf = 0;
         ++issued;
@@ -617,6 +644,7 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     }
     if (warp < p.early_warps)
         while (issued < total && issued < p.pre_tiles) issue_tile();  // weights first
+    if (p.early_delay == 0) prefetch_x();
     if constexpr (!IS_MOE) pdl_wait();
     if (trace && threadIdx.x == 0) trace[1] = global_timer_ns();
     if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
