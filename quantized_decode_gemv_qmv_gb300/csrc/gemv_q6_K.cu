@@ -12,6 +12,8 @@ const void *gemv_tiles_probe_fn_q6_K(int mode, int nc) { return tiles_probe_kern
 
 const void *gemv_tiles_yq_fn_q6_K(int mode, bool probe) { return tiles_yq_kernel_fn<FMT_Q6_K>(mode, probe); }
 
+const void *gemv_tiles_rowrun_fn_q6_K(int mode, int nc) { return tiles_rowrun_kernel_fn<FMT_Q6_K>(mode, nc); }
+
 const void *gemv_generic_fn_q6_K(int mode)
 {
     constexpr int F = FMT_Q6_K;

@@ -327,7 +327,9 @@ __device__ __forceinline__ void store_rows_q8_1(const GemvParams &p, const float
 // per-piece division of one run of pieces over the warp: Q4_0 / Q4_K (144-byte
 // units) the step 1.020 -> 1.002 ms and the MoE calls 5 % faster; Q6_K (with
 // each lane's first piece rotated to a line boundary) 4096x14336 11.40 -> 10.96
-// us and 5-8 columns 4-5 % faster, its 32000x4096 launch 2.6 % slower.
+// us and 5-8 columns 4-5 % faster, its 32000x4096 launch 2.6 % slower -- that
+// one, two tiles per row group, takes the ROWRUN variant (whole warp on one
+// row, 512 bytes per instruction): 21.75 -> 20.94 us.
 template <int LPR, int SEG, int... J>
 __device__ __forceinline__ void copy_row_pieces(uint32_t dst, const uint8_t *src, int kq, int lim,
                                                 std::integer_sequence<int, J...>)
@@ -342,7 +344,7 @@ __device__ __forceinline__ void copy_row_pieces(uint32_t dst, const uint8_t *src
 // the timeline stores (p.trace) and the withheld share (p.withhold).  The
 // ordinary kernels carry neither: the instructions would sit on the path from
 // the dependency wait to the first decode, which every launch pays.
-template <int F, int NC, int MODE, int RW, bool TC = false, bool PROBE = false, bool YQ = false>
+template <int F, int NC, int MODE, int RW, bool TC = false, bool PROBE = false, bool YQ = false, bool ROWRUN = false>
 __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEBUG) ? 2 : 1)
     gemv_tiles_kernel(const GemvParams p)
 {
@@ -600,7 +602,20 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
             const int64_t grow = ld_g * RW;  // first row of the group inside the matrix
             const uint8_t *base = W + (row_base + grow) * rb + static_cast<int64_t>(ld_kt) * (UW * UNIT);
             const int lim = min(UW, U - ld_kt * UW) * UNIT / 16;  // valid pieces per tile row
-            if (cr < p.M - grow) {
+            if constexpr (ROWRUN) {
+                // the whole warp on one row at a time: 512 contiguous bytes per
+                // instruction, each lane's first piece rotated to a 512-byte block
+#pragma unroll
+                for (int r = 0; r < RW; ++r) {
+                    if (r < p.M - grow) {
+                        const uint8_t *rowp = base + r * rb;
+                        const int k0 = (lane - static_cast<int>(reinterpret_cast<uintptr_t>(rowp) >> 4)) & 31;
+                        copy_row_pieces<32, SEG>(ring + static_cast<uint32_t>(ld_buf * TB + r * SS + k0 * 16),
+                                                 rowp + k0 * 16, k0, lim,
+                                                 std::make_integer_sequence<int, (SEG + 31) / 32>{});
+                    }
+                }
+            } else if (cr < p.M - grow) {
                 const uint8_t *rowp = base + cr * rb;
                 const int k0 = (ck - static_cast<int>(reinterpret_cast<uintptr_t>(rowp) >> 4)) & (G::LPR - 1);
                 copy_row_pieces<G::LPR, SEG>(ring + static_cast<uint32_t>(ld_buf * TB + cr * SS + k0 * 16),
@@ -861,6 +876,18 @@ const void *tiles_probe_kernel_fn(int mode, int nc)
     if (mode == MODE_PLAIN && nc == 1) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_PLAIN, 4, false, true>);
     if (mode == MODE_PLAIN && nc == 2) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 2, MODE_PLAIN, 4, false, true>);
     if (mode == MODE_GATE && nc == 1) return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_GATE, 4, false, true>);
+    return nullptr;
+}
+
+// The row-run variant (ROWRUN) of the plain Q6_K GEMV of one column: tiles
+// copied one row at a time by the whole warp (the planner's choice for short
+// rows, where the stream rather than the decode bounds the launch).
+template <int F>
+const void *tiles_rowrun_kernel_fn(int mode, int nc)
+{
+    if constexpr (F == FMT_Q6_K)
+        if (mode == MODE_PLAIN && nc == 1)
+            return reinterpret_cast<const void *>(&gemv_tiles_kernel<F, 1, MODE_PLAIN, 4, false, false, false, true>);
     return nullptr;
 }
 
