@@ -61,7 +61,7 @@ MMA_MIN_COLS = 9
 
 # dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from one ncu
 # capture, valid only while the kernel sources hash to CSRC_SHA.
-TRAFFIC = {"csrc_sha": "171aeadeafac0efc", "bytes_per_launch": 28538272,
+TRAFFIC = {"csrc_sha": "f4382115bbc2e604", "bytes_per_launch": 28538720,
            "shape": "mean of the step's launch kinds qkv, o, gate+up, down"}
 
 
@@ -596,6 +596,9 @@ def run_gpu(args):
     out_rows = [3 * D_MODEL, D_MODEL, D_MODEL]
     yoff = np.concatenate([[0], np.cumsum(out_rows * N_LAYERS)])
     acts = [torch.empty((1, D_FF), dtype=torch.float32, device=device) for _ in range(N_LAYERS)]
+    # q8_1 hand-off: gate+up writes its SwiGLU output as q8_1 blocks, which down reads
+    actq = [torch.empty((1, q.q8_1_bytes(D_FF)), dtype=torch.uint8, device=device) for _ in range(N_LAYERS)]
+    handoff_q8_1 = args.handoff == "q8_1"
 
     def io_set():
         """Device input and output buffers of one step and their per-launch views."""
@@ -617,8 +620,13 @@ def run_gpu(args):
             q.mul_mat_vec_f32(Q4_K, W[0], 3 * D_MODEL, D_MODEL, xs[l][0], out=ys[l][0], stream=stream)
         elif name == "o":
             q.mul_mat_vec_f32(Q4_K, W[0], D_MODEL, D_MODEL, xs[l][1], out=ys[l][1], stream=stream)
+        elif name == "gate_up" and handoff_q8_1:
+            q.mul_mat_vec_fused_q8_1(Q4_K, W[1], D_FF, D_MODEL, x=xs[l][2], W_gate=W[0], out_q8_1=actq[l],
+                                     want_y=False, stream=stream)
         elif name == "gate_up":
             q.mul_mat_vec_gate_up_swiglu_f32(Q4_K, W[0], W[1], D_FF, D_MODEL, xs[l][2], out=acts[l], stream=stream)
+        elif handoff_q8_1:
+            q.mul_mat_vec(Q4_K, W[0], D_MODEL, D_FF, actq[l], 1, out=ys[l][2], stream=stream)
         else:
             q.mul_mat_vec_f32(Q4_K, W[0], D_MODEL, D_FF, acts[l], out=ys[l][2], stream=stream)
 
@@ -1020,6 +1028,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=6.0, help="CPU-baseline timing budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timing section")
+    ap.add_argument("--handoff", choices=["fp32", "q8_1"], default="fp32",
+                    help="how the SwiGLU output reaches the down projection in the step")
     ap.add_argument("--kernel-only", default=None,
                     help="profiling aid: only GEMV launches of one shape, step kind, or the MoE call (moe)")
     ap.add_argument("--launches", type=int, default=8)

@@ -51,6 +51,16 @@ qmv_status qmv_debug_subblock_sums(int type, const void *W, int64_t M, int64_t K
 qmv_status qmv_debug_f32_withheld_share(int type, const void *W, int64_t M, int64_t K, const float *x,
                                         int64_t ldx, int ncols, float *y, uint64_t wait_ns, void *stream);
 
+/* The same withheld share for qmv_mul_mat_vec_fused_q8_1 of one column
+ * (plain, fp32 input x of K contiguous values, no biases; y optional, yq
+ * required): the warps that give up write NaN to their rows of y, and every
+ * q8_1 block holding one of those rows gets a NaN scale (half 0x7e00); every
+ * other output is the value qmv_mul_mat_vec_fused_q8_1 computes.
+ * QMV_ERR_CONFIG as above; the argument errors of qmv_mul_mat_vec_fused_q8_1
+ * otherwise.  No counterpart in the pages. */
+qmv_status qmv_debug_f32_withheld_share_q8_1(int type, const void *W, int64_t M, int64_t K, const float *x,
+                                             float *y, void *yq, uint64_t wait_ns, void *stream);
+
 /* Timeline of the streaming GEMV launches, for measuring where a launch's
  * time goes.  While enabled, each of the next `slots` launches that have an
  * instrumented twin (any call of qmv.h whose launch takes one; other launches

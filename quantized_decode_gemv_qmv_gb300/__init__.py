@@ -31,7 +31,8 @@ EXPORTS = (
     "qmv_mul_mat_vec_fused", "qmv_mul_mat_vec_fused_q8_1", "qmv_mul_mat_vec_id_fused",
     "qmv_debug_subblock_sums", "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
     "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv", "qmv_read_bandwidth_probe",
-    "qmv_set_early_warps", "qmv_set_early_delay", "qmv_debug_f32_withheld_share", "qmv_debug_trace",
+    "qmv_set_early_warps", "qmv_set_early_delay", "qmv_debug_f32_withheld_share",
+    "qmv_debug_f32_withheld_share_q8_1", "qmv_debug_trace",
 )
 
 
@@ -101,6 +102,7 @@ def lib():
         L.qmv_read_bandwidth_probe.argtypes = [_vp, ctypes.c_size_t, _vp, _vp]
         L.qmv_describe_gemv.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.POINTER(LaunchInfo)]
         L.qmv_debug_f32_withheld_share.argtypes = [_int, _vp, _i64, _i64, _vp, _i64, _int, _vp, ctypes.c_uint64, _vp]
+        L.qmv_debug_f32_withheld_share_q8_1.argtypes = [_int, _vp, _i64, _i64, _vp, _vp, _vp, ctypes.c_uint64, _vp]
         L.qmv_debug_trace.argtypes = [_vp, _i64]
         for name in ("qmv_quantize_q8_1", "qmv_quantize_weights", "qmv_mul_mat_vec",
                      "qmv_mul_mat_vec_gate_up_swiglu", "qmv_mul_mat_vec_id", "qmv_mul_mat_vec_f32",
@@ -110,7 +112,7 @@ def lib():
                      "qmv_device_fault", "qmv_set_tuning", "qmv_set_stream_tuning", "qmv_set_pdl",
                      "qmv_set_checked", "qmv_set_mma_min_cols", "qmv_describe_gemv",
                      "qmv_read_bandwidth_probe", "qmv_set_early_warps", "qmv_set_early_delay", "qmv_debug_f32_withheld_share",
-                     "qmv_debug_trace"):
+                     "qmv_debug_f32_withheld_share_q8_1", "qmv_debug_trace"):
             getattr(L, name).restype = _int
         _lib = L
     return _lib
@@ -492,6 +494,25 @@ def debug_f32_withheld_share(qtype: int, W, M: int, K: int, x, wait_ns: int, out
     _call("qmv_debug_f32_withheld_share", dev, stream, qtype, _ptr(W), M, K, _ptr(x2), ldx, ncols, _ptr(out),
           ctypes.c_uint64(wait_ns))
     return out
+
+
+def debug_f32_withheld_share_q8_1(qtype: int, W, M: int, K: int, x, wait_ns: int, stream=None):
+    """Test only: mul_mat_vec_fused_q8_1 (plain, one column, fp32 x) with the
+    withheld share of debug_f32_withheld_share; returns (y, yq).  The rows of
+    the warps that give up come back NaN, and their q8_1 blocks with a NaN
+    scale (see include/qmv_debug.h)."""
+    import torch
+
+    x2, _ = _x2d(x, K)
+    if x2.shape[0] != 1 or not x2.is_contiguous():
+        raise ValueError("x must be one contiguous column")
+    _weights(W, "W", qtype, M, K)
+    y = torch.empty((1, M), dtype=torch.float32, device=W.device)
+    yq = torch.empty((1, _q8_1_bytes(M, 1)), dtype=torch.uint8, device=W.device)
+    dev = _device_of((("W", W), ("x", x2)), stream)
+    _call("qmv_debug_f32_withheld_share_q8_1", dev, stream, qtype, _ptr(W), M, K, _ptr(x2), _ptr(y), _ptr(yq),
+          ctypes.c_uint64(wait_ns))
+    return y, yq
 
 
 TRACE_MAX_CTAS = 1024

@@ -937,6 +937,36 @@ qmv_status qmv_debug_f32_withheld_share(int type, const void *W, int64_t M, int6
     return launch(L, static_cast<cudaStream_t>(stream));
 }
 
+qmv_status qmv_debug_f32_withheld_share_q8_1(int type, const void *W, int64_t M, int64_t K, const float *x, float *y,
+                                             void *yq, uint64_t wait_ns, void *stream)
+{
+    qmv_status s = check_common(type, W, M, K, x, y ? static_cast<void *>(y) : yq);
+    if (s != QMV_OK) return s;
+    if (!yq) return QMV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(yq) % 4) return QMV_ERR_ALIGN;
+    if (wait_ns < 1 || wait_ns > WAIT_LIMIT_NS) return QMV_ERR_SHAPE;
+    if (M > (int64_t(1) << 31)) return QMV_ERR_SHAPE;
+    if ((s = check_f32(type, W, nullptr, K, K)) != QMV_OK) return s;
+    if ((s = check_gemv_ranges(type, M, K, &W, 1, 1, nullptr, x, K, 1, y, y ? uint64_t(M) : 0u)) != QMV_OK) return s;
+    QMV_RANGE(yq, qmv_q8_1_bytes(M, 1));
+    DevInfo dev;
+    if ((s = device_info(dev)) != QMV_OK) return s;
+    GemvParams p = base_params(type, W, M, K, nullptr, 1);
+    p.xf = x;
+    p.ldx = K;
+    p.y = y;
+    p.yq = static_cast<uint8_t *>(yq);
+    Launch L;
+    if ((s = plan_f32(type, MODE_PLAIN, dev, p, 1, 1, L)) != QMV_OK) return s;
+    if (L.cluster < 2 || !L.probe) return QMV_ERR_CONFIG;
+    if ((s = ensure_smem_attr(dev, L.probe)) != QMV_OK) return s;
+    L.fn = L.probe;
+    L.probe = nullptr;
+    L.p.withhold = 1;
+    L.p.withhold_wait_ns = wait_ns;
+    return launch(L, static_cast<cudaStream_t>(stream));
+}
+
 qmv_status qmv_mul_mat_vec_gate_up_swiglu_f32(int type, const void *W_gate, const void *W_up, int64_t M, int64_t K,
                                               const float *x, int64_t ldx, int ncols, float *y, void *stream)
 {

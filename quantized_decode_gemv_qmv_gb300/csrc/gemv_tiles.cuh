@@ -264,8 +264,8 @@ __device__ __forceinline__ uint32_t cluster_share_bytes(int n_all, uint32_t cran
 
 // A warp whose activations never arrived: code 2 in the fault word, and NaN in
 // every output of its rows r0 .. r_end-1 (y if given, and the CTA's buffer of
-// rows for the q8_1 output, whose blocks then carry a NaN scale), so a bad
-// result cannot pass for a good one.  Out of line, so that the code the warp
+// rows for the q8_1 output, whose blocks then carry a NaN scale:
+// mark_nan_block_group4), so a bad result cannot pass for a good one.  Out of line, so that the code the warp
 // runs when the activations do arrive stays as short as without it (inline,
 // it made the step's launches about 0.5 % slower on GB300).
 static __device__ __noinline__ void give_up_rows(float *y, int64_t ldy, int ncols, int64_t r0, int64_t r_end, int lane,
@@ -277,6 +277,21 @@ static __device__ __noinline__ void give_up_rows(float *y, int64_t ldy, int ncol
             if (y) y[(size_t)c * ldy + r] = __int_as_float(0x7fc00000);
             if (ybuf) ybuf[c * ybuf_rows + (r - yrow0)] = __int_as_float(0x7fc00000);
         }
+}
+
+// A block holding a NaN (the rows of a warp that gave up, see give_up_rows)
+// gets a NaN scale, so that no consumer can take it for a good block: the
+// quantizer's amax would pass over the NaN (fmaxf returns the other operand)
+// and its code would not show it either.  Called like q8_1_block_group4, by
+// every lane of the warp, lanes 4g..4g+3 holding one block.
+__device__ __forceinline__ void mark_nan_block_group4(const float (&v)[8], uint32_t &ds)
+{
+    int bad = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bad |= v[i] != v[i] ? 1 : 0;
+    bad |= __shfl_xor_sync(0xffffffffu, bad, 1);
+    bad |= __shfl_xor_sync(0xffffffffu, bad, 2);
+    if (bad) ds = (ds & 0xffff0000u) | 0x7e00u;
 }
 
 // The q8_1 output (p.yq): after the CTA barrier, the CTA's fp32 rows in ybuf
@@ -309,6 +324,7 @@ __device__ __forceinline__ void store_rows_q8_1(const GemvParams &p, const float
         uint32_t w0, w1, ds;
         int sum, part;
         q8_1_block_group4(v, w0, w1, ds, sum, part);
+        mark_nan_block_group4(v, ds);
         if (ok) {
             uint32_t *o = reinterpret_cast<uint32_t *>(p.yq + (size_t)c * p.yq_col_bytes + (size_t)(b0 + b) * Q8_1_BYTES);
             o[1 + 2 * j] = w0;

@@ -97,6 +97,13 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert wh(14, p, 16, 2304, p, 2304, 1, p, 1000, nul) == 3
     assert wh(12, p, 16, 4096, p, 4096, 9, p, 1000, nul) == 4
     assert wh(12, ctypes.c_void_p(0x1008), 16, 4096, p, 4096, 1, p, 1000, nul) == 5
+    whq = L.qmv_debug_f32_withheld_share_q8_1
+    assert whq(12, p, 16, 4096, p, p, p, 0, nul) == 3
+    assert whq(12, p, 16, 4096, p, p, nul, 1000, nul) == 1
+    assert whq(12, p, 16, 4096, p, nul, nul, 1000, nul) == 1
+    assert whq(12, p, 16, 4096, p, p, ctypes.c_void_p(0x1002), 1000, nul) == 5
+    assert whq(14, p, 16, 2304, p, p, p, 1000, nul) == 3
+    assert whq(12, ctypes.c_void_p(0x1008), 16, 4096, p, p, p, 1000, nul) == 5
     # fused fp32-input calls: the tile kernel's shapes (Q4_0/Q4_K: K % 256, Q6_K: K % 2048), 16-byte aligned W
     assert L.qmv_mul_mat_vec_f32(14, p, 16, 2304, p, 2304, 1, p, nul) == 3
     assert L.qmv_mul_mat_vec_f32(2, p, 16, 96, p, 96, 1, p, nul) == 3

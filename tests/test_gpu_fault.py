@@ -91,3 +91,41 @@ def test_withheld_share_needs_an_instrumented_kernel(q):
         q.debug_f32_withheld_share(t, dev(W), M, K, dev(x), 1_000_000, out=y)
     assert e.value.status == 10
     assert np.all(host(y) == 7.0) and q.device_fault() == 0
+
+
+@pytest.mark.parametrize("t,M,K", [(oracle.Q4_K, 4096, 4096), (oracle.Q4_K, 1000, 2048), (oracle.Q6_K, 777, 2048)])
+def test_withheld_share_with_q8_1_output(q, t, M, K):
+    """The q8_1-output GEMV with the wait run out: NaN rows in y, a NaN scale
+    on every block holding one (the quantizer's amax alone would pass over
+    them), every other row and block as the ordinary call gives them, and the
+    next ordinary calls exact."""
+    W = oracle.quantize_rows(t, synthetic.weights_f32(2400 + M, M, K))
+    x = synthetic.activations_f32(2401 + M, 1, K, outlier_frac=0.01)
+    Wd, xd = dev(W), dev(x)
+    assert q.device_fault() == 0
+    y_ok, yq_ok = q.mul_mat_vec_fused_q8_1(t, Wd, M, K, x=xd)
+    y_ok, yq_ok = host(y_ok)[0], host(yq_ok)[0]
+    assert q.device_fault() == 0
+
+    y, yq = q.debug_f32_withheld_share_q8_1(t, Wd, M, K, xd, 1_000_000)
+    y, yq = host(y)[0], host(yq)[0]
+    assert q.device_fault() == 2
+    nan = np.isnan(y)
+    assert nan.any() and not nan.all()
+    assert np.array_equal(y[~nan].view(np.uint32), y_ok[~nan].view(np.uint32))
+    nb = (M + 31) // 32
+    blocks, blocks_ok = yq[: nb * 36].reshape(nb, 36), yq_ok[: nb * 36].reshape(nb, 36)
+    bad = np.zeros(nb, bool)
+    np.logical_or.at(bad, np.arange(M) // 32, nan)
+    assert np.array_equal(blocks[~bad], blocks_ok[~bad])
+    d = blocks[bad, 0:2].copy().view(np.float16)[:, 0]
+    assert np.all(np.isnan(d)), "a block holding a NaN row has a NaN scale"
+    assert np.array_equal(yq[nb * 36:], yq_ok[nb * 36:])  # the padding blocks
+    assert q.device_fault() == 0
+
+    for _ in range(2):
+        y2, yq2 = q.mul_mat_vec_fused_q8_1(t, Wd, M, K, x=xd)
+        assert np.array_equal(host(y2)[0].view(np.uint32), y_ok.view(np.uint32))
+        assert np.array_equal(host(yq2)[0], yq_ok)
+    assert q.device_fault() == 0
+    assert np.array_equal(yq_ok, oracle.quantize_q8_1(y_ok[None])[0])
