@@ -312,9 +312,10 @@ qmv_status qmv_set_stream_tuning(int type, int dec_warps, int pre_tiles);
 qmv_status qmv_set_early_warps(int type, int early_warps);
 
 /* Delay, in ns, between the start of a CTA and its early weight requests, for
- * launches of `type` in which every warp requests all of its tiles before the
- * dependency wait and the next kernel's CTA fits beside this one on the SM
- * (the 4096x4096 class of shapes).  Such a CTA typically starts just as the
+ * launches of `type` in which the next kernel's CTA fits beside this one on
+ * the SM and either every warp requests all of its tiles before the
+ * dependency wait (the 4096x4096 class of shapes) or the activations are fp32
+ * (the _f32 and fused calls given x).  Such a CTA typically starts just as the
  * kernel beside it passes its own dependency wait; holding the requests back
  * lets that kernel's activation loads reach the memory system first, while
  * the tiles still land long before this launch needs them.  ns: 1..100000

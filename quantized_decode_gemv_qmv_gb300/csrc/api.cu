@@ -538,9 +538,13 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     // CTA starts (see the kernel).  Measured on GB300: 4096x4096 Q4_K chained
     // 3.59 -> 3.00 us per call, the step's o launch 4.61 -> 4.29 us, no launch
     // slower; the same delay on launches that stream more than their rings hold
-    // made 14336x4096 and the Q6_K 4096x14336 launch 1-2 % slower.
+    // made 14336x4096 and the Q6_K 4096x14336 launch (q8_1 input) 1-2 %
+    // slower.  fp32-input launches take it too: their neighbours are mostly
+    // fp32-input launches, whose activation loads (4x the bytes, quantized on
+    // arrival) gain most from going first; the step 0.4 % faster, the qkv
+    // launch 7.28 -> 7.08 us (200 ns: 0.25 %; 600 ns: less than 400).
     p.early_delay = 0;
-    if (!is_moe && tiles_per_warp <= p.pre_tiles && tu.early_delay_ns.load() >= 0 &&
+    if (!is_moe && (tiles_per_warp <= p.pre_tiles || p.xf != nullptr) && tu.early_delay_ns.load() >= 0 &&
         occupancy(dev.dev, fn, cta_warps * 32, smem) >= 2) {
         const int ns = tu.early_delay_ns.load() > 0 ? tu.early_delay_ns.load() : EARLY_DELAY_NS;
         p.early_delay = static_cast<int>(static_cast<int64_t>(ns) * dev.clock_khz / 1000000);

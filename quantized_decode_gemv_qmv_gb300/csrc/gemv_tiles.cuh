@@ -417,7 +417,13 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
                 mbar_init(xbar, 1);
                 fence_mbar_init();  // visible to the partners before they pass the cluster wait below
             }
+            // Every CTA of the cluster runs (its shared memory may be written)
+            // once this wait returns.  The CTAs of a cluster start together, so
+            // it returns at once here, where the CTA has no copies in flight;
+            // after the dependency wait it sat on the path to the staging (the
+            // step 0.3 % slower on GB300).
             cluster_arrive_relaxed();
+            cluster_wait();
         }
     }
     // This CTA's share of x's 32-value blocks (fp32 input: the blocks it will
@@ -428,8 +434,9 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     // and the staging loads bypass L1).  Issued at entry where the early
     // weight requests are held back (p.early_delay), else right after those
     // requests.  Measured on GB300 with activations not in L2: the step 1.030
-    // -> 1.004 ms with the prefetch at entry, and qkv, gate+up and down a
-    // further 1 % faster with it after their early requests (o 7 % slower).
+    // -> 1.004 ms with the prefetch at entry; without the hold-back, qkv,
+    // gate+up and down a further 1 % faster with it after their early
+    // requests (o 7 % slower); with it, the step 0.6 % slower that way.
     auto prefetch_x = [&]() {
         if constexpr ((MODE == MODE_PLAIN || MODE == MODE_GATE) && !MMA) {
             if (p.xf != nullptr) {
@@ -678,7 +685,6 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
     if (p.early_delay == 0) prefetch_x();
     if constexpr (!IS_MOE) pdl_wait();
     if (trace && threadIdx.x == 0) trace[1] = global_timer_ns();
-    if (ncta > 1) cluster_wait();  // every CTA of the cluster runs: its shared memory may be written
     if (!MMA && ncta > 1 && threadIdx.x == 0)
         mbar_arrive_expect_tx(xbar, cluster_share_bytes<F>(p.ncols * p.units_per_row * 8, crank, ncta));
     if constexpr (IS_MOE)
