@@ -318,9 +318,12 @@ qmv_status qmv_set_early_warps(int type, int early_warps);
  * (the _f32 and fused calls given x).  Such a CTA typically starts just as the
  * kernel beside it passes its own dependency wait; holding the requests back
  * lets that kernel's activation loads reach the memory system first, while
- * the tiles still land long before this launch needs them.  ns: 1..100000
- * sets the delay, 0 restores the built-in default (400 ns, measured on
- * GB300), -1 turns it off.  Results are identical for every setting.
+ * the tiles still land long before this launch needs them; fp32-input
+ * launches so held back also request every warp's whole ring of tiles early.
+ * ns: 1..100000 sets the delay, 0 restores the built-in defaults (400 ns for
+ * q8_1 input, 700 ns for fp32 input, measured on GB300), -1 turns it off
+ * (fp32-input launches then request one tile per warp early).  Results are
+ * identical for every setting.
  * Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above.  (A tuning entry point of
  * this library; the pages have no counterpart.) */
 qmv_status qmv_set_early_delay(int type, int ns);

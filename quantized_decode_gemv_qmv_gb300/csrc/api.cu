@@ -95,8 +95,9 @@ constexpr int MAX_CLUSTER = 8;         // portable cluster size limit
 // plus one for the invalid ids, and gridDim.y is at most 65535
 constexpr int64_t MAX_EXPERTS = 65534;
 // Delay of the early weight requests of launches that request their whole
-// matrix early (plan_tiles).
+// matrix early (q8_1 input), and of launches with fp32 input (plan_tiles).
 constexpr int EARLY_DELAY_NS = 400;
+constexpr int EARLY_DELAY_F32_NS = 700;
 
 std::atomic<int> g_pdl{1};
 
@@ -112,7 +113,7 @@ struct Tuning {
     std::atomic<int> dec_warps{0}, pre_tiles{0};
     std::atomic<int> mma_min_cols{0};  // 0: MMA_MIN_COLS; 9: never
     std::atomic<int> early_warps{0};   // 0: every decoding warp requests its early tiles
-    std::atomic<int> early_delay_ns{0};  // 0: EARLY_DELAY_NS; -1: no delay
+    std::atomic<int> early_delay_ns{0};  // 0: EARLY_DELAY_NS / EARLY_DELAY_F32_NS; -1: no delay
 };
 Tuning g_tuning[3];
 
@@ -530,23 +531,32 @@ TilePlan plan_tiles(int type, int mode, const DevInfo &dev, GemvParams &p, int n
     const int64_t tiles_per_warp =
         (groups_per_cta + wpc - 1) / wpc * ((U + 32 / rw - 1) / (32 / rw)) *
         ((mode == MODE_GATE || mode == MODE_MOE_GATE) ? 2 : 1);
+    // Held-back early requests (see the kernel): where the next kernel's CTA
+    // can sit beside this one, and either every warp requests all of its
+    // tiles early or the activations are fp32, the early requests wait a few
+    // hundred ns after the CTA starts, so that the neighbour's activation
+    // loads reach the memory system first.  Measured on GB300:
+    // - whole matrix early (q8_1 input), EARLY_DELAY_NS: 4096x4096 Q4_K
+    //   chained 3.59 -> 3.00 us per call, no launch slower; on launches that
+    //   stream more than their rings hold (q8_1 input) 14336x4096 and Q6_K
+    //   4096x14336 went 1-5 % slower, so those keep none;
+    // - fp32 input, EARLY_DELAY_F32_NS, and then every warp requests its
+    //   whole ring early: their neighbours are mostly fp32-input launches,
+    //   whose activation loads (4x the bytes, quantized on arrival) gain most
+    //   from going first.  The step 0.996 -> 0.990 ms with the hold-back of
+    //   400 ns and one early tile per warp, 0.981 with the whole ring, 0.976
+    //   to 0.979 with the whole ring and 700 ns (500: 0.978, 900: 0.980, 1200:
+    //   0.988; the whole ring without the hold-back: slower).
+    const bool beside = !is_moe && occupancy(dev.dev, fn, cta_warps * 32, smem) >= 2;
+    const bool hold_f32 = beside && p.xf != nullptr && tu.early_delay_ns.load() >= 0;
     p.pre_tiles = tu.pre_tiles.load() > 0 ? std::min(stages, tu.pre_tiles.load())
-                                          : (tiles_per_warp <= stages ? stages : 1);
+                                          : ((tiles_per_warp <= stages || hold_f32) ? stages : 1);
     p.early_warps = tu.early_warps.load() > 0 ? tu.early_warps.load() : wpc;
-    // Where every warp requests all of its tiles early and the next kernel's
-    // CTA can sit beside this one, those requests wait EARLY_DELAY_NS after the
-    // CTA starts (see the kernel).  Measured on GB300: 4096x4096 Q4_K chained
-    // 3.59 -> 3.00 us per call, the step's o launch 4.61 -> 4.29 us, no launch
-    // slower; the same delay on launches that stream more than their rings hold
-    // made 14336x4096 and the Q6_K 4096x14336 launch (q8_1 input) 1-2 %
-    // slower.  fp32-input launches take it too: their neighbours are mostly
-    // fp32-input launches, whose activation loads (4x the bytes, quantized on
-    // arrival) gain most from going first; the step 0.4 % faster, the qkv
-    // launch 7.28 -> 7.08 us (200 ns: 0.25 %; 600 ns: less than 400).
     p.early_delay = 0;
-    if (!is_moe && (tiles_per_warp <= p.pre_tiles || p.xf != nullptr) && tu.early_delay_ns.load() >= 0 &&
-        occupancy(dev.dev, fn, cta_warps * 32, smem) >= 2) {
-        const int ns = tu.early_delay_ns.load() > 0 ? tu.early_delay_ns.load() : EARLY_DELAY_NS;
+    if (beside && (tiles_per_warp <= p.pre_tiles || p.xf != nullptr) && tu.early_delay_ns.load() >= 0) {
+        const int ns = tu.early_delay_ns.load() > 0 ? tu.early_delay_ns.load()
+                       : p.xf != nullptr              ? EARLY_DELAY_F32_NS
+                                                      : EARLY_DELAY_NS;
         p.early_delay = static_cast<int>(static_cast<int64_t>(ns) * dev.clock_khz / 1000000);
     }
     p.act_bytes = static_cast<uint32_t>(act);

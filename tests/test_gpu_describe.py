@@ -56,8 +56,11 @@ def test_geometry_is_plausible_and_shared_by_both_inputs(q, name, t, M, K, gate,
     assert 1 <= a["pre_tiles"] <= a["stages"] and a["cluster"] == 1
     assert 0 < a["smem"] <= 227 * 1024
     b = q.describe_gemv(t, M, K, ncols, gate_up=gate, fp32_input=True)
-    for k in ("tile_kernel", "rows_per_tile", "block", "stages", "dec_warps", "pre_tiles"):
+    for k in ("tile_kernel", "rows_per_tile", "block", "stages", "dec_warps"):
         assert a[k] == b[k], k
+    # how many tiles are requested before the dependency wait changes no result:
+    # an fp32-input launch held back requests its whole ring
+    assert b["pre_tiles"] in (a["pre_tiles"], b["stages"])
     assert b["cluster"] in (1, 2) and b["grid"] % b["cluster"] == 0
 
 
