@@ -54,7 +54,9 @@ def host(t):
 
 
 @pytest.mark.parametrize("t,M,K,ncols", [(oracle.Q4_K, 4096, 4096, 1), (oracle.Q4_K, 1003, 2048, 2),
-                                         (oracle.Q6_K, 517, 4096, 2), (oracle.Q4_0, 700, 1024, 1)])
+                                         (oracle.Q6_K, 517, 4096, 2), (oracle.Q4_0, 700, 1024, 1),
+                                         # long rows (the step's down projection has K = 11008)
+                                         (oracle.Q4_K, 1024, 11008, 1), (oracle.Q4_K, 777, 8192, 2)])
 def test_withheld_share_runs_the_wait_out(q, t, M, K, ncols):
     W = oracle.quantize_rows(t, synthetic.weights_f32(2200 + M, M, K))
     x = synthetic.activations_f32(2201 + M, ncols, K, outlier_frac=0.01)
@@ -93,7 +95,8 @@ def test_withheld_share_needs_an_instrumented_kernel(q):
     assert np.all(host(y) == 7.0) and q.device_fault() == 0
 
 
-@pytest.mark.parametrize("t,M,K", [(oracle.Q4_K, 4096, 4096), (oracle.Q4_K, 1000, 2048), (oracle.Q6_K, 777, 2048)])
+@pytest.mark.parametrize("t,M,K", [(oracle.Q4_K, 4096, 4096), (oracle.Q4_K, 1000, 2048), (oracle.Q6_K, 777, 2048),
+                                   (oracle.Q4_K, 1024, 11008)])
 def test_withheld_share_with_q8_1_output(q, t, M, K):
     """The q8_1-output GEMV with the wait run out: NaN rows in y, a NaN scale
     on every block holding one (the quantizer's amax alone would pass over
