@@ -321,9 +321,15 @@ qmv_status qmv_set_early_warps(int type, int early_warps);
  * the tiles still land long before this launch needs them; fp32-input
  * launches so held back also request every warp's whole ring of tiles early.
  * ns: 1..100000 sets the delay, 0 restores the built-in defaults (400 ns for
- * q8_1 input, 700 ns for fp32 input, measured on GB300), -1 turns it off
- * (fp32-input launches then request one tile per warp early).  Results are
- * identical for every setting.
+ * q8_1 input, 700 ns for fp32 input, measured on GB300 with the library's
+ * GEMVs back to back on one stream), -1 turns it off (fp32-input launches
+ * then request one tile per warp early).  The defaults assume that the
+ * kernel before this one on the stream is another GEMV of this library, so
+ * that its CTAs start beside it; after a kernel launched without
+ * programmatic dependent launch the CTAs start only once it has finished,
+ * and the delay then only postpones the first tiles (about the delay per
+ * launch): turn it off for such a sequence.  Results are identical for
+ * every setting.
  * Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above.  (A tuning entry point of
  * this library; the pages have no counterpart.) */
 qmv_status qmv_set_early_delay(int type, int ns);
