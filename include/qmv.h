@@ -327,9 +327,13 @@ qmv_status qmv_set_early_warps(int type, int early_warps);
  * kernel before this one on the stream is another GEMV of this library, so
  * that its CTAs start beside it; after a kernel launched without
  * programmatic dependent launch the CTAs start only once it has finished,
- * and the delay then only postpones the first tiles (about the delay per
- * launch): turn it off for such a sequence.  Results are identical for
- * every setting.
+ * and the delay then only postpones the first tiles: measured on GB300, a
+ * Q4_K fp32-input GEMV right after a PyTorch elementwise kernel took 11.82
+ * instead of 10.29 us at 12288x4096, 8.55 instead of 7.57 at 4096x4096 and
+ * 12.81 instead of 11.74 at 4096x11008 with the defaults; back to back it
+ * took 7.17 instead of 7.31, 4.42 instead of 4.63 and 8.95 instead of 8.86.
+ * Turn it off where the GEMVs mostly follow other kernels.  Results are
+ * identical for every setting.
  * Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above.  (A tuning entry point of
  * this library; the pages have no counterpart.) */
 qmv_status qmv_set_early_delay(int type, int ns);
