@@ -323,17 +323,20 @@ qmv_status qmv_set_early_warps(int type, int early_warps);
  * ns: 1..100000 sets the delay, 0 restores the built-in defaults (400 ns for
  * q8_1 input, 700 ns for fp32 input, measured on GB300 with the library's
  * GEMVs back to back on one stream), -1 turns it off (fp32-input launches
- * then request one tile per warp early).  The defaults assume that the
- * kernel before this one on the stream is another GEMV of this library, so
- * that its CTAs start beside it; after a kernel launched without
- * programmatic dependent launch the CTAs start only once it has finished,
- * and the delay then only postpones the first tiles: measured on GB300, a
- * Q4_K fp32-input GEMV right after a PyTorch elementwise kernel took 11.82
- * instead of 10.29 us at 12288x4096, 8.55 instead of 7.57 at 4096x4096 and
- * 12.81 instead of 11.74 at 4096x11008 with the defaults; back to back it
- * took 7.17 instead of 7.31, 4.42 instead of 4.63 and 8.95 instead of 8.86.
- * Turn it off where the GEMVs mostly follow other kernels.  Results are
- * identical for every setting.
+ * then request one tile per warp early).  The hold-back pays only while the
+ * kernel before this one on the stream still runs (another GEMV of this
+ * library, which lets this launch start early); where the CTA's last warp
+ * neither decodes nor requests tiles early, it waits for that kernel at once
+ * and ends the hold-back as soon as the wait returns.  After a kernel
+ * launched without programmatic dependent launch the CTAs start only once it
+ * has finished, and what remains of the hold-back and the fuller early
+ * requests still costs: measured on GB300, a Q4_K fp32-input GEMV right
+ * after a PyTorch elementwise kernel took 11.14 instead of 10.22 us at
+ * 12288x4096, 7.85 instead of 7.45 at 4096x4096 and 12.25 instead of 11.70
+ * at 4096x11008 with the defaults (without the early end: 11.82, 8.55,
+ * 12.81); back to back 7.28, 4.37 and 9.01 us instead of 7.34, 4.62 and
+ * 8.88.  Turn it off where the GEMVs mostly follow other kernels.  Results
+ * are identical for every setting.
  * Returns QMV_ERR_TYPE / QMV_ERR_SHAPE as above.  (A tuning entry point of
  * this library; the pages have no counterpart.) */
 qmv_status qmv_set_early_delay(int type, int ns);

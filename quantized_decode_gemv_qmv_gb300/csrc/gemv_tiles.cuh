@@ -675,9 +675,35 @@ __global__ void __launch_bounds__(TILE_MAX_THREADS, (NC == 1 && MODE != MODE_DEB
         // back briefly (p.early_delay), so that the neighbour's activation
         // loads reach the memory system first; the tiles still land long
         // before this launch needs them.  Bounded by the clock alone.
+        // That neighbour exists only while the kernel before this one on the
+        // stream still runs (a GEMV of this library, which lets this launch
+        // start early).  So the CTA's last warp, where it neither decodes nor
+        // requests tiles early, waits for that kernel at once and raises a
+        // flag in shared memory (in the slack after the mbarrier) when the
+        // wait returns: after a kernel that was already done when this CTA
+        // started, the hold-back ends at once instead of only postponing the
+        // first tiles.
         if (p.early_delay > 0) {
+            const uint32_t flag = xbar + 8;
+            const int last = static_cast<int>(blockDim.x >> 5) - 1;
+            const bool sentinel = last >= nwarps && last >= p.early_warps;
+            if (sentinel) {
+                if (threadIdx.x == 0) asm volatile("st.volatile.shared.u32 [%0], 0;" ::"r"(flag) : "memory");
+                __syncthreads();
+                if (warp == last) {
+                    pdl_wait();
+                    if (lane == 0) asm volatile("st.volatile.shared.u32 [%0], 1;" ::"r"(flag) : "memory");
+                }
+            }
             const long long c0 = clock64();
-            while (clock64() - c0 < p.early_delay) __nanosleep(64);
+            while (clock64() - c0 < p.early_delay) {
+                if (sentinel) {
+                    uint32_t done;
+                    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(done) : "r"(flag) : "memory");
+                    if (done) break;
+                }
+                __nanosleep(64);
+            }
         }
     }
     if (warp < p.early_warps)
